@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Benchmark of batch-invariant RMSNorm forward + backward on GB300.
+
+One step = the whole hot path over one batch of the workload in one physical
+layout: rmsnorm_fwd on every call, rmsnorm_dweight_begin, rmsnorm_bwd_dx
+(dx fused with the dweight contribution) on every call, dweight_finalize.
+Inputs are resident in HBM when the timed region starts; L2 is flushed
+(256 MB write) before every timed step; each step is timed with CUDA events
+on the launching stream.  `value` is active tokens per second; the roofline
+object reports the dominant kernel (the fused backward) against the measured
+HBM copy bandwidth.  `e2e` is the same metric through the public API with
+host buffers: plans built on the host, inputs copied in from pinned memory
+and y, dx, dweight copied back, all inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1] [--layout full]
+  python bench.py --impl reference ...   # the FP64 oracle on host cores (reported baseline)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "RMSNorm fwd+bwd tokens/s and HBM GB/s (% of roofline), bitwise across layouts"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c1")
+    ap.add_argument("--layout", default=None, help="headline layout (default: the workload's)")
+    ap.add_argument("--all-layouts", action="store_true", help="also time every layout cell")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_desc(wl, lay_name, n_phys):
+    heads = "x".join(str(h) for h in wl.heads)
+    return (f"{wl.name}: hidden={wl.hidden}, heads={heads}, {len(wl.lengths)} samples, "
+            f"{wl.n_tokens} active tokens, layout={lay_name} ({n_phys} physical token slots)")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+class Step:
+    """Device-resident buffers of one layout and the launch sequence of one step."""
+
+    def __init__(self, wl, lay, x_log, dy_log, w, rpt, device):
+        import torch
+        import invariant_rmsnorm_fwd_gb300 as rb
+        self.rb = rb
+        H = wl.hidden
+        self.H, self.rpt, self.eps = H, rpt, wl.eps
+        self.w = w
+        self.calls = []
+        for tok in lay.calls:
+            cl = rb.call_layout(tok, rpt, lay.n_logical_tokens, device=device)
+            tid = cl.tok_id.long()
+            act = tid >= 0
+            xp = torch.zeros((tok.size, rpt, H), dtype=torch.bfloat16, device=device)
+            dp = torch.zeros_like(xp)
+            xp[act] = x_log[tid[act]]
+            dp[act] = dy_log[tid[act]]
+            self.calls.append((cl, xp, dp, torch.empty_like(xp), torch.empty_like(xp)))
+        self.ws = rb.DweightWorkspace(wl.n_tokens * rpt, H, device=device)
+        self.dw = torch.empty(H, dtype=torch.float32, device=device)
+        self.n_active = wl.n_tokens
+        self.bwd_events = []
+
+    def run(self, stream, time_bwd=False):
+        import torch
+        rb = self.rb
+        for cl, xp, dp, yp, dxp in self.calls:
+            rb.rmsnorm_fwd(xp, self.w, cl, self.eps, y=yp, stream=stream)
+        self.ws.begin(stream)
+        for cl, xp, dp, yp, dxp in self.calls:
+            if time_bwd:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            rb.rmsnorm_bwd_dx(xp, self.w, dp, cl, self.eps, dx=dxp, workspace=self.ws, stream=stream)
+            if time_bwd:
+                e1.record(stream)
+                self.bwd_events.append((e0, e1))
+        self.ws.finalize(self.dw, stream)
+
+    def time_fwd_only(self, stream):
+        import torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for cl, xp, dp, yp, dxp in self.calls:
+            self.rb.rmsnorm_fwd(xp, self.w, cl, self.eps, y=yp, stream=stream)
+        e1.record(stream)
+        return e0, e1
+
+    def gather(self, n_tok):
+        import torch
+        y = torch.empty((n_tok, self.rpt, self.H), dtype=torch.bfloat16, device=self.dw.device)
+        dx = torch.empty_like(y)
+        for cl, xp, dp, yp, dxp in self.calls:
+            tid = cl.tok_id.long()
+            act = tid >= 0
+            y[tid[act]] = yp[act]
+            dx[tid[act]] = dxp[act]
+        return y, dx, self.dw.clone()
+
+
+def time_steps(step, stream, steps, warmup, flush, dist=None, time_bwd=False):
+    import torch
+    for _ in range(warmup):
+        step.run(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    times = []
+    step.bwd_events = []
+    for _ in range(steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step.run(stream, time_bwd=time_bwd)
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ms = [a.elapsed_time(b) for a, b in times]
+    bwd_ms = [a.elapsed_time(b) for a, b in step.bwd_events]
+    return ms, bwd_ms
+
+
+def e2e_steps(wl, lay, x_log_host, dy_log_host, w, rpt, steps, warmup, device):
+    """Public API with host buffers: per step, build plans, copy inputs in from pinned
+    memory, run, copy y/dx/dweight back.  Returns (ms per step, h2d bytes, d2h bytes)."""
+    import torch
+    import invariant_rmsnorm_fwd_gb300 as rb
+    H = wl.hidden
+    stream = torch.cuda.current_stream()
+    # pinned physical host buffers per call (the caller's own data, laid out physically)
+    host = []
+    for tok in lay.calls:
+        act = tok >= 0
+        xh = torch.zeros((tok.size, rpt, H), dtype=torch.bfloat16).pin_memory()
+        dh = torch.zeros_like(xh).pin_memory()
+        idx = torch.as_tensor(tok[act]).long()
+        xh[torch.as_tensor(act)] = x_log_host[idx]
+        dh[torch.as_tensor(act)] = dy_log_host[idx]
+        host.append((tok, xh, dh, torch.empty_like(xh).pin_memory(), torch.empty_like(xh).pin_memory()))
+    dev = [(torch.empty(xh.shape, dtype=torch.bfloat16, device=device),
+            torch.empty(xh.shape, dtype=torch.bfloat16, device=device),
+            torch.empty(xh.shape, dtype=torch.bfloat16, device=device),
+            torch.empty(xh.shape, dtype=torch.bfloat16, device=device)) for _, xh, _, _, _ in host]
+    ws = rb.DweightWorkspace(wl.n_tokens * rpt, H, device=device)
+    dw_d = torch.empty(H, dtype=torch.float32, device=device)
+    dw_h = torch.empty(H, dtype=torch.float32).pin_memory()
+    h2d = d2h = 0
+
+    def one():
+        nonlocal h2d, d2h
+        h2d = d2h = 0
+        cls = []
+        for (tok, xh, dh, yh, dxh), (xd, dd, yd, dxd) in zip(host, dev):
+            cl = rb.call_layout(tok, rpt, lay.n_logical_tokens, device=device)
+            h2d += tok.nbytes + (cl.plan.numel() if cl.plan is not None else 0)
+            xd.copy_(xh, non_blocking=True)
+            dd.copy_(dh, non_blocking=True)
+            h2d += xh.numel() * 2 * 2
+            rb.rmsnorm_fwd(xd, w, cl, wl.eps, y=yd, stream=stream)
+            cls.append(cl)
+        ws.begin(stream)
+        for cl, (tok, xh, dh, yh, dxh), (xd, dd, yd, dxd) in zip(cls, host, dev):
+            rb.rmsnorm_bwd_dx(xd, w, dd, cl, wl.eps, dx=dxd, workspace=ws, stream=stream)
+        ws.finalize(dw_d, stream)
+        for (tok, xh, dh, yh, dxh), (xd, dd, yd, dxd) in zip(host, dev):
+            yh.copy_(yd, non_blocking=True)
+            dxh.copy_(dxd, non_blocking=True)
+            d2h += yd.numel() * 2 * 2
+        dw_h.copy_(dw_d, non_blocking=True)
+        d2h += H * 4
+        torch.cuda.synchronize()
+
+    for _ in range(warmup):
+        one()
+    ts = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        one()
+        ts.append((time.perf_counter() - t0) * 1e3)
+    return statistics.median(ts), h2d, d2h
+
+
+def cpu_baseline(wl, x_log, dy_log, w, rpt, seconds):
+    """The FP64 oracle as it stands (single-threaded C) on a bounded sample of rows."""
+    import oracle
+    H = wl.hidden
+    xr = x_log.reshape(-1, H)
+    dr = dy_log.reshape(-1, H)
+    n = xr.shape[0]
+    chunk = max(1, min(n, (1 << 22) // H))
+    done = 0
+    t0 = time.perf_counter()
+    r0 = 0
+    while time.perf_counter() - t0 < seconds:
+        r1 = min(n, r0 + chunk)
+        xs, ds = xr[r0:r1], dr[r0:r1]
+        oracle.forward(xs, w, wl.eps)
+        oracle.backward(xs, w, ds, wl.eps)
+        done += r1 - r0
+        r0 = 0 if r1 >= n else r1
+    dt = time.perf_counter() - t0
+    tokens = done / rpt
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} logical rows of hidden {H} (fwd + bwd incl. dweight, FP64 C, "
+                      f"single thread) in {dt:.1f} s, cycled over the first rows of the workload"}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import torch
+    import synth
+    import invariant_rmsnorm_fwd_gb300 as rb
+    from invariant_rmsnorm_fwd_gb300 import layout as L, harness
+
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist = tdist
+
+    wl = synth.config(args.config)
+    lay_name = args.layout or wl.headline
+    rpt_list = list(wl.heads)
+    hbm_peak, peak_kind = measured_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    steps_data = []
+    for hs, rpt in enumerate(rpt_list):
+        n_rows = wl.n_tokens * rpt
+        x = synth.logical_tensor(wl, synth.TAG_X, n_rows, wl.x_std, hs, device=device).reshape(wl.n_tokens, rpt, wl.hidden)
+        dy = synth.logical_tensor(wl, synth.TAG_DY, n_rows, wl.dy_std, hs, device=device).reshape(wl.n_tokens, rpt, wl.hidden)
+        w = synth.weight(wl, hs, device=device)
+        steps_data.append((rpt, x, dy, w))
+
+    lays = L.workload_layouts(wl, kinds=[lay_name])
+    lay = lays[lay_name]
+    step_objs = [Step(wl, lay, x, dy, w, rpt, device) for rpt, x, dy, w in steps_data]
+
+    class Multi:
+        def __init__(self, steps):
+            self.steps = steps
+            self.bwd_events = []
+
+        def run(self, stream, time_bwd=False):
+            for s in self.steps:
+                s.bwd_events = []
+                s.run(stream, time_bwd)
+            self.bwd_events = [e for s in self.steps for e in s.bwd_events]
+
+    multi = Multi(step_objs)
+    clocks = ClockSampler(local)
+    launches0 = rb.kernel_launches()
+    clocks.start()
+    ms, bwd_ms = time_steps(multi, stream, args.steps, args.warmup, flush, dist, time_bwd=True)
+    clk = clocks.stop()
+    launches = (rb.kernel_launches() - launches0) // (args.steps + args.warmup)
+    ms_step = statistics.mean(ms)
+    if dist is not None:
+        t = torch.tensor([ms_step], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    H = wl.hidden
+    heff = H * sum(rpt_list)
+    n_act = wl.n_tokens
+    alg_step = 10.0 * heff * n_act                  # bytes: fwd x+y, bwd x+dy+dx (bf16)
+    bwd_calls = len(lay.calls) * len(rpt_list)
+    bwd_per_launch_ms = statistics.mean(bwd_ms) if bwd_ms else float("nan")
+    alg_bwd_launch = 6.0 * heff * n_act / bwd_calls
+    achieved_bwd = alg_bwd_launch / (bwd_per_launch_ms * 1e-3) / 1e9
+    tokens_per_s = n_act / (ms_step * 1e-3) * world
+
+    # forward alone, for the record
+    fwd_ms = []
+    for _ in range(max(3, args.steps // 2)):
+        flush.fill_(1)
+        evs = [s.time_fwd_only(stream) for s in step_objs]
+        torch.cuda.synchronize()
+        fwd_ms.append(sum(a.elapsed_time(b) for a, b in evs))
+    fwd_gbs = 4.0 * heff * n_act / (statistics.mean(fwd_ms) * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC,
+        "value": round(tokens_per_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "io_dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64/Box-Muller, keyed by logical token id)",
+        "config": {"workload": workload_desc(wl, lay_name, lay.n_physical), "hidden": H,
+                   "heads": list(wl.heads), "tokens": n_act, "layout": lay_name, "calls": len(lay.calls),
+                   "l2": "flushed before every timed step (256 MB write); inputs already in HBM",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "hbm_gbs_step": round(alg_step / (ms_step * 1e-3) / 1e9, 1),
+        "frac_step": round(alg_step / (ms_step * 1e-3) / 1e9 / hbm_peak, 4),
+        "fwd_gbs": round(fwd_gbs, 1),
+        "roofline": {"bound": "hbm", "kernel": "row_team_kernel<dx+dweight> (fused backward)",
+                     "achieved": round(achieved_bwd, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved_bwd / hbm_peak, 4), "traffic": None,
+                     "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": alg_bwd_launch,
+                     "launch_ms": round(bwd_per_launch_ms, 5)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+
+    if rank == 0 and args.all_layouts:
+        per = {}
+        ref_out = None
+        bitwise = True
+        for k, v in L.workload_layouts(wl).items():
+            so = [Step(wl, v, x, dy, w, rpt, device) for rpt, x, dy, w in steps_data]
+            m = Multi(so)
+            t, _ = time_steps(m, stream, max(3, args.steps // 2), 2, flush)
+            per[k] = {"ms": round(statistics.mean(t), 4), "calls": len(v.calls),
+                      "tokens_per_s": round(n_act / (statistics.mean(t) * 1e-3), 1)}
+            outs = [s.gather(wl.n_tokens) for s in so]
+            if ref_out is None:
+                ref_out = outs
+            else:
+                for a, b in zip(outs, ref_out):
+                    for ta, tb in zip(a, b):
+                        bitwise &= harness.bitwise_diff("t", ta, tb, k, "ref").equal
+            del so, m
+        line["layouts"] = per
+        line["bitwise_across_layouts"] = bool(bitwise)
+
+    if rank == 0 and not args.no_e2e:
+        x_h = [d[1].cpu() for d in steps_data]
+        dy_h = [d[2].cpu() for d in steps_data]
+        tot_ms, tot_in, tot_out = 0.0, 0, 0
+        for (rpt, x, dy, w), xh, dh in zip(steps_data, x_h, dy_h):
+            e_ms, bi, bo = e2e_steps(wl, lay, xh, dh, w, rpt, max(3, args.steps // 4), 2, device)
+            tot_ms += e_ms
+            tot_in += bi
+            tot_out += bo
+        line["e2e"] = {"value": round(n_act / (tot_ms * 1e-3) * world, 1), "unit": "tokens/s",
+                       "h2d_bytes_per_step": int(tot_in), "d2h_bytes_per_step": int(tot_out),
+                       "ms_per_step": round(tot_ms, 3)}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rpt, x, dy, w = steps_data[0]
+        n_cpu = min(x.shape[0], 4096)
+        line["cpu_baseline"] = cpu_baseline(wl, x[:n_cpu].cpu(), dy[:n_cpu].cpu(), w.cpu(), rpt,
+                                            args.cpu_seconds)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def reference_arm(args, rank, world):
+    """The oracle (FP64 C, as it stands) on the host cores, bounded per step."""
+    if rank != 0:
+        return
+    import torch
+    import synth
+    wl = synth.config(args.config)
+    lay_name = args.layout or wl.headline
+    rpt = wl.heads[0]
+    n_rows = min(wl.n_tokens * rpt, max(64, (1 << 21) // wl.hidden))
+    x = synth.logical_tensor(wl, synth.TAG_X, n_rows, wl.x_std, 0)
+    dy = synth.logical_tensor(wl, synth.TAG_DY, n_rows, wl.dy_std, 0)
+    w = synth.weight(wl, 0)
+    import oracle
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle.forward(x[:64], w, wl.eps)
+    times, rows_done = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        done = 0
+        while time.perf_counter() - t0 < per_step:
+            oracle.forward(x, w, wl.eps)
+            oracle.backward(x, w, dy, wl.eps)
+            done += n_rows
+        times.append(time.perf_counter() - t0)
+        rows_done.append(done)
+    tok_s = (sum(rows_done) / rpt) / sum(times)
+    sample = (f"{n_rows} logical rows of {wl.name} (hidden {wl.hidden}) repeated for ~{per_step:.1f} s per step; "
+              f"FP64 C oracle, single thread")
+    ms = statistics.mean(times) * 1e3
+    line = {"metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{wl.name}: hidden={wl.hidden}, layout={lay_name} (oracle works in logical order)",
+                       "hidden": wl.hidden, "tokens": wl.n_tokens},
+            "cpu_baseline": {"value": round(tok_s, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(tok_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

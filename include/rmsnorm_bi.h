@@ -1,0 +1,190 @@
+/*
+ * rmsnorm_bi.h - batch-invariant RMSNorm forward/backward for GB300 (sm_103a).
+ *
+ * The operation.  For every active physical row holding logical row g of a
+ * token multiset, with hidden size H and weight w:
+ *     rstd_g = 1 / sqrt(mean_h(x_gh^2) + eps),  xhat = x * rstd,  y = xhat * w
+ *     dx     = rstd * (g - xhat * mean_h(g * xhat)),  g = dy * w
+ *     dw_h   = sum over active logical rows of dy_gh * xhat_gh   (FP32)
+ * ("[WS1 Closeout][Backward] Reusable gradient-invariance harness and
+ * operator adapters", RL-Kernel #270: Scope and Required adapters, RMSNorm
+ * dx/dweight; the closed forms are the benchmark statement's.)
+ *
+ * The guarantee.  y, dx and dweight are bitwise identical for the same
+ * logical token multiset whatever its physical layout: one packed call,
+ * chunked-prefill pieces, one call per sample, right/left padding, permuted
+ * sample order ("WS1 C4 (#270) closeout evidence", section "The matrix is
+ * falsifiable").  Nothing is accumulated with atomics and no reduction shape
+ * depends on the row count of a call: row sums use a fixed tree that depends
+ * only on H, and dweight sums per-logical-row FP32 contributions in
+ * canonical logical order (same page, "Historical finding - RMSNorm dweight
+ * is not chunk/batch decomposable"): 64-row logical blocks, each reduced by
+ * a complete pairwise tree, then a pairwise tree with odd carry over the
+ * block partials.  Blocks cut by a call boundary spill their per-row
+ * contributions to the workspace and are reduced by dweight_finalize with
+ * the same tree.  Inactive (padding) rows contribute exactly nothing, and
+ * their outputs are never written.
+ *
+ * Conventions.
+ *  - bf16 tensors are passed as uint16_t bit patterns; FP32 as float.
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates nothing.  Everything is enqueued on `stream` and returns
+ *    before it runs.  The caller keeps inputs alive until the stream
+ *    reaches the call.
+ *  - A physical row r of a call is token slot r / rows_per_token, head
+ *    r % rows_per_token; its first element is at
+ *    (r / rows_per_token) * token_stride + (r % rows_per_token) * hidden.
+ *    Every row start must be 16-byte aligned: tensors 16-byte aligned,
+ *    hidden and token_stride multiples of 8.
+ *  - Return value: RMSNORM_OK (0) or a negative RMSNORM_ERR_* code.  Errors
+ *    a host can see (null pointers, sizes, alignment, a missing plan) return
+ *    synchronously with nothing enqueued.  Errors only the GPU can see (a
+ *    logical row contributed twice or never, a workspace set up for other
+ *    sizes, a pipeline wait that timed out) set bits in the workspace's
+ *    status word (rmsnorm_dweight_status); no kernel ever traps.
+ *  - Supported hidden sizes: multiples of 8 up to 4096, multiples of 512
+ *    up to 8192, and multiples of 1024 up to 16384.
+ */
+#ifndef RMSNORM_BI_H
+#define RMSNORM_BI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *rmsnorm_stream_t;
+
+enum {
+    RMSNORM_OK = 0,
+    RMSNORM_ERR_NULL = -1,        /* a required pointer is NULL */
+    RMSNORM_ERR_HIDDEN = -2,      /* hidden size not supported (see above) */
+    RMSNORM_ERR_ALIGN = -3,       /* pointer not 16-byte aligned or stride not a multiple of 8 */
+    RMSNORM_ERR_STRIDE = -4,      /* token_stride < rows_per_token * hidden */
+    RMSNORM_ERR_LAYOUT = -5,      /* negative sizes, rows_per_token < 1, too many rows */
+    RMSNORM_ERR_WORKSPACE = -6,   /* workspace smaller than rmsnorm_dweight_workspace_bytes */
+    RMSNORM_ERR_PLAN = -7,        /* dweight contribution requested without a plan */
+    RMSNORM_ERR_ID = -8,          /* plan build: token id < -1 or >= n_logical_tokens */
+    RMSNORM_ERR_DUPLICATE = -9,   /* plan build: a logical token appears twice in one call */
+    RMSNORM_ERR_CAPACITY = -10,   /* plan build: output buffer too small */
+    RMSNORM_ERR_CUDA = -11,       /* a CUDA runtime call or kernel launch failed */
+    RMSNORM_ERR_DEVICE = -12      /* the current device is not sm_103 */
+};
+
+/* Device status word bits (rmsnorm_dweight_status). */
+enum {
+    RMSNORM_STATUS_DOUBLE = 1,    /* a logical row contributed more than once */
+    RMSNORM_STATUS_MISSING = 2,   /* finalize found a logical row that never contributed */
+    RMSNORM_STATUS_HEADER = 4,    /* workspace was begun for other sizes, or never begun */
+    RMSNORM_STATUS_PLAN = 8,      /* a plan entry points outside the call or the multiset */
+    RMSNORM_STATUS_TIMEOUT = 16   /* a pipeline wait gave up after about one second */
+};
+
+/*
+ * One call's physical layout.  tok_id maps every token slot to its canonical
+ * logical token id g = (sum of lengths of samples with a smaller sample_id)
+ * + position, or -1 for an inactive (padding) slot.  With rows_per_token = R
+ * (per-head norms, e.g. R = number of heads), token g covers logical rows
+ * g*R .. g*R+R-1 (token-major, head-minor).  n_logical_tokens is the size of
+ * the whole multiset and is the same for every call of every layout.
+ * plan/plan_items come from rmsnorm_plan_build (copied to the device) and are
+ * needed only by the calls that contribute to dweight.
+ */
+typedef struct rmsnorm_layout {
+    int64_t n_tokens;            /* token slots in this call */
+    int32_t rows_per_token;      /* 1 for RMSNorm over hidden; heads for per-head norms */
+    int32_t reserved0;           /* must be 0 */
+    int64_t token_stride;        /* elements between consecutive token slots */
+    const int32_t *tok_id;       /* device [n_tokens] */
+    int64_t n_logical_tokens;    /* tokens in the whole logical multiset */
+    const void *plan;            /* device copy of rmsnorm_plan_build's output, or NULL */
+    int64_t plan_items;          /* items in plan */
+} rmsnorm_layout_t;
+
+/*
+ * Forward: y = x * rstd * w on every active row; inactive rows of y are not
+ * written.  x, y: bf16 rows as described above; weight: bf16 [hidden];
+ * rstd: optional FP32 [n_tokens * rows_per_token] (NULL to skip), written for
+ * active rows only.  In-place (y == x) is allowed.
+ */
+int rmsnorm_fwd(const uint16_t *x, const uint16_t *weight, int64_t hidden, float eps,
+                const rmsnorm_layout_t *layout, uint16_t *y, float *rstd,
+                rmsnorm_stream_t stream);
+
+/*
+ * Backward input gradient dx = rstd * (dy*w - xhat * mean(dy*w*xhat)) on every
+ * active row (inactive rows of dx untouched).  rstd is recomputed bitwise as
+ * in rmsnorm_fwd.  If workspace is non-NULL the same pass also contributes
+ * this call's rows to dweight (layout->plan required); dx may then be NULL to
+ * skip writing it.  dx may alias dy.
+ */
+int rmsnorm_bwd_dx(const uint16_t *x, const uint16_t *weight, const uint16_t *dy,
+                   int64_t hidden, float eps, const rmsnorm_layout_t *layout,
+                   uint16_t *dx, void *workspace, rmsnorm_stream_t stream);
+
+/*
+ * dweight contribution only: adds this call's rows (c_g = dy_g * xhat_g in
+ * FP32) to the workspace without computing dx.  Same as rmsnorm_bwd_dx with
+ * dx == NULL, minus the weight (not needed).
+ */
+int rmsnorm_bwd_dweight_contrib(const uint16_t *x, const uint16_t *dy, int64_t hidden,
+                                float eps, const rmsnorm_layout_t *layout, void *workspace,
+                                rmsnorm_stream_t stream);
+
+/*
+ * Workspace for one dweight reduction over n_logical_rows = n_logical_tokens
+ * * rows_per_token rows of width hidden: a header with the status word,
+ * per-block and per-row flags, the block partials, finalize scratch, and a
+ * dense FP32 spill area [n_logical_rows][hidden] for rows of blocks that are
+ * cut by a call boundary.  Returns 0 for unsupported sizes.
+ */
+size_t rmsnorm_dweight_workspace_bytes(int64_t n_logical_rows, int64_t hidden);
+
+/*
+ * Starts a reduction: writes the header and clears flags and status.  Every
+ * logical row must then be contributed exactly once, by any number of
+ * rmsnorm_bwd_dx / rmsnorm_bwd_dweight_contrib calls in any order on this
+ * stream, before dweight_finalize.  Calls on other streams must be ordered
+ * with events by the caller.
+ */
+int rmsnorm_dweight_begin(void *workspace, size_t bytes, int64_t n_logical_rows,
+                          int64_t hidden, rmsnorm_stream_t stream);
+
+/*
+ * Ends a reduction: reduces the spilled rows of cut blocks with the same
+ * 64-leaf tree, then all block partials with the fixed carry tree, and
+ * writes dweight (FP32 [hidden]).  n_logical_rows == 0 gives dweight = +0.0.
+ */
+int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t hidden, float *dweight,
+                     rmsnorm_stream_t stream);
+
+/* Synchronises `stream` and copies the workspace's status word to *status. */
+int rmsnorm_dweight_status(const void *workspace, rmsnorm_stream_t stream, int32_t *status);
+
+/*
+ * Host-side planner (no GPU needed).  From a HOST copy of a call's tok_id it
+ * writes the work items that rmsnorm_bwd_dx / rmsnorm_bwd_dweight_contrib
+ * execute: one item per logical block wholly inside the call (its 64 rows in
+ * logical order) and items of up to 64 rows from blocks cut by a call
+ * boundary.  rmsnorm_plan_bytes gives a capacity that always suffices.
+ * Errors: RMSNORM_ERR_ID, RMSNORM_ERR_DUPLICATE, RMSNORM_ERR_CAPACITY.
+ * The plan depends only on tok_id, rows_per_token and n_logical_tokens.
+ */
+int rmsnorm_plan_bytes(int64_t n_tokens, int32_t rows_per_token, size_t *bytes);
+int rmsnorm_plan_build(const int32_t *host_tok_id, int64_t n_tokens, int32_t rows_per_token,
+                       int64_t n_logical_tokens, void *host_plan, size_t capacity,
+                       int64_t *plan_items, int64_t *whole_blocks, int64_t *spill_rows);
+
+/* Static text for a return code. */
+const char *rmsnorm_strerror(int code);
+
+/* Number of kernels this library has launched in this process (all devices). */
+int64_t rmsnorm_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RMSNORM_BI_H */

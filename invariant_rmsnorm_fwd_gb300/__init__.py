@@ -1,0 +1,242 @@
+"""Batch-invariant RMSNorm forward/backward for GB300 (sm_103a).
+
+Thin Python binding over the C ABI in include/rmsnorm_bi.h: every function
+here marshals arguments and calls the library; every step of the computation
+runs in the library's CUDA kernels.  There is no CPU path: if the library is
+missing and cannot be built, importing the binding's functions raises.
+
+PyTorch supplies device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import layout  # noqa: F401  (host layout mapper)
+
+_lib = None
+
+OK = 0
+ERR_NAMES = {
+    -1: "NULL", -2: "HIDDEN", -3: "ALIGN", -4: "STRIDE", -5: "LAYOUT", -6: "WORKSPACE",
+    -7: "PLAN", -8: "ID", -9: "DUPLICATE", -10: "CAPACITY", -11: "CUDA", -12: "DEVICE",
+}
+STATUS_DOUBLE, STATUS_MISSING, STATUS_HEADER, STATUS_PLAN, STATUS_TIMEOUT = 1, 2, 4, 8, 16
+PLAN_ITEM_BYTES = 528
+
+
+class RmsNormError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = _load().rmsnorm_strerror(code).decode() if _lib is not None else str(code)
+        super().__init__(f"{where}: {ERR_NAMES.get(code, code)} ({msg})")
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [
+        ("n_tokens", ctypes.c_int64),
+        ("rows_per_token", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("token_stride", ctypes.c_int64),
+        ("tok_id", ctypes.c_void_p),
+        ("n_logical_tokens", ctypes.c_int64),
+        ("plan", ctypes.c_void_p),
+        ("plan_items", ctypes.c_int64),
+    ]
+
+
+def library_path() -> str:
+    from . import _build
+    return _build.LIB
+
+
+def _load():
+    """Load the CUDA library, building it in-tree first if it is absent or stale."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    from . import _build
+    path = _build.build()
+    lib = ctypes.CDLL(path)
+    P, I64, I32, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    LP = ctypes.POINTER(_Layout)
+    sig = {
+        "rmsnorm_fwd": ([P, P, I64, F, LP, P, P, P], ctypes.c_int),
+        "rmsnorm_bwd_dx": ([P, P, P, I64, F, LP, P, P, P], ctypes.c_int),
+        "rmsnorm_bwd_dweight_contrib": ([P, P, I64, F, LP, P, P], ctypes.c_int),
+        "rmsnorm_dweight_workspace_bytes": ([I64, I64], ctypes.c_size_t),
+        "rmsnorm_dweight_begin": ([P, ctypes.c_size_t, I64, I64, P], ctypes.c_int),
+        "dweight_finalize": ([P, I64, I64, P, P], ctypes.c_int),
+        "rmsnorm_dweight_status": ([P, P, ctypes.POINTER(I32)], ctypes.c_int),
+        "rmsnorm_plan_bytes": ([I64, I32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+        "rmsnorm_plan_build": ([P, I64, I32, I64, P, ctypes.c_size_t, ctypes.POINTER(I64),
+                                ctypes.POINTER(I64), ctypes.POINTER(I64)], ctypes.c_int),
+        "rmsnorm_strerror": ([ctypes.c_int], ctypes.c_char_p),
+        "rmsnorm_kernel_launches": ([], I64),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise RmsNormError(rc, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def kernel_launches() -> int:
+    return int(_load().rmsnorm_kernel_launches())
+
+
+# ------------------------------------------------------------------ planning
+
+def plan_build(tok_id: np.ndarray, rows_per_token: int, n_logical_tokens: int):
+    """Host planner (C++ in the library).  Returns (plan bytes as np.uint8, items,
+    whole blocks, spilled rows)."""
+    lib = _load()
+    tok_id = np.ascontiguousarray(tok_id, dtype=np.int32)
+    cap = ctypes.c_size_t(0)
+    _check(lib.rmsnorm_plan_bytes(tok_id.size, rows_per_token, ctypes.byref(cap)), "rmsnorm_plan_bytes")
+    buf = np.empty(max(int(cap.value), PLAN_ITEM_BYTES), dtype=np.uint8)
+    items, whole, spill = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib.rmsnorm_plan_build(tok_id.ctypes.data_as(ctypes.c_void_p), tok_id.size, rows_per_token,
+                                  n_logical_tokens, buf.ctypes.data_as(ctypes.c_void_p), buf.size,
+                                  ctypes.byref(items), ctypes.byref(whole), ctypes.byref(spill)),
+           "rmsnorm_plan_build")
+    return buf[:items.value * PLAN_ITEM_BYTES], items.value, whole.value, spill.value
+
+
+@dataclass
+class CallLayout:
+    """Device-side descriptor of one call: token ids and (optionally) its plan."""
+    tok_id: object                      # torch int32 [n_tokens] on the device
+    plan: object                        # torch uint8 on the device, or None
+    plan_items: int
+    n_tokens: int
+    rows_per_token: int
+    n_logical_tokens: int
+    whole_blocks: int = 0
+    spill_rows: int = 0
+
+    def struct(self, token_stride: int) -> _Layout:
+        return _Layout(self.n_tokens, self.rows_per_token, 0, token_stride,
+                       self.tok_id.data_ptr() if self.n_tokens else None,
+                       self.n_logical_tokens,
+                       self.plan.data_ptr() if self.plan is not None and self.plan_items else None,
+                       self.plan_items)
+
+
+def call_layout(tok_id: np.ndarray, rows_per_token: int, n_logical_tokens: int, device="cuda",
+                with_plan: bool = True) -> CallLayout:
+    import torch
+    tok_id = np.ascontiguousarray(tok_id, dtype=np.int32)
+    tdev = torch.from_numpy(tok_id).to(device)
+    plan = None
+    items = whole = spill = 0
+    if with_plan:
+        pbytes, items, whole, spill = plan_build(tok_id, rows_per_token, n_logical_tokens)
+        plan = torch.from_numpy(pbytes.copy()).to(device) if items else torch.zeros(16, dtype=torch.uint8,
+                                                                                      device=device)
+    return CallLayout(tdev, plan, items, tok_id.size, rows_per_token, n_logical_tokens, whole, spill)
+
+
+# ------------------------------------------------------------------ ops
+
+def _rows_view(t, rpt: int, hidden: int):
+    """Token stride in elements of a [n_tokens, rpt*hidden] or [n_tokens, rpt, hidden] tensor."""
+    if t.dim() == 3:
+        assert t.shape[1] == rpt and t.shape[2] == hidden and t.stride(2) == 1 and t.stride(1) == hidden
+    else:
+        assert t.dim() == 2 and t.shape[1] == rpt * hidden and t.stride(1) == 1
+    return t.stride(0)
+
+
+def rmsnorm_fwd(x, weight, lay: CallLayout, eps: float, y=None, rstd=None, stream=None):
+    import torch
+    H = weight.shape[0]
+    if y is None:
+        y = torch.empty_like(x)
+    stride = _rows_view(x, lay.rows_per_token, H)
+    assert _rows_view(y, lay.rows_per_token, H) == stride
+    L = lay.struct(stride)
+    _check(_load().rmsnorm_fwd(_ptr(x), _ptr(weight), H, eps, ctypes.byref(L), _ptr(y), _ptr(rstd),
+                               _stream(stream)), "rmsnorm_fwd")
+    return y
+
+
+def rmsnorm_bwd_dx(x, weight, dy, lay: CallLayout, eps: float, dx=None, workspace=None, stream=None,
+                   write_dx: bool = True):
+    import torch
+    H = weight.shape[0]
+    if dx is None and write_dx:
+        dx = torch.empty_like(dy)
+    stride = _rows_view(x, lay.rows_per_token, H)
+    assert _rows_view(dy, lay.rows_per_token, H) == stride
+    if dx is not None:
+        assert _rows_view(dx, lay.rows_per_token, H) == stride
+    L = lay.struct(stride)
+    _check(_load().rmsnorm_bwd_dx(_ptr(x), _ptr(weight), _ptr(dy), H, eps, ctypes.byref(L), _ptr(dx),
+                                  None if workspace is None else _ptr(workspace.buf), _stream(stream)),
+           "rmsnorm_bwd_dx")
+    return dx
+
+
+def rmsnorm_bwd_dweight_contrib(x, dy, hidden: int, lay: CallLayout, eps: float, workspace, stream=None):
+    stride = _rows_view(x, lay.rows_per_token, hidden)
+    L = lay.struct(stride)
+    _check(_load().rmsnorm_bwd_dweight_contrib(_ptr(x), _ptr(dy), hidden, eps, ctypes.byref(L),
+                                               _ptr(workspace.buf), _stream(stream)),
+           "rmsnorm_bwd_dweight_contrib")
+
+
+class DweightWorkspace:
+    """Device workspace of one dweight reduction (allocated by PyTorch)."""
+
+    def __init__(self, n_logical_rows: int, hidden: int, device="cuda"):
+        import torch
+        self.n_rows = int(n_logical_rows)
+        self.hidden = int(hidden)
+        self.bytes = int(_load().rmsnorm_dweight_workspace_bytes(self.n_rows, self.hidden))
+        if self.bytes == 0:
+            raise RmsNormError(-5, "rmsnorm_dweight_workspace_bytes")
+        self.buf = torch.empty(self.bytes, dtype=torch.uint8, device=device)
+        assert self.buf.data_ptr() % 256 == 0
+
+    def begin(self, stream=None):
+        _check(_load().rmsnorm_dweight_begin(_ptr(self.buf), self.bytes, self.n_rows, self.hidden,
+                                             _stream(stream)), "rmsnorm_dweight_begin")
+
+    def finalize(self, dweight=None, stream=None):
+        import torch
+        if dweight is None:
+            dweight = torch.empty(self.hidden, dtype=torch.float32, device=self.buf.device)
+        _check(_load().dweight_finalize(_ptr(self.buf), self.n_rows, self.hidden, _ptr(dweight),
+                                        _stream(stream)), "dweight_finalize")
+        return dweight
+
+    def status(self, stream=None) -> int:
+        out = ctypes.c_int32(0)
+        _check(_load().rmsnorm_dweight_status(_ptr(self.buf), _stream(stream), ctypes.byref(out)),
+               "rmsnorm_dweight_status")
+        return int(out.value)
+
+
+def dweight_finalize(workspace: DweightWorkspace, dweight=None, stream=None):
+    return workspace.finalize(dweight, stream)

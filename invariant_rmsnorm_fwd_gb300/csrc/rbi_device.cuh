@@ -1,0 +1,334 @@
+// Device helpers for the batch-invariant RMSNorm kernels (sm_103a).
+//
+// Every floating-point operation on the numeric path is an explicit
+// round-to-nearest intrinsic (__fadd_rn, __fmul_rn, __fmaf_rn, ...), and the
+// library is compiled with -fmad=false, so the compiler can neither contract
+// nor reassociate: a value depends only on the operands and the fixed order
+// written here, never on which kernel, launch shape or layout produced it.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace rbi {
+
+constexpr int kBlockRows = 64;       // logical block of the dweight reduction
+constexpr int kBlockLevels = 6;      // log2(kBlockRows)
+constexpr unsigned kFull = 0xffffffffu;
+
+// Status bits (mirror RMSNORM_STATUS_* in the public header).
+constexpr int kStDouble = 1, kStMissing = 2, kStHeader = 4, kStPlan = 8, kStTimeout = 16;
+
+// ----------------------------------------------------------------- workspace
+
+constexpr uint64_t kWsMagic = 0x3149422d4d524e52ull;   // "RNMR-BI1"
+
+struct WsHeader {
+    uint64_t magic;
+    int64_t n_rows;
+    int64_t hidden;
+    int64_t n_blocks;
+    int32_t status;
+    int32_t pad[55];
+};
+static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
+
+struct WsView {                      // device addresses of the workspace regions
+    WsHeader *hdr;
+    uint8_t *block_state;            // [nb]   1 = whole block partial written
+    uint8_t *leaf_flag;              // [N]    1 = row spilled
+    float *block_partial;            // [nb][H]
+    float *scratch_a;                // [ceil(nb/64)][H]
+    float *scratch_b;                // [ceil(nb/64)][H]
+    float *spill;                    // [N][H]
+    int64_t n_rows, hidden, n_blocks;
+};
+
+__host__ __device__ inline int64_t align256(int64_t v) { return (v + 255) & ~int64_t(255); }
+
+// Region offsets depend only on (N, H); host and device compute them alike.
+struct WsLayout {
+    int64_t off_state, off_flag, off_partial, off_sa, off_sb, off_spill, total;
+    __host__ __device__ WsLayout(int64_t N, int64_t H) {
+        int64_t nb = (N + kBlockRows - 1) / kBlockRows;
+        int64_t ng = (nb + kBlockRows - 1) / kBlockRows;
+        off_state = 256;
+        off_flag = align256(off_state + nb);
+        off_partial = align256(off_flag + N);
+        off_sa = align256(off_partial + nb * H * 4);
+        off_sb = align256(off_sa + ng * H * 4);
+        off_spill = align256(off_sb + ng * H * 4);
+        total = align256(off_spill + N * H * 4);
+    }
+};
+
+inline WsView ws_view(void *base, int64_t N, int64_t H) {
+    WsLayout L(N, H);
+    uint8_t *b = static_cast<uint8_t *>(base);
+    WsView v;
+    v.hdr = reinterpret_cast<WsHeader *>(b);
+    v.block_state = b + L.off_state;
+    v.leaf_flag = b + L.off_flag;
+    v.block_partial = reinterpret_cast<float *>(b + L.off_partial);
+    v.scratch_a = reinterpret_cast<float *>(b + L.off_sa);
+    v.scratch_b = reinterpret_cast<float *>(b + L.off_sb);
+    v.spill = reinterpret_cast<float *>(b + L.off_spill);
+    v.n_rows = N;
+    v.hidden = H;
+    v.n_blocks = (N + kBlockRows - 1) / kBlockRows;
+    return v;
+}
+
+__device__ __forceinline__ void set_status(WsHeader *h, int bit) {
+    // Error reporting only: a plain store of the OR of what this thread saw.
+    // Concurrent writers can only lose a bit if two different errors race,
+    // and any non-zero word already reports failure.
+    volatile int32_t *s = &h->status;
+    *s = *s | bit;
+}
+
+__device__ __forceinline__ bool header_ok(const WsView &ws) {
+    const WsHeader *h = ws.hdr;
+    return h->magic == kWsMagic && h->n_rows == ws.n_rows && h->hidden == ws.hidden;
+}
+
+// ----------------------------------------------------------------- plan items
+
+struct PlanItem {                    // written by the host planner
+    int32_t kind;                    // 0 = whole logical block, 1 = rows of cut blocks
+    int32_t block;                   // block id for kind 0, -1 otherwise
+    int32_t count;                   // used slots
+    int32_t reserved;
+    int32_t prow[kBlockRows];        // physical row within the call, -1 = empty slot
+    int32_t lrow[kBlockRows];        // logical row id, -1 = empty slot
+};
+static_assert(sizeof(PlanItem) == 528, "plan item layout is part of the ABI");
+
+// ----------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity; gives up after ~1 s of wall time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > 1000000000ull) return false;
+    }
+}
+
+// One-dimensional bulk copy global -> this CTA's shared memory, completion
+// counted in bytes on `bar`.  Both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_global_stream_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_global_f32x4(float *p, float a, float b, float c, float d) {
+    asm volatile("st.global.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_global_f32x4(const float *p) {
+    float4 v;
+    asm volatile("ld.global.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
+// ----------------------------------------------------------------- bf16
+
+// bf16 -> f32 is exact: the bf16 bits are the top half of the binary32.
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// f32 -> bf16 round-to-nearest-even (hardware cvt.rn.bf16x2.f32).
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ----------------------------------------------------------------- row sums
+//
+// Canonical row-sum tree for hidden size H (V = H/8 vectors of 8 columns):
+//  1. each vector's 8 terms are folded in column order with fused multiply-
+//     adds: s = a0*b0; s = fma(a_i, b_i, s) for i = 1..7;
+//  2. the V vector sums, zero-padded to P = next power of two >= V, are
+//     added by a complete pairwise tree with adjacent pairing: (0,1), (2,3),
+//     ..., then adjacent pairs of those, and so on.
+// The tree depends on H only.  The kernels realise step 2 as xor-butterflies
+// (xor 1, 2, 4, ...) over lanes and then over warps, which is this tree.
+
+__device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8]) {
+    float s = __fmul_rn(a[0], b[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) s = __fmaf_rn(a[i], b[i], s);
+    return s;
+}
+
+// Butterfly over lanes xor 1 .. width/2 (width a power of two <= 32): every
+// lane of each aligned group of `width` lanes ends with the group's sum.
+__device__ __forceinline__ float lane_tree(float v, int width) {
+#pragma unroll
+    for (int k = 1; k < 32; k <<= 1)
+        if (k < width) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, k));
+    return v;
+}
+
+// rstd = 1 / sqrt(ss / H + eps), each step correctly rounded.
+__device__ __forceinline__ float row_rstd(float ss, float Hf, float eps) {
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, Hf), eps)));
+}
+
+// m = mean(g * xhat) = (rstd * sum(g * x)) / H.
+__device__ __forceinline__ float row_mean_gxhat(float gx, float rstd, float Hf) {
+    return __fdiv_rn(__fmul_rn(gx, rstd), Hf);
+}
+
+// ----------------------------------------------------------------- 64-leaf tree
+//
+// Streaming form of the complete pairwise tree over the 64 leaves of a
+// logical block: leaf n (0..63) is combined with the pending partials whose
+// bits are set in n (binary counter), earlier leaves always on the left.
+// After leaf 63 the returned value is the block partial.  Any subtree of 2^k
+// aligned leaves can be pushed as one item at level k.
+
+template <int NCOL>
+struct TreeStack {
+    float s[kBlockLevels][NCOL];
+
+    // Push v (a complete subtree of 2^level leaves) as item `idx` at that
+    // level; on return v holds the partial that was just completed (the whole
+    // block after the last item).  idx is uniform across the threads that
+    // share the tree.
+    __device__ __forceinline__ void push(float (&v)[NCOL], int idx, int level) {
+        bool carry = true;
+#pragma unroll
+        for (int l = 0; l < kBlockLevels; ++l) {
+            if (l < level || !carry) continue;
+            const bool bit = (idx >> (l - level)) & 1;
+#pragma unroll
+            for (int c = 0; c < NCOL; ++c) {
+                const float sum = __fadd_rn(s[l][c], v[c]);
+                s[l][c] = bit ? s[l][c] : v[c];
+                v[c] = bit ? sum : v[c];
+            }
+            carry = bit;
+        }
+    }
+
+    // Carry-tree result of n items (1 <= n <= 63) pushed as push(v, i, 0),
+    // i = 0..n-1: the pending partials (set bits of n) folded from the lowest
+    // level up, later items always on the right.  This is the pairwise tree
+    // that pairs (2i, 2i+1) at every level and carries an odd last element.
+    __device__ __forceinline__ void fold(int n, float (&res)[NCOL]) const {
+        bool have = false;
+#pragma unroll
+        for (int c = 0; c < NCOL; ++c) res[c] = 0.f;
+#pragma unroll
+        for (int l = 0; l < kBlockLevels; ++l) {
+            if (!((n >> l) & 1)) continue;
+            if (!have) {
+#pragma unroll
+                for (int c = 0; c < NCOL; ++c) res[c] = s[l][c];
+                have = true;
+            } else {
+#pragma unroll
+                for (int c = 0; c < NCOL; ++c) res[c] = __fadd_rn(s[l][c], res[c]);
+            }
+        }
+    }
+};
+
+}  // namespace rbi

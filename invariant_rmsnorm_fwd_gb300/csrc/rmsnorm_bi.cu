@@ -1,0 +1,391 @@
+// C-ABI entry points of the batch-invariant RMSNorm library (sm_103a).
+//
+// Launch shapes depend on the hidden size and the device's SM count only;
+// which CTA handles which row never changes a value (see rmsnorm_kernels.cuh),
+// so results are identical for every layout and every grid.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/rmsnorm_bi.h"
+#include "rmsnorm_kernels.cuh"
+
+using namespace rbi;
+
+namespace {
+
+std::atomic<int64_t> g_launches{0};
+
+struct DeviceInfo {
+    bool ready = false;
+    int status = RMSNORM_OK;
+    int sms = 0;
+    int max_smem = 0;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+int device_info(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RMSNORM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        d.status = (major == 10 && minor == 3) ? RMSNORM_OK : RMSNORM_ERR_DEVICE;
+        d.ready = true;
+    }
+    *out = &d;
+    return d.status;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- shapes
+
+struct Shape {
+    bool small = false;   // small_row_kernel
+    int p2 = 0;           // lanes per row (small)
+    int k = 1;            // CTAs per team (large)
+    int threads = 0;      // threads per CTA (large)
+};
+
+bool hidden_shape(int64_t H, Shape *s) {
+    if (H < 8 || H % 8 != 0 || H > 16384) return false;
+    const int64_t V = H / 8;
+    if (V <= 32) {
+        s->small = true;
+        int p = 1;
+        while (p < V) p <<= 1;
+        s->p2 = p;
+        return true;
+    }
+    if (V <= 512) {
+        s->k = 1;
+        s->threads = int((V + 31) / 32 * 32);
+        return true;
+    }
+    for (int k = 2; k <= 4; k *= 2) {
+        if (V % (32 * k) == 0 && V / k <= 512) {
+            s->k = k;
+            s->threads = int(V / k);
+            return true;
+        }
+    }
+    return false;
+}
+
+int check_layout(const rmsnorm_layout_t *L, int64_t H) {
+    if (!L) return RMSNORM_ERR_NULL;
+    if (L->n_tokens < 0 || L->rows_per_token < 1 || L->reserved0 != 0 || L->n_logical_tokens < 0 ||
+        L->plan_items < 0)
+        return RMSNORM_ERR_LAYOUT;
+    if (L->n_tokens > 0 && !L->tok_id) return RMSNORM_ERR_NULL;
+    if (L->token_stride % 8 != 0) return RMSNORM_ERR_ALIGN;
+    if (L->token_stride < int64_t(L->rows_per_token) * H) return RMSNORM_ERR_STRIDE;
+    const int64_t rows = L->n_tokens * L->rows_per_token;
+    if (rows >= (int64_t(1) << 31) || L->n_logical_tokens * L->rows_per_token >= (int64_t(1) << 31))
+        return RMSNORM_ERR_LAYOUT;
+    return RMSNORM_OK;
+}
+
+// ---------------------------------------------------------------- launches
+
+constexpr int kHeaderSmem = 128 + 8 * 8 * 16 + 2 * 16 * 32 * 4;
+constexpr int kMaxStages = 8;
+
+template <int MODE, int K, int R>
+int launch_team(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
+    constexpr int nt = ModeTraits<MODE>::kTensors;
+    const int64_t slice = (p.hidden / 8 / K) * 16;
+    const int64_t stage_bytes = slice * nt * R;
+    const int64_t budget = int64_t(d.max_smem) - kHeaderSmem;
+    int S = int(budget / stage_bytes);
+    if (S > kMaxStages) S = kMaxStages;
+    if (S < 2) return RMSNORM_ERR_HIDDEN;
+    const int smem = int(kHeaderSmem + S * stage_bytes);
+    auto kern = row_team_kernel<MODE, K, R>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(sh.threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    int64_t clusters;
+    if (K > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = K;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(K * d.sms);
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1)
+            return RMSNORM_ERR_CUDA;
+        clusters = active;
+    } else {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, sh.threads, smem) != cudaSuccess ||
+            per_sm < 1)
+            return RMSNORM_ERR_CUDA;
+        clusters = int64_t(per_sm) * d.sms;
+    }
+    if (clusters > p.n_units) clusters = p.n_units;
+    if (clusters < 1) return RMSNORM_OK;
+    cfg.gridDim = dim3(unsigned(clusters * K));
+    if (cudaLaunchKernelEx(&cfg, kern, p, S) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return RMSNORM_OK;
+}
+
+template <int MODE, int R>
+int launch_team_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t s) {
+    switch (sh.k) {
+        case 1: return launch_team<MODE, 1, R>(p, sh, d, s);
+        case 2: return launch_team<MODE, 2, R>(p, sh, d, s);
+        case 4: return launch_team<MODE, 4, R>(p, sh, d, s);
+        default: return RMSNORM_ERR_HIDDEN;
+    }
+}
+
+template <int MODE, int P2>
+int launch_small(const KParams &p, const DeviceInfo &d, cudaStream_t stream) {
+    constexpr int U = 4;
+    auto kern = small_row_kernel<MODE, P2, U>;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)
+        return RMSNORM_ERR_CUDA;
+    int64_t blocks = int64_t(per_sm) * d.sms;
+    const int64_t need = (p.n_units + 7) / 8;            // 8 warps per block, one unit per warp
+    if (blocks > need) blocks = need;
+    if (blocks < 1) return RMSNORM_OK;
+    kern<<<unsigned(blocks), 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return RMSNORM_OK;
+}
+
+template <int MODE>
+int launch_small_p(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t s) {
+    switch (sh.p2) {
+        case 1: return launch_small<MODE, 1>(p, d, s);
+        case 2: return launch_small<MODE, 2>(p, d, s);
+        case 4: return launch_small<MODE, 4>(p, d, s);
+        case 8: return launch_small<MODE, 8>(p, d, s);
+        case 16: return launch_small<MODE, 16>(p, d, s);
+        case 32: return launch_small<MODE, 32>(p, d, s);
+        default: return RMSNORM_ERR_HIDDEN;
+    }
+}
+
+template <int MODE>
+int run_rows(KParams p, const Shape &sh, const rmsnorm_layout_t *L, cudaStream_t stream) {
+    DeviceInfo *d = nullptr;
+    int rc = device_info(&d);
+    if (rc != RMSNORM_OK) return rc;
+    constexpr int R = (MODE == kFwd) ? 8 : 4;
+    const bool plan = p.use_plan != 0;
+    if (plan) {
+        p.n_units = L->plan_items;
+    } else if (sh.small) {
+        p.n_units = (p.n_rows + kBlockRows - 1) / kBlockRows;
+    } else {
+        p.n_units = (p.n_rows + R - 1) / R;
+    }
+    if (p.n_units == 0) return RMSNORM_OK;
+    if (sh.small) return launch_small_p<MODE>(p, sh, *d, stream);
+    return launch_team_k<MODE, R>(p, sh, *d, stream);
+}
+
+KParams base_params(const rmsnorm_layout_t *L, int64_t H, float eps) {
+    KParams p = {};
+    p.tok_id = L->tok_id;
+    p.n_rows = L->n_tokens * L->rows_per_token;
+    p.token_stride = L->token_stride;
+    p.rpt = L->rows_per_token;
+    p.hidden = int32_t(H);
+    p.eps = eps;
+    p.items = static_cast<const PlanItem *>(L->plan);
+    p.use_plan = L->plan != nullptr ? 1 : 0;
+    return p;
+}
+
+int ws_checks(const void *ws, int64_t N, int64_t H) {
+    if (!ws) return RMSNORM_ERR_NULL;
+    if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RMSNORM_ERR_ALIGN;
+    if (N < 0) return RMSNORM_ERR_LAYOUT;
+    Shape sh;
+    if (!hidden_shape(H, &sh)) return RMSNORM_ERR_HIDDEN;
+    return RMSNORM_OK;
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" int rmsnorm_fwd(const uint16_t *x, const uint16_t *weight, int64_t hidden, float eps,
+                           const rmsnorm_layout_t *layout, uint16_t *y, float *rstd, rmsnorm_stream_t stream) {
+    Shape sh;
+    if (!hidden_shape(hidden, &sh)) return RMSNORM_ERR_HIDDEN;
+    int rc = check_layout(layout, hidden);
+    if (rc) return rc;
+    if (layout->n_tokens == 0) return RMSNORM_OK;
+    if (!x || !weight || !y) return RMSNORM_ERR_NULL;
+    if (!aligned16(x) || !aligned16(weight) || !aligned16(y)) return RMSNORM_ERR_ALIGN;
+    KParams p = base_params(layout, hidden, eps);
+    p.x = x;
+    p.w = weight;
+    p.out = y;
+    p.rstd_out = rstd;
+    return run_rows<kFwd>(p, sh, layout, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int rmsnorm_bwd_dx(const uint16_t *x, const uint16_t *weight, const uint16_t *dy, int64_t hidden,
+                              float eps, const rmsnorm_layout_t *layout, uint16_t *dx, void *workspace,
+                              rmsnorm_stream_t stream) {
+    Shape sh;
+    if (!hidden_shape(hidden, &sh)) return RMSNORM_ERR_HIDDEN;
+    int rc = check_layout(layout, hidden);
+    if (rc) return rc;
+    if (!workspace && !dx) return RMSNORM_ERR_NULL;
+    if (workspace && !layout->plan && layout->n_tokens > 0) return RMSNORM_ERR_PLAN;
+    const int64_t N = layout->n_logical_tokens * layout->rows_per_token;
+    if (workspace && (rc = ws_checks(workspace, N, hidden))) return rc;
+    if (layout->n_tokens == 0) return RMSNORM_OK;
+    if (!x || !weight || !dy) return RMSNORM_ERR_NULL;
+    if (!aligned16(x) || !aligned16(weight) || !aligned16(dy) || (dx && !aligned16(dx))) return RMSNORM_ERR_ALIGN;
+    KParams p = base_params(layout, hidden, eps);
+    p.x = x;
+    p.w = weight;
+    p.dy = dy;
+    p.out = dx;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!workspace) return run_rows<kDx>(p, sh, layout, s);
+    p.ws = ws_view(workspace, N, hidden);
+    return run_rows<kDxDw>(p, sh, layout, s);
+}
+
+extern "C" int rmsnorm_bwd_dweight_contrib(const uint16_t *x, const uint16_t *dy, int64_t hidden, float eps,
+                                           const rmsnorm_layout_t *layout, void *workspace,
+                                           rmsnorm_stream_t stream) {
+    Shape sh;
+    if (!hidden_shape(hidden, &sh)) return RMSNORM_ERR_HIDDEN;
+    int rc = check_layout(layout, hidden);
+    if (rc) return rc;
+    const int64_t N = layout->n_logical_tokens * layout->rows_per_token;
+    if ((rc = ws_checks(workspace, N, hidden))) return rc;
+    if (layout->n_tokens == 0) return RMSNORM_OK;
+    if (!layout->plan) return RMSNORM_ERR_PLAN;
+    if (!x || !dy) return RMSNORM_ERR_NULL;
+    if (!aligned16(x) || !aligned16(dy)) return RMSNORM_ERR_ALIGN;
+    KParams p = base_params(layout, hidden, eps);
+    p.x = x;
+    p.dy = dy;
+    p.ws = ws_view(workspace, N, hidden);
+    return run_rows<kDw>(p, sh, layout, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t rmsnorm_dweight_workspace_bytes(int64_t n_logical_rows, int64_t hidden) {
+    Shape sh;
+    if (n_logical_rows < 0 || n_logical_rows >= (int64_t(1) << 31) || !hidden_shape(hidden, &sh)) return 0;
+    return size_t(WsLayout(n_logical_rows, hidden).total);
+}
+
+extern "C" int rmsnorm_dweight_begin(void *workspace, size_t bytes, int64_t n_logical_rows, int64_t hidden,
+                                     rmsnorm_stream_t stream) {
+    int rc = ws_checks(workspace, n_logical_rows, hidden);
+    if (rc) return rc;
+    const size_t need = rmsnorm_dweight_workspace_bytes(n_logical_rows, hidden);
+    if (need == 0) return RMSNORM_ERR_LAYOUT;
+    if (bytes < need) return RMSNORM_ERR_WORKSPACE;
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    WsView ws = ws_view(workspace, n_logical_rows, hidden);
+    const int64_t flag_bytes = reinterpret_cast<uint8_t *>(ws.block_partial) - ws.block_state;
+    int64_t blocks = (flag_bytes / 16 + 255) / 256;
+    if (blocks > int64_t(d->sms) * 4) blocks = int64_t(d->sms) * 4;
+    if (blocks < 1) blocks = 1;
+    ws_begin_kernel<<<unsigned(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ws);
+    if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return RMSNORM_OK;
+}
+
+extern "C" int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t hidden, float *dweight,
+                                rmsnorm_stream_t stream) {
+    int rc = ws_checks(workspace, n_logical_rows, hidden);
+    if (rc) return rc;
+    if (!dweight) return RMSNORM_ERR_NULL;
+    if (!aligned16(dweight)) return RMSNORM_ERR_ALIGN;
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    WsView ws = ws_view(workspace, n_logical_rows, hidden);
+    const int V = int(hidden / 8);
+    const unsigned gx = unsigned((V + 31) / 32);
+    if (ws.n_blocks == 0) {
+        zero_f32_kernel<<<1, 256, 0, s>>>(dweight, hidden);
+        if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        return RMSNORM_OK;
+    }
+    // pass 1 reads the block partials (rebuilding cut blocks); later passes
+    // ping-pong between the two scratch areas; the last pass writes dweight.
+    int64_t n = ws.n_blocks;
+    const float *in = nullptr;
+    bool first = true;
+    int flip = 0;
+    while (true) {
+        const int64_t groups = (n + kBlockRows - 1) / kBlockRows;
+        float *out = groups == 1 ? dweight : (flip ? ws.scratch_b : ws.scratch_a);
+        tree_pass_kernel<<<dim3(gx, unsigned(groups)), 256, 0, s>>>(ws, in, out, n, first ? 1 : 0);
+        if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (groups == 1) break;
+        in = out;
+        n = groups;
+        first = false;
+        flip ^= 1;
+    }
+    return RMSNORM_OK;
+}
+
+extern "C" int rmsnorm_dweight_status(const void *workspace, rmsnorm_stream_t stream, int32_t *status) {
+    if (!workspace || !status) return RMSNORM_ERR_NULL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const WsHeader *h = static_cast<const WsHeader *>(workspace);
+    if (cudaMemcpyAsync(status, &h->status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
+extern "C" const char *rmsnorm_strerror(int code) {
+    switch (code) {
+        case RMSNORM_OK: return "ok";
+        case RMSNORM_ERR_NULL: return "a required pointer is NULL";
+        case RMSNORM_ERR_HIDDEN: return "hidden size not supported";
+        case RMSNORM_ERR_ALIGN: return "pointer not 16-byte aligned or stride not a multiple of 8";
+        case RMSNORM_ERR_STRIDE: return "token_stride smaller than rows_per_token * hidden";
+        case RMSNORM_ERR_LAYOUT: return "invalid layout sizes";
+        case RMSNORM_ERR_WORKSPACE: return "workspace too small";
+        case RMSNORM_ERR_PLAN: return "dweight contribution needs a plan";
+        case RMSNORM_ERR_ID: return "token id out of range";
+        case RMSNORM_ERR_DUPLICATE: return "logical token appears twice in one call";
+        case RMSNORM_ERR_CAPACITY: return "plan buffer too small";
+        case RMSNORM_ERR_CUDA: return "CUDA runtime error";
+        case RMSNORM_ERR_DEVICE: return "device is not sm_103";
+        default: return "unknown error";
+    }
+}
+
+extern "C" int64_t rmsnorm_kernel_launches(void) { return g_launches.load(); }

@@ -1,0 +1,625 @@
+// Kernels of the batch-invariant RMSNorm library (sm_103a).
+//
+// Two kernel families share the numeric helpers of rbi_device.cuh:
+//
+//  * row_team_kernel (hidden > 256): a "team" of K CTAs (a thread-block
+//    cluster when K > 1) owns one row at a time; every thread owns one
+//    16-byte vector of 8 columns.  Rows are staged into shared memory by 1-D
+//    bulk copies (cp.async.bulk + mbarrier transaction counts) issued S
+//    batches ahead by one elected thread; each batch holds R rows.  Per batch
+//    the team forms the row sums (lane butterfly, then a butterfly over the
+//    warp partials, exchanged through distributed shared memory when K > 1),
+//    then writes y or dx and feeds the dweight leaves of the batch into the
+//    64-leaf tree held in registers.  CTAs are persistent: cluster c takes
+//    work units c, c + n_clusters, ...
+//
+//  * small_row_kernel (hidden <= 256): a team is P2 = next_pow2(hidden/8)
+//    lanes of one warp, so a warp works on 32/P2 rows at once with 16-byte
+//    vector loads straight into registers; the rows of a step are combined
+//    across teams by a butterfly before entering the 64-leaf tree.
+//
+// Work units are either plan items (64 row slots: a whole logical block in
+// logical order, or rows of blocks cut by a call boundary) or, without a
+// plan, 64 consecutive physical rows / R-row batches whose tok_id says
+// whether a row is active.  Which unit a CTA processes never changes a
+// value: every output depends only on its row (y, dx, the leaf) or on the
+// fixed trees.
+#pragma once
+#include "rbi_device.cuh"
+
+namespace rbi {
+
+enum Mode : int { kFwd = 0, kDx = 1, kDxDw = 2, kDw = 3 };
+
+__device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+struct KParams {
+    const uint16_t *x;
+    const uint16_t *dy;
+    const uint16_t *w;
+    uint16_t *out;                   // y (kFwd) or dx (kDx, kDxDw); may be null in kDxDw
+    float *rstd_out;                 // kFwd, optional
+    const int32_t *tok_id;
+    int64_t n_rows;                  // physical rows of the call = n_tokens * rpt
+    int64_t token_stride;            // elements
+    int32_t rpt;                     // rows per token
+    int32_t hidden;
+    float eps;
+    int32_t use_plan;                // 1: units are plan items
+    const PlanItem *items;
+    int64_t n_units;                 // plan items, or batches / 64-row groups without a plan
+    WsView ws;
+};
+
+__device__ __forceinline__ int64_t row_offset(const KParams &p, int64_t prow) {
+    if (p.rpt == 1) return prow * p.token_stride;
+    const int64_t t = prow / p.rpt;
+    return t * p.token_stride + (prow - t * p.rpt) * int64_t(p.hidden);
+}
+
+template <int MODE>
+struct ModeTraits {
+    static constexpr bool kNeedDy = MODE != kFwd;
+    static constexpr bool kNeedGx = MODE == kDx || MODE == kDxDw;   // sum(g*x) for dx
+    static constexpr bool kLeaves = MODE == kDxDw || MODE == kDw;
+    static constexpr bool kWritesOut = MODE != kDw;
+    static constexpr int kTensors = kNeedDy ? 2 : 1;
+};
+
+// Book-keeping of a whole block (one thread per team): it must not have been
+// contributed before, by a whole item or by spilled rows.
+__device__ __forceinline__ void mark_whole_block(const WsView &ws, int64_t b) {
+    bool dup = ws.block_state[b] != 0;
+    const uint64_t *f = reinterpret_cast<const uint64_t *>(ws.leaf_flag + b * kBlockRows);
+    const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
+    if (rows == kBlockRows) {
+#pragma unroll
+        for (int i = 0; i < kBlockRows / 8; ++i) dup |= f[i] != 0;
+    } else {
+        for (int64_t i = 0; i < rows; ++i) dup |= ws.leaf_flag[b * kBlockRows + i] != 0;
+    }
+    if (dup) set_status(ws.hdr, kStDouble);
+    ws.block_state[b] = 1;
+}
+
+__device__ __forceinline__ void mark_spilled_row(const WsView &ws, int64_t lrow) {
+    if (ws.leaf_flag[lrow] != 0 || ws.block_state[lrow / kBlockRows] != 0) set_status(ws.hdr, kStDouble);
+    ws.leaf_flag[lrow] = 1;
+}
+
+// =====================================================================
+// Large hidden sizes: team = K CTAs, one vector per thread, bulk-copy staging
+// =====================================================================
+
+struct StageMeta {
+    int64_t off;                     // element offset of this CTA's slice of the row, -1 = empty slot
+    int32_t lrow;                    // logical row (plan modes)
+    int32_t prow;                    // physical row
+};
+
+template <int R>
+struct SlotBatch {                   // metadata of one batch, held by the producer thread
+    int32_t prow[R];
+    int32_t lrow[R];
+};
+
+template <int MODE, int K, int R>
+__global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const int S) {
+    using T = ModeTraits<MODE>;
+    constexpr int kNB = kBlockRows / R;                 // batches per plan item
+    constexpr int kLogR = (R == 1) ? 0 : (R == 2) ? 1 : (R == 4) ? 2 : 3;
+    constexpr int kNVal = T::kNeedGx ? 2 * R : R;       // row sums reduced per batch
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                       // [8]
+    int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + 64);
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + 128);               // [S][R]
+    float *red = reinterpret_cast<float *>(smem + 128 + 8 * 8 * 16);           // [2][kNVal][32]
+    uint8_t *stages = smem + 128 + 8 * 8 * 16 + 2 * 16 * 32 * 4;               // [S][T][R][slice]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const uint32_t rank = (K > 1) ? cluster_rank() : 0u;
+    const int H = p.hidden;
+    const int V = H >> 3;
+    const int Vc = V / K;                                // vectors per CTA
+    const bool has_vec = tid < Vc;
+    const int W = (K == 1) ? ((V + 31) >> 5) : nwarps * K;
+    int Wp2 = 1;
+    while (Wp2 < W) Wp2 <<= 1;
+    const uint32_t slice_bytes = uint32_t(Vc) * 16u;
+    const int64_t col0 = int64_t(rank) * Vc * 8;        // first column of this CTA
+    const int64_t my_col = col0 + int64_t(tid) * 8;     // first column of this thread
+    const float Hf = float(H);
+
+    const int64_t cluster_id = blockIdx.x / K;
+    const int64_t n_clusters = gridDim.x / K;
+    const int64_t my_units = p.n_units > cluster_id ? (p.n_units - cluster_id + n_clusters - 1) / n_clusters : 0;
+    const int64_t per_unit = p.use_plan ? kNB : 1;
+    const int64_t n_batches = my_units * per_unit;
+
+    auto stage_ptr = [&](int s, int t, int r) -> uint8_t * {
+        return stages + ((int64_t(s) * T::kTensors + t) * R + r) * slice_bytes;
+    };
+
+    // ---- producer (thread 0): metadata of batch k, loaded one batch ahead
+    auto load_meta = [&](int64_t k, SlotBatch<R> &mb) {
+        if (k >= n_batches) return;
+        if (p.use_plan) {
+            const PlanItem *it = p.items + (cluster_id + (k / kNB) * n_clusters);
+            const int sub = int(k % kNB);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                mb.prow[r] = it->prow[sub * R + r];
+                mb.lrow[r] = it->lrow[sub * R + r];
+            }
+        } else {
+            const int64_t gb = cluster_id + k * n_clusters;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int64_t row = gb * R + r;
+                int32_t id = -1;
+                if (row < p.n_rows) id = p.tok_id[row / p.rpt];
+                mb.prow[r] = id >= 0 ? int32_t(row) : -1;
+                mb.lrow[r] = -1;
+            }
+        }
+    };
+    auto issue = [&](int64_t k, const SlotBatch<R> &mb) {
+        if (k >= n_batches) return;
+        const int s = int(k % S);
+        StageMeta *m = meta + s * R;
+        uint32_t n_act = 0;
+        int64_t offs[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            int32_t pr = mb.prow[r], lr = mb.lrow[r];
+            bool act = pr >= 0;
+            if (act && (pr >= p.n_rows || (T::kLeaves && (lr < 0 || lr >= p.ws.n_rows)))) {
+                if (T::kLeaves) set_status(p.ws.hdr, kStPlan);
+                act = false;
+            }
+            offs[r] = act ? row_offset(p, pr) + col0 : -1;
+            m[r].off = offs[r];
+            m[r].lrow = lr;
+            m[r].prow = pr;
+            n_act += act ? 1u : 0u;
+        }
+        mbar_arrive_expect_tx(&bars[s], n_act * slice_bytes * T::kTensors);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (offs[r] < 0) continue;
+            bulk_copy_g2s(stage_ptr(s, 0, r), p.x + offs[r], slice_bytes, &bars[s]);
+            if (T::kNeedDy) bulk_copy_g2s(stage_ptr(s, 1, r), p.dy + offs[r], slice_bytes, &bars[s]);
+        }
+    };
+
+    SlotBatch<R> next_meta;
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (K > 1) cluster_barrier(); else __syncthreads();
+    if (tid == 0) {
+        SlotBatch<R> mb;
+        for (int64_t k = 0; k < S - 1; ++k) {
+            load_meta(k, mb);
+            issue(k, mb);
+        }
+        load_meta(S - 1, next_meta);
+    }
+
+    float wv[8];
+    if (MODE != kDw && has_vec) unpack8(*reinterpret_cast<const uint4 *>(p.w + my_col), wv);
+
+    TreeStack<8> tree;                 // levels >= log2(R): partials of the current block
+    int32_t kind = 0, block = -1;
+
+#pragma unroll 1
+    for (int64_t k = 0; k < n_batches; ++k) {
+        const int s = int(k % S);
+        const uint32_t parity = uint32_t((k / S) & 1);
+        const int sub = int(k % per_unit);
+        if (p.use_plan && T::kLeaves && sub == 0) {
+            const PlanItem *it = p.items + (cluster_id + (k / kNB) * n_clusters);
+            kind = it->kind;
+            block = it->block;
+            if ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1)) {
+                if (tid == 0 && rank == 0) set_status(p.ws.hdr, kStPlan);
+                kind = 2;                                  // malformed item: contributes nothing
+            }
+        }
+        if (!mbar_wait_bounded(&bars[s], parity)) {
+            *abort_flag = 1;
+            if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
+        }
+        const StageMeta *m = meta + s * R;
+
+        // ---- per-thread partial row sums
+        float val[kNVal];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float a = 0.f, b = 0.f;
+            if (m[r].off >= 0 && has_vec) {
+                float xf[8];
+                unpack8(ld_shared_v4(stage_ptr(s, 0, r) + tid * 16), xf);
+                a = dot8(xf, xf);
+                if (T::kNeedGx) {
+                    float df[8], gf[8];
+                    unpack8(ld_shared_v4(stage_ptr(s, 1, r) + tid * 16), df);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) gf[i] = __fmul_rn(df[i], wv[i]);
+                    b = dot8(gf, xf);
+                }
+            }
+            val[r] = a;
+            if (T::kNeedGx) val[R + r] = b;
+        }
+#pragma unroll
+        for (int j = 0; j < kNVal; ++j) val[j] = lane_tree(val[j], 32);
+        float *rb = red + (k & 1) * (2 * 16 * 32);
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < kNVal; ++j) rb[j * 32 + warp] = val[j];
+        }
+        if (K > 1) cluster_barrier(); else __syncthreads();
+        {
+            int ab = *abort_flag;
+            if (K > 1) {
+#pragma unroll
+                for (int q = 0; q < K; ++q)
+                    ab |= __float_as_int(ld_cluster_f32(map_to_rank(smem_addr(abort_flag), uint32_t(q))));
+            }
+            if (ab) {
+                // give copies still in flight into our stages a bounded time to land
+                if (tid == 0)
+                    for (int64_t kk = k + 1; kk < k + S - 1 && kk < n_batches; ++kk)
+                        mbar_wait_bounded(&bars[kk % S], uint32_t((kk / S) & 1));
+                break;
+            }
+        }
+        if (tid == 0) {
+            SlotBatch<R> cur = next_meta;
+            issue(k + S - 1, cur);
+            load_meta(k + S, next_meta);
+        }
+
+        // ---- team sums: butterfly over the warp partials (zero-padded)
+#pragma unroll
+        for (int j = 0; j < kNVal; ++j) {
+            float v = 0.f;
+            if (lane < W) {
+                if (K == 1) {
+                    v = rb[j * 32 + lane];
+                } else {
+                    const uint32_t src = smem_addr(rb + j * 32 + (lane % nwarps));
+                    v = ld_cluster_f32(map_to_rank(src, uint32_t(lane / nwarps)));
+                }
+            }
+            v = lane_tree(v, Wp2);
+            val[j] = __shfl_sync(kFull, v, 0);
+        }
+
+        // ---- outputs and dweight leaves
+        TreeStack<8> mini;             // levels < log2(R): the batch's own subtree
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool act = m[r].off >= 0;
+            const float rstd = row_rstd(val[r], Hf, p.eps);
+            float leaf[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) leaf[i] = 0.f;
+            if (act && has_vec) {
+                float xf[8], xh[8], o[8];
+                unpack8(ld_shared_v4(stage_ptr(s, 0, r) + tid * 16), xf);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) xh[i] = __fmul_rn(xf[i], rstd);
+                if (MODE == kFwd) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) o[i] = __fmul_rn(xh[i], wv[i]);
+                    st_global_v4(p.out + m[r].off + tid * 8, pack8(o));
+                } else {
+                    float df[8];
+                    unpack8(ld_shared_v4(stage_ptr(s, 1, r) + tid * 16), df);
+                    if (T::kNeedGx && p.out != nullptr) {
+                        const float mg = row_mean_gxhat(val[R + r], rstd, Hf);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float g = __fmul_rn(df[i], wv[i]);
+                            o[i] = __fmul_rn(rstd, __fmaf_rn(-xh[i], mg, g));
+                        }
+                        st_global_v4(p.out + m[r].off + tid * 8, pack8(o));
+                    }
+                    if (T::kLeaves) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) leaf[i] = __fmul_rn(df[i], xh[i]);
+                    }
+                }
+            }
+            if (MODE == kFwd && act && p.rstd_out != nullptr && tid == 0 && rank == 0)
+                p.rstd_out[m[r].prow] = rstd;
+            if (T::kLeaves) {
+                if (kind == 0) {
+                    mini.push(leaf, r, 0);
+                    if (r == R - 1) {
+                        tree.push(leaf, sub, kLogR);
+                        if (sub == kNB - 1) {             // leaf[] is the block partial
+                            if (has_vec) {
+                                float *dst = p.ws.block_partial + int64_t(block) * H + my_col;
+                                st_global_f32x4(dst, leaf[0], leaf[1], leaf[2], leaf[3]);
+                                st_global_f32x4(dst + 4, leaf[4], leaf[5], leaf[6], leaf[7]);
+                            }
+                            if (tid == 0 && rank == 0) mark_whole_block(p.ws, block);
+                        }
+                    }
+                } else if (kind == 1 && act) {
+                    if (has_vec) {
+                        float *dst = p.ws.spill + int64_t(m[r].lrow) * H + my_col;
+                        st_global_f32x4(dst, leaf[0], leaf[1], leaf[2], leaf[3]);
+                        st_global_f32x4(dst + 4, leaf[4], leaf[5], leaf[6], leaf[7]);
+                    }
+                    if (tid == 0 && rank == 0) mark_spilled_row(p.ws, m[r].lrow);
+                }
+            }
+        }
+    }
+    if (K > 1) cluster_barrier();      // peers may still read our partials
+}
+
+// =====================================================================
+// Small hidden sizes: team = P2 lanes of a warp, register-direct loads
+// =====================================================================
+
+template <int MODE, int P2, int U>
+__global__ void __launch_bounds__(256) small_row_kernel(const KParams p) {
+    using T = ModeTraits<MODE>;
+    constexpr int TPW = 32 / P2;                         // teams (rows) per warp step
+    constexpr int kSteps = kBlockRows / TPW;             // steps per 64-slot unit
+    constexpr int kLogTPW = (TPW == 1) ? 0 : (TPW == 2) ? 1 : (TPW == 4) ? 2 : (TPW == 8) ? 3 : (TPW == 16) ? 4 : 5;
+    static_assert(kSteps % U == 0 || U >= kSteps, "steps per unit must be a multiple of U");
+    constexpr int kU = U < kSteps ? U : kSteps;
+
+    const int lane = threadIdx.x & 31;
+    const int team = lane / P2, tl = lane % P2;
+    const int H = p.hidden, V = H >> 3;
+    const bool has_vec = tl < V;
+    const float Hf = float(H);
+    const int64_t gwarp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+
+    float wv[8];
+    if (MODE != kDw && has_vec) unpack8(*reinterpret_cast<const uint4 *>(p.w + tl * 8), wv);
+
+#pragma unroll 1
+    for (int64_t u = gwarp; u < p.n_units; u += nwarps) {
+        const PlanItem *it = p.use_plan ? p.items + u : nullptr;
+        int32_t kind = 0, block = -1;
+        if (it) {
+            kind = it->kind;
+            block = it->block;
+            if (T::kLeaves && ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1))) {
+                if (lane == 0) set_status(p.ws.hdr, kStPlan);
+                kind = 2;                                  // malformed item: contributes nothing
+            }
+        }
+        TreeStack<8> tree;
+#pragma unroll 1
+        for (int st0 = 0; st0 < kSteps; st0 += kU) {
+            // resolve slots and issue loads for kU steps
+            int64_t off[kU];
+            int32_t lrow[kU], prow[kU];
+            uint4 xv[kU], dv[kU];
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const int slot = (st0 + q) * TPW + team;
+                int32_t pr, lr = -1;
+                if (it) {
+                    pr = it->prow[slot];
+                    lr = it->lrow[slot];
+                } else {
+                    const int64_t row = u * kBlockRows + slot;
+                    pr = (row < p.n_rows && p.tok_id[row / p.rpt] >= 0) ? int32_t(row) : -1;
+                }
+                bool act = pr >= 0;
+                if (act && (pr >= p.n_rows || (T::kLeaves && (lr < 0 || lr >= p.ws.n_rows)))) {
+                    if (T::kLeaves && tl == 0) set_status(p.ws.hdr, kStPlan);
+                    act = false;
+                }
+                off[q] = act ? row_offset(p, pr) + tl * 8 : -1;
+                lrow[q] = lr;
+                prow[q] = pr;
+                xv[q] = make_uint4(0, 0, 0, 0);
+                dv[q] = make_uint4(0, 0, 0, 0);
+                if (act && has_vec) {
+                    xv[q] = ld_global_stream_v4(p.x + off[q]);
+                    if (T::kNeedDy) dv[q] = ld_global_stream_v4(p.dy + off[q]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const bool act = off[q] >= 0;
+                float xf[8], df[8];
+                unpack8(xv[q], xf);
+                unpack8(dv[q], df);
+                float ss = 0.f, gx = 0.f;
+                if (act && has_vec) {
+                    ss = dot8(xf, xf);
+                    if (T::kNeedGx) {
+                        float gf[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) gf[i] = __fmul_rn(df[i], wv[i]);
+                        gx = dot8(gf, xf);
+                    }
+                }
+                ss = lane_tree(ss, P2);
+                if (T::kNeedGx) gx = lane_tree(gx, P2);
+                const float rstd = row_rstd(ss, Hf, p.eps);
+                float leaf[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) leaf[i] = 0.f;
+                if (act && has_vec) {
+                    float xh[8], o[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) xh[i] = __fmul_rn(xf[i], rstd);
+                    if (MODE == kFwd) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) o[i] = __fmul_rn(xh[i], wv[i]);
+                        st_global_v4(p.out + off[q], pack8(o));
+                    } else {
+                        if (T::kNeedGx && p.out != nullptr) {
+                            const float mg = row_mean_gxhat(gx, rstd, Hf);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float g = __fmul_rn(df[i], wv[i]);
+                                o[i] = __fmul_rn(rstd, __fmaf_rn(-xh[i], mg, g));
+                            }
+                            st_global_v4(p.out + off[q], pack8(o));
+                        }
+                        if (T::kLeaves) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) leaf[i] = __fmul_rn(df[i], xh[i]);
+                        }
+                    }
+                }
+                if (MODE == kFwd && act && p.rstd_out != nullptr && tl == 0) p.rstd_out[prow[q]] = rstd;
+                if (T::kLeaves) {
+                    if (kind == 0) {
+                        // combine the TPW rows of this step (adjacent teams first)
+#pragma unroll
+                        for (int kk = P2; kk < 32; kk <<= 1)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) leaf[i] = __fadd_rn(leaf[i], __shfl_xor_sync(kFull, leaf[i], kk));
+                        tree.push(leaf, st0 + q, kLogTPW);
+                        if (st0 + q == kSteps - 1 && team == 0 && has_vec) {
+                            float *dst = p.ws.block_partial + int64_t(block) * H + tl * 8;
+                            st_global_f32x4(dst, leaf[0], leaf[1], leaf[2], leaf[3]);
+                            st_global_f32x4(dst + 4, leaf[4], leaf[5], leaf[6], leaf[7]);
+                        }
+                        if (st0 + q == kSteps - 1 && lane == 0) mark_whole_block(p.ws, block);
+                    } else if (kind == 1 && act) {
+                        if (has_vec) {
+                            float *dst = p.ws.spill + int64_t(lrow[q]) * H + tl * 8;
+                            st_global_f32x4(dst, leaf[0], leaf[1], leaf[2], leaf[3]);
+                            st_global_f32x4(dst + 4, leaf[4], leaf[5], leaf[6], leaf[7]);
+                        }
+                        if (tl == 0) mark_spilled_row(p.ws, lrow[q]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// =====================================================================
+// Workspace set-up and the final reduction
+// =====================================================================
+
+__global__ void ws_begin_kernel(WsView ws) {
+    const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = int64_t(gridDim.x) * blockDim.x;
+    // block_state and leaf_flag are contiguous up to the partials: clear both
+    uint8_t *base = ws.block_state;
+    const int64_t bytes = reinterpret_cast<uint8_t *>(ws.block_partial) - base;   // multiple of 256
+    uint4 *b4 = reinterpret_cast<uint4 *>(base);
+    for (int64_t i = tid; i < bytes / 16; i += nthr) b4[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) {
+        ws.hdr->n_rows = ws.n_rows;
+        ws.hdr->hidden = ws.hidden;
+        ws.hdr->n_blocks = ws.n_blocks;
+        ws.hdr->status = 0;
+        ws.hdr->magic = kWsMagic;
+    }
+}
+
+// One pass of the carry tree over `n_in` partials [n_in][H]: group j of 64
+// consecutive inputs is reduced to out[j] (complete 64-tree for a full group,
+// carry tree for a last partial group).  Thread (v, q) reduces the inputs
+// [8q, 8q+8) of the group for columns 8v..8v+7 (levels 1-3); one thread per
+// vector then reduces the up to 8 subgroup results (levels 4-6).  Splitting
+// at aligned power-of-two subgroups leaves the tree unchanged.  In the first
+// pass (from_blocks) an input block cut by a call boundary is rebuilt from
+// its spilled rows with the same 64-leaf tree as the in-kernel path.
+__device__ __forceinline__ void load8(const float *src, float (&v)[8]) {
+    const float4 a = ld_global_f32x4(src), b = ld_global_f32x4(src + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__global__ void __launch_bounds__(256) tree_pass_kernel(WsView ws, const float *in, float *out, int64_t n_in,
+                                                        int from_blocks) {
+    __shared__ float part[8][32][8];                     // [q][vector in CTA][column]
+    const int H = int(ws.hidden), V = H >> 3;
+    const int vl = threadIdx.x & 31, q = threadIdx.x >> 5;
+    const int v = blockIdx.x * 32 + vl;
+    const bool has_vec = v < V;
+    const int64_t j = blockIdx.y;
+    const int64_t g0 = j * kBlockRows;
+    const int64_t m = min64(kBlockRows, n_in - g0);   // inputs in this group
+    if (from_blocks && !header_ok(ws)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) set_status(ws.hdr, kStHeader);
+        return;                                          // uniform across the CTA
+    }
+    const int cnt = int(max64(0, min64(8, m - int64_t(q) * 8)));
+    TreeStack<8> st;
+    for (int i = 0; i < cnt; ++i) {
+        const int64_t b = g0 + int64_t(q) * 8 + i;
+        float val[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) val[c] = 0.f;
+        if (from_blocks && ws.block_state[b] == 0) {
+            const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
+            if (vl == 0 && blockIdx.x == 0) {
+                bool missing = false;
+                for (int64_t r = 0; r < rows; ++r) missing |= ws.leaf_flag[b * kBlockRows + r] == 0;
+                if (missing) set_status(ws.hdr, kStMissing);
+            }
+            TreeStack<8> lt;
+#pragma unroll 1
+            for (int r = 0; r < kBlockRows; ++r) {
+                float leaf[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) leaf[c] = 0.f;
+                if (r < rows && has_vec) load8(ws.spill + (b * kBlockRows + r) * int64_t(H) + int64_t(v) * 8, leaf);
+                lt.push(leaf, r, 0);
+                if (r == kBlockRows - 1) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) val[c] = leaf[c];
+                }
+            }
+        } else if (has_vec) {
+            load8((from_blocks ? ws.block_partial : in) + b * int64_t(H) + int64_t(v) * 8, val);
+        }
+        st.push(val, i, 0);
+    }
+    if (cnt > 0) {
+        float acc[8];
+        st.fold(cnt, acc);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) part[q][vl][c] = acc[c];
+    }
+    __syncthreads();
+    if (q == 0 && has_vec) {
+        const int ns = int((m + 7) / 8);
+        TreeStack<8> st2;
+        for (int i = 0; i < ns; ++i) {
+            float val[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) val[c] = part[i][vl][c];
+            st2.push(val, i, 0);
+        }
+        float res[8];
+        st2.fold(ns, res);
+        float *dst = out + j * int64_t(H) + int64_t(v) * 8;
+        st_global_f32x4(dst, res[0], res[1], res[2], res[3]);
+        st_global_f32x4(dst + 4, res[4], res[5], res[6], res[7]);
+    }
+}
+
+__global__ void zero_f32_kernel(float *p, int64_t n) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
+        p[i] = 0.f;
+}
+
+}  // namespace rbi

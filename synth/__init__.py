@@ -180,7 +180,7 @@ def config(name: str, seed: int = 0) -> Workload:
                         chunk_rows=[7, 4, 7, 7, 2, 7, 6, 7, 7, 5], seed=seed)
     if name == "c0p":
         return Workload("c0p", 8, np.array([11, 16, 13, 19]), dy_std=1.0,
-                        chunk_rows=7, seed=seed, extra={"per_sample_chunks": True})
+                        chunk_rows=7, seed=seed, extra={"per_sample_chunks": True, "slot": 20})
     if name == "c1":
         return Workload("c1", 4096, lengths_uniform(seed + 1, 8, 512, 4096),
                         chunk_rows=1024, seed=seed)

@@ -1,0 +1,127 @@
+"""Layout mapper and host planner (CPU only)."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from invariant_rmsnorm_fwd_gb300 import layout as L
+from invariant_rmsnorm_fwd_gb300.harness import layouts_differ
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_pages_worked_layout_table_is_reproduced():
+    g = json.load(open(os.path.join(GOLD, "pages_layout.json")))
+    wl = synth.config("c0p")
+    assert list(wl.lengths) == g["sample_lengths"] and wl.hidden == g["hidden"]
+    lays = L.workload_layouts(wl)
+    for cell, want in g["cells"].items():
+        if cell == "singleton_s0":
+            lay = lays["singleton"]
+            assert lay.rows_per_call[0] == want["rows"][0]
+            assert len(lay.calls) == len(wl.lengths)
+            continue
+        lay = lays[cell]
+        assert len(lay.calls) == want["calls"], cell
+        assert lay.rows_per_call == want["rows"], cell
+
+
+def test_c0_chunk_boundaries_over_packed_stream():
+    lay = L.workload_layouts(synth.config("c0"))["chunked"]
+    assert list(np.cumsum(lay.rows_per_call)) == [7, 11, 18, 25, 27, 34, 40, 47, 54, 59]
+    assert L.workload_layouts(synth.config("c0"))["padded_right"].rows_per_call == [80]
+
+
+@pytest.mark.parametrize("cfg", ["c0", "c0p", "c1", "c2", "c3", "c4"])
+def test_every_layout_is_a_partition_and_differs_from_full(cfg):
+    wl = synth.config(cfg)
+    lays = L.workload_layouts(wl)
+    for name, lay in lays.items():
+        lay.check_partition()
+        if name != "full":
+            assert layouts_differ(lays["full"], lay), name
+
+
+def test_logical_id_is_layout_independent():
+    lengths = np.array([3, 1, 2])
+    perm = L.make_layout("permuted", lengths, perm=np.array([2, 0, 1]))
+    assert list(perm.calls[0]) == [4, 5, 0, 1, 2, 3]
+    left = L.make_layout("padded_left", lengths, slot=3)
+    assert list(left.calls[0]) == [0, 1, 2, -1, -1, 3, -1, 4, 5]
+
+
+def test_partition_check_rejects_duplicates():
+    lay = L.Layout("bad", [np.array([0, 1], np.int32), np.array([1, 2], np.int32)], 3)
+    with pytest.raises(ValueError):
+        lay.check_partition()
+
+
+# ------------------------------------------------------------------ planner
+
+def _items(buf, n):
+    a = np.frombuffer(buf.tobytes(), dtype=np.int32).reshape(n, 132)
+    return a[:, 0], a[:, 1], a[:, 2], a[:, 4:68], a[:, 68:132]
+
+
+def _plan(tok, rpt, ntok):
+    import invariant_rmsnorm_fwd_gb300 as rb
+    return rb.plan_build(tok, rpt, ntok)
+
+
+@pytest.mark.parametrize("cfg,kind,rpt", [("c0", "chunked", 1), ("c0", "padded_left", 1), ("c0p", "singleton", 1),
+                                          ("c1", "chunked", 1), ("c2", "padded_right_chunked", 1),
+                                          ("c3", "chunked", 32), ("c4", "permuted_slots_left_chunked", 1)])
+def test_plan_covers_every_active_row_once(cfg, kind, rpt):
+    wl = synth.config(cfg)
+    lay = L.workload_layouts(wl, kinds=[kind])[kind]
+    N = wl.n_tokens * rpt
+    seen = np.zeros(N, dtype=np.int64)
+    whole_blocks = []
+    for tok in lay.calls[:40]:
+        buf, n, whole, spill = _plan(tok, rpt, wl.n_tokens)
+        kind_a, block, count, prow, lrow = _items(buf, n)
+        assert np.all(kind_a[:whole] == 0) and np.all(kind_a[whole:] == 1)
+        for i in range(n):
+            used = lrow[i][lrow[i] >= 0]
+            pr = prow[i][lrow[i] >= 0]
+            assert used.size == count[i]
+            # physical row -> token slot -> logical id agrees with the plan
+            assert np.array_equal(tok[pr // rpt].astype(np.int64) * rpt + pr % rpt, used)
+            seen[used] += 1
+            if kind_a[i] == 0:
+                b = block[i]
+                assert np.array_equal(used, np.arange(b * 64, min(b * 64 + 64, N)))
+                whole_blocks.append(b)
+        assert int(np.sum(count[whole:])) == spill
+    assert seen.max() <= 1
+    assert len(set(whole_blocks)) == len(whole_blocks)
+
+
+def test_plan_whole_vs_cut_blocks():
+    tok = np.arange(0, 130, dtype=np.int32)              # ids 0..129 of N=200: blocks 0,1 whole, block 2 cut
+    buf, n, whole, spill = _plan(tok, 1, 200)
+    assert (whole, spill) == (2, 2)
+    tok = np.arange(128, 200, dtype=np.int32)            # block 2 (128..191) whole, block 3 (192..199) whole
+    buf, n, whole, spill = _plan(tok, 1, 200)
+    assert (whole, spill) == (2, 0)
+
+
+def test_plan_rejects_bad_ids():
+    import invariant_rmsnorm_fwd_gb300 as rb
+    with pytest.raises(rb.RmsNormError) as e:
+        _plan(np.array([0, 1, 1], np.int32), 1, 5)
+    assert e.value.code == -9
+    with pytest.raises(rb.RmsNormError) as e:
+        _plan(np.array([0, 5], np.int32), 1, 5)
+    assert e.value.code == -8
+    with pytest.raises(rb.RmsNormError):
+        _plan(np.array([-2], np.int32), 1, 5)
+
+
+def test_plan_is_a_function_of_the_ids_only():
+    tok = synth.seeded_permutation(3, 300).astype(np.int32)
+    a = _plan(tok, 1, 300)[0]
+    b = _plan(tok.copy(), 1, 300)[0]
+    assert np.array_equal(a, b)
