@@ -81,14 +81,22 @@ class ClockSampler:
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
 
     def start(self):
+        """Start sampling every 100 ms; returns once the first sample is on disk (or after 5 s)."""
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5.0:
+            self.fh.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -350,8 +358,14 @@ def main():
     launches0 = rb.kernel_launches()
     clocks.start()
     ms, bwd_ms = time_steps(multi, stream, args.steps, args.warmup, flush, dist, time_bwd=True)
-    clk = clocks.stop()
     launches = (rb.kernel_launches() - launches0) // (args.steps + args.warmup)
+    # keep the same step running (untimed) so the clock samples cover the load
+    t_end = time.time() + 0.6
+    while time.time() < t_end:
+        for _ in range(20):
+            multi.run(stream)
+        torch.cuda.synchronize()
+    clk = clocks.stop()
     ms_step = statistics.mean(ms)
     if dist is not None:
         t = torch.tensor([ms_step], device=device)

@@ -139,7 +139,7 @@ class CallLayout:
         return _Layout(self.n_tokens, self.rows_per_token, 0, token_stride,
                        self.tok_id.data_ptr() if self.n_tokens else None,
                        self.n_logical_tokens,
-                       self.plan.data_ptr() if self.plan is not None and self.plan_items else None,
+                       self.plan.data_ptr() if self.plan is not None else None,
                        self.plan_items)
 
 

@@ -239,16 +239,110 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// ----------------------------------------------------------------- packed FP32x2
+//
+// sm_100-class GPUs execute two FP32 lanes per instruction (add/mul/fma
+// .rn.f32x2).  Each lane is an ordinary IEEE binary32 round-to-nearest-even
+// operation, so values are the same as with scalar __fadd_rn/__fmul_rn/
+// __fmaf_rn; only the instruction count halves.
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+// 8 bf16 (one uint4) -> 4 float2 holding columns (0,1), (2,3), (4,5), (6,7).
+__device__ __forceinline__ void unpack8x2(const uint4 &v, float2 (&f)[4]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint4 pack8x2(const float2 (&f)[4]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(f[i].x, f[i].y);
+        w[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Vector sum of the large-hidden kernels: columns 0,2,4,6 and 1,3,5,7 are
+// folded in two FMA chains (a0*b0, then fma with the next column of the
+// chain), and the two chains are added: (even chain) + (odd chain).
+__device__ __forceinline__ float dot8x2(const float2 (&a)[4], const float2 (&b)[4]) {
+    float2 s = mul2(a[0], b[0]);
+#pragma unroll
+    for (int i = 1; i < 4; ++i) s = fma2(a[i], b[i], s);
+    return __fadd_rn(s.x, s.y);
+}
+
+// Warp "transpose-reduce" of NV values per lane (NV a power of two <= 32):
+// value j's 32 lane terms are added by a complete tree that pairs lanes 16
+// apart first, then 8, 4, 2, 1.  On return lane l holds the warp total of
+// value j = l >> (5 - log2 NV).  Each pair sum is formed once, by the lane
+// that keeps it; NV-1 exchanges plus log2(32/NV) butterflies in all.
+template <int NV>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[NV], int lane) {
+#pragma unroll
+    for (int c = NV, d = 16; c > 1; c >>= 1, d >>= 1) {
+        const bool upper = (lane & d) != 0;
+        const int h = c >> 1;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? v[i] : v[i + h];
+            const float keep = upper ? v[i + h] : v[i];
+            v[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, d));
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int d = 16 / NV; d >= 1; d >>= 1) r = __fadd_rn(r, __shfl_xor_sync(kFull, r, d));
+    return r;
+}
+
 // ----------------------------------------------------------------- row sums
 //
-// Canonical row-sum tree for hidden size H (V = H/8 vectors of 8 columns):
-//  1. each vector's 8 terms are folded in column order with fused multiply-
-//     adds: s = a0*b0; s = fma(a_i, b_i, s) for i = 1..7;
-//  2. the V vector sums, zero-padded to P = next power of two >= V, are
-//     added by a complete pairwise tree with adjacent pairing: (0,1), (2,3),
-//     ..., then adjacent pairs of those, and so on.
-// The tree depends on H only.  The kernels realise step 2 as xor-butterflies
-// (xor 1, 2, 4, ...) over lanes and then over warps, which is this tree.
+// Canonical row-sum trees.  The sum of squares (and, in the backward, the
+// sum of dy*w*x) of a row is formed by a tree that depends on H only:
+//
+//  hidden <= 256 (small_row_kernel): each 8-column vector is folded in
+//   column order with fused multiply-adds (s = a0*b0; s = fma(ai, bi, s)),
+//   then the V = H/8 vector sums, zero-padded to P = next_pow2(V), are added
+//   by a complete tree with adjacent pairing: (0,1), (2,3), ... (xor
+//   butterflies 1, 2, 4, ...).
+//  hidden > 256 (row_team_kernel): each vector is folded as two chains
+//   (columns 0,2,4,6 and 1,3,5,7, see dot8x2) that are then added; the 32
+//   vectors of warp w (vectors 32w..32w+31, absent ones +0) by a complete
+//   tree pairing lanes 16 apart first, then 8, 4, 2, 1; the W warp sums by
+//   adding warp w+32 to warp w when W > 32, then the same tree over the 32
+//   slots (absent warps +0).
+//
+// The forward and the backward use the same kernel family for a given H, so
+// rstd is bitwise the same in both.
 
 __device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8]) {
     float s = __fmul_rn(a[0], b[0]);
@@ -326,6 +420,45 @@ struct TreeStack {
             } else {
 #pragma unroll
                 for (int c = 0; c < NCOL; ++c) res[c] = __fadd_rn(s[l][c], res[c]);
+            }
+        }
+    }
+};
+
+// Same tree over float2 column pairs.  push_static is for compile-time item
+// indices (the rows of one batch); push_dyn for a run-time index that is
+// uniform across the team (the batch within a block): the trailing one bits
+// of idx say how many pending partials the new subtree closes.
+template <int NC>
+struct TreeStack2 {
+    float2 s[kBlockLevels][NC];
+
+    template <int LEVEL>
+    __device__ __forceinline__ void push_static(float2 (&v)[NC], int idx) {
+#pragma unroll
+        for (int l = LEVEL; l < kBlockLevels; ++l) {
+            if ((idx >> (l - LEVEL)) & 1) {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) v[c] = add2(s[l][c], v[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) s[l][c] = v[c];
+                break;
+            }
+        }
+    }
+
+    template <int LEVEL>
+    __device__ __forceinline__ void push_dyn(float2 (&v)[NC], int idx) {
+        const int t = __ffs(~idx) - 1;                   // trailing ones of idx
+#pragma unroll
+        for (int l = LEVEL; l < kBlockLevels; ++l) {
+            if (l - LEVEL < t) {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) v[c] = add2(s[l][c], v[c]);
+            } else if (l - LEVEL == t) {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) s[l][c] = v[c];
             }
         }
     }

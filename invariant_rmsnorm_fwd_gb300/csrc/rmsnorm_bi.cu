@@ -97,8 +97,7 @@ int check_layout(const rmsnorm_layout_t *L, int64_t H) {
 
 // ---------------------------------------------------------------- launches
 
-constexpr int kHeaderSmem = 128 + 8 * 8 * 16 + 2 * 16 * 32 * 4;
-constexpr int kMaxStages = 8;
+constexpr int kHeaderSmem = kSmemStageOff;
 
 template <int MODE, int K, int R>
 int launch_team(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
@@ -195,7 +194,8 @@ int run_rows(KParams p, const Shape &sh, const rmsnorm_layout_t *L, cudaStream_t
     constexpr int R = (MODE == kFwd) ? 8 : 4;
     const bool plan = p.use_plan != 0;
     if (plan) {
-        p.n_units = L->plan_items;
+        // dweight modes work on whole plan items; the others on R-row batches of items
+        p.n_units = (ModeTraits<MODE>::kLeaves || sh.small) ? L->plan_items : L->plan_items * (kBlockRows / R);
     } else if (sh.small) {
         p.n_units = (p.n_rows + kBlockRows - 1) / kBlockRows;
     } else {

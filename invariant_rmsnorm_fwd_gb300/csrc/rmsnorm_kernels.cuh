@@ -104,19 +104,33 @@ struct SlotBatch {                   // metadata of one batch, held by the produ
     int32_t lrow[R];
 };
 
+// Shared-memory header of row_team_kernel: barriers, abort flag, per-stage
+// row metadata, and the warp partials of the row sums.
+constexpr int kMaxStages = 8;
+constexpr int kMaxBatch = 8;                     // R <= 8
+constexpr int kMaxTeamWarps = 64;                // W <= 64
+constexpr int kMaxVals = 16;                     // row sums per batch <= 16
+constexpr int kSmemMetaOff = 128;
+constexpr int kSmemRedOff = kSmemMetaOff + kMaxStages * kMaxBatch * 16;
+constexpr int kSmemStageOff = kSmemRedOff + 2 * 16 * kMaxVals * 4;   // [2 parity][16 local warps][kMaxVals]
+static_assert(kSmemStageOff % 128 == 0, "stage buffers are 128-byte aligned");
+
 template <int MODE, int K, int R>
 __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const int S) {
     using T = ModeTraits<MODE>;
     constexpr int kNB = kBlockRows / R;                 // batches per plan item
     constexpr int kLogR = (R == 1) ? 0 : (R == 2) ? 1 : (R == 4) ? 2 : 3;
-    constexpr int kNVal = T::kNeedGx ? 2 * R : R;       // row sums reduced per batch
+    constexpr int NV = T::kNeedGx ? 2 * R : R;          // row sums reduced per batch
+    constexpr int kLogNV = (NV == 2) ? 1 : (NV == 4) ? 2 : (NV == 8) ? 3 : 4;
+    constexpr int kSh = 5 - kLogNV;                     // lane >> kSh = value index after reduce
+    static_assert(NV <= kMaxVals && R <= kMaxBatch, "batch too large");
 
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                       // [8]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                       // [kMaxStages]
     int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + 64);
-    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + 128);               // [S][R]
-    float *red = reinterpret_cast<float *>(smem + 128 + 8 * 8 * 16);           // [2][kNVal][32]
-    uint8_t *stages = smem + 128 + 8 * 8 * 16 + 2 * 16 * 32 * 4;               // [S][T][R][slice]
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + kSmemMetaOff);      // [S][R]
+    float *red = reinterpret_cast<float *>(smem + kSmemRedOff);                // [2][16][NV]
+    uint8_t *stages = smem + kSmemStageOff;                                    // [S][T][R][slice]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
@@ -125,18 +139,19 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
     const int V = H >> 3;
     const int Vc = V / K;                                // vectors per CTA
     const bool has_vec = tid < Vc;
-    const int W = (K == 1) ? ((V + 31) >> 5) : nwarps * K;
-    int Wp2 = 1;
-    while (Wp2 < W) Wp2 <<= 1;
+    const int W = nwarps * K;                            // warps in the team
     const uint32_t slice_bytes = uint32_t(Vc) * 16u;
     const int64_t col0 = int64_t(rank) * Vc * 8;        // first column of this CTA
     const int64_t my_col = col0 + int64_t(tid) * 8;     // first column of this thread
     const float Hf = float(H);
 
+    // Work units: plan items (64 slots) for the dweight modes; single R-row
+    // batches otherwise (a batch of a plan item, or R consecutive physical rows).
+    const bool item_units = p.use_plan && T::kLeaves;
     const int64_t cluster_id = blockIdx.x / K;
     const int64_t n_clusters = gridDim.x / K;
     const int64_t my_units = p.n_units > cluster_id ? (p.n_units - cluster_id + n_clusters - 1) / n_clusters : 0;
-    const int64_t per_unit = p.use_plan ? kNB : 1;
+    const int64_t per_unit = item_units ? kNB : 1;
     const int64_t n_batches = my_units * per_unit;
 
     auto stage_ptr = [&](int s, int t, int r) -> uint8_t * {
@@ -147,8 +162,17 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
     auto load_meta = [&](int64_t k, SlotBatch<R> &mb) {
         if (k >= n_batches) return;
         if (p.use_plan) {
-            const PlanItem *it = p.items + (cluster_id + (k / kNB) * n_clusters);
-            const int sub = int(k % kNB);
+            int64_t item;
+            int sub;
+            if (item_units) {
+                item = cluster_id + (k / kNB) * n_clusters;
+                sub = int(k % kNB);
+            } else {
+                const int64_t gb = cluster_id + k * n_clusters;
+                item = gb / kNB;
+                sub = int(gb % kNB);
+            }
+            const PlanItem *it = p.items + item;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 mb.prow[r] = it->prow[sub * R + r];
@@ -174,7 +198,7 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
         int64_t offs[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            int32_t pr = mb.prow[r], lr = mb.lrow[r];
+            const int32_t pr = mb.prow[r], lr = mb.lrow[r];
             bool act = pr >= 0;
             if (act && (pr >= p.n_rows || (T::kLeaves && (lr < 0 || lr >= p.ws.n_rows)))) {
                 if (T::kLeaves) set_status(p.ws.hdr, kStPlan);
@@ -211,10 +235,10 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
         load_meta(S - 1, next_meta);
     }
 
-    float wv[8];
-    if (MODE != kDw && has_vec) unpack8(*reinterpret_cast<const uint4 *>(p.w + my_col), wv);
+    float2 wv[4];
+    if (MODE != kDw && has_vec) unpack8x2(*reinterpret_cast<const uint4 *>(p.w + my_col), wv);
 
-    TreeStack<8> tree;                 // levels >= log2(R): partials of the current block
+    TreeStack2<4> tree;                 // levels >= log2(R): partials of the current block
     int32_t kind = 0, block = -1;
 
 #pragma unroll 1
@@ -222,7 +246,7 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
         const int s = int(k % S);
         const uint32_t parity = uint32_t((k / S) & 1);
         const int sub = int(k % per_unit);
-        if (p.use_plan && T::kLeaves && sub == 0) {
+        if (item_units && sub == 0) {
             const PlanItem *it = p.items + (cluster_id + (k / kNB) * n_clusters);
             kind = it->kind;
             block = it->block;
@@ -237,33 +261,29 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
         }
         const StageMeta *m = meta + s * R;
 
-        // ---- per-thread partial row sums
-        float val[kNVal];
+        // ---- per-thread partial row sums, then the warp transpose-reduce
+        float val[NV];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             float a = 0.f, b = 0.f;
             if (m[r].off >= 0 && has_vec) {
-                float xf[8];
-                unpack8(ld_shared_v4(stage_ptr(s, 0, r) + tid * 16), xf);
-                a = dot8(xf, xf);
+                float2 xf[4];
+                unpack8x2(ld_shared_v4(stage_ptr(s, 0, r) + tid * 16), xf);
+                a = dot8x2(xf, xf);
                 if (T::kNeedGx) {
-                    float df[8], gf[8];
-                    unpack8(ld_shared_v4(stage_ptr(s, 1, r) + tid * 16), df);
+                    float2 df[4], gf[4];
+                    unpack8x2(ld_shared_v4(stage_ptr(s, 1, r) + tid * 16), df);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) gf[i] = __fmul_rn(df[i], wv[i]);
-                    b = dot8(gf, xf);
+                    for (int i = 0; i < 4; ++i) gf[i] = mul2(df[i], wv[i]);
+                    b = dot8x2(gf, xf);
                 }
             }
             val[r] = a;
             if (T::kNeedGx) val[R + r] = b;
         }
-#pragma unroll
-        for (int j = 0; j < kNVal; ++j) val[j] = lane_tree(val[j], 32);
-        float *rb = red + (k & 1) * (2 * 16 * 32);
-        if (lane == 0) {
-#pragma unroll
-            for (int j = 0; j < kNVal; ++j) rb[j * 32 + warp] = val[j];
-        }
+        const float wsum = warp_transpose_reduce<NV>(val, lane);
+        float *rb = red + (k & 1) * (16 * kMaxVals);     // [16 local warps][NV] per parity
+        if ((lane & ((1 << kSh) - 1)) == 0) rb[warp * kMaxVals + (lane >> kSh)] = wsum;
         if (K > 1) cluster_barrier(); else __syncthreads();
         {
             int ab = *abort_flag;
@@ -286,55 +306,78 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
             load_meta(k + S, next_meta);
         }
 
-        // ---- team sums: butterfly over the warp partials (zero-padded)
+        // ---- team sums: lane w takes warp w (+ warp w+32), then the same
+        // transpose-reduce over the 32 slots; every warp does it redundantly.
+        {
+            float tv[NV];
 #pragma unroll
-        for (int j = 0; j < kNVal; ++j) {
-            float v = 0.f;
-            if (lane < W) {
-                if (K == 1) {
-                    v = rb[j * 32 + lane];
-                } else {
-                    const uint32_t src = smem_addr(rb + j * 32 + (lane % nwarps));
-                    v = ld_cluster_f32(map_to_rank(src, uint32_t(lane / nwarps)));
+            for (int j = 0; j < NV; ++j) tv[j] = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int w = lane + 32 * half;
+                if (w < W) {
+                    const int cta = w / nwarps, lw = w - cta * nwarps;
+                    const float *src = rb + lw * kMaxVals;
+#pragma unroll
+                    for (int j = 0; j < NV; ++j) {
+                        float v;
+                        if (K == 1) v = src[j];
+                        else v = ld_cluster_f32(map_to_rank(smem_addr(src + j), uint32_t(cta)));
+                        tv[j] = half ? __fadd_rn(tv[j], v) : v;
+                    }
                 }
             }
-            v = lane_tree(v, Wp2);
-            val[j] = __shfl_sync(kFull, v, 0);
+            const float tsum = warp_transpose_reduce<NV>(tv, lane);
+            // lane l now holds team sum j = l >> kSh: ss_j (j < R) or gx_{j-R}
+            const int j = lane >> kSh;
+            const float rs = row_rstd(tsum, Hf, p.eps);               // meaningful for j < R
+            if (T::kNeedGx) {
+                const int src_lane = (j >= R ? j - R : j) << kSh;
+                const float rs_row = __shfl_sync(kFull, rs, src_lane);
+                const float mg = row_mean_gxhat(tsum, rs_row, Hf);    // meaningful for j >= R
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    val[r] = __shfl_sync(kFull, rs, r << kSh);
+                    val[R + r] = __shfl_sync(kFull, mg, (R + r) << kSh);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) val[r] = __shfl_sync(kFull, rs, r << kSh);
+            }
         }
 
         // ---- outputs and dweight leaves
-        TreeStack<8> mini;             // levels < log2(R): the batch's own subtree
+        TreeStack2<4> mini;            // levels < log2(R): the batch's own subtree
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const bool act = m[r].off >= 0;
-            const float rstd = row_rstd(val[r], Hf, p.eps);
-            float leaf[8];
+            const float rstd = val[r];
+            float2 leaf[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) leaf[i] = 0.f;
+            for (int i = 0; i < 4; ++i) leaf[i] = make_float2(0.f, 0.f);
             if (act && has_vec) {
-                float xf[8], xh[8], o[8];
-                unpack8(ld_shared_v4(stage_ptr(s, 0, r) + tid * 16), xf);
+                const float2 r2 = make_float2(rstd, rstd);
+                float2 xf[4], xh[4], o[4];
+                unpack8x2(ld_shared_v4(stage_ptr(s, 0, r) + tid * 16), xf);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) xh[i] = __fmul_rn(xf[i], rstd);
+                for (int i = 0; i < 4; ++i) xh[i] = mul2(xf[i], r2);
                 if (MODE == kFwd) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) o[i] = __fmul_rn(xh[i], wv[i]);
-                    st_global_v4(p.out + m[r].off + tid * 8, pack8(o));
+                    for (int i = 0; i < 4; ++i) o[i] = mul2(xh[i], wv[i]);
+                    st_global_v4(p.out + m[r].off + tid * 8, pack8x2(o));
                 } else {
-                    float df[8];
-                    unpack8(ld_shared_v4(stage_ptr(s, 1, r) + tid * 16), df);
+                    float2 df[4];
+                    unpack8x2(ld_shared_v4(stage_ptr(s, 1, r) + tid * 16), df);
                     if (T::kNeedGx && p.out != nullptr) {
-                        const float mg = row_mean_gxhat(val[R + r], rstd, Hf);
+                        const float nm = -val[R + r];
+                        const float2 nm2 = make_float2(nm, nm);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float g = __fmul_rn(df[i], wv[i]);
-                            o[i] = __fmul_rn(rstd, __fmaf_rn(-xh[i], mg, g));
-                        }
-                        st_global_v4(p.out + m[r].off + tid * 8, pack8(o));
+                        for (int i = 0; i < 4; ++i) o[i] = mul2(r2, fma2(xh[i], nm2, mul2(df[i], wv[i])));
+                        st_global_v4(p.out + m[r].off + tid * 8, pack8x2(o));
                     }
                     if (T::kLeaves) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) leaf[i] = __fmul_rn(df[i], xh[i]);
+                        for (int i = 0; i < 4; ++i) leaf[i] = mul2(df[i], xh[i]);
                     }
                 }
             }
@@ -342,14 +385,14 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
                 p.rstd_out[m[r].prow] = rstd;
             if (T::kLeaves) {
                 if (kind == 0) {
-                    mini.push(leaf, r, 0);
+                    if (R > 1) mini.template push_static<0>(leaf, r);
                     if (r == R - 1) {
-                        tree.push(leaf, sub, kLogR);
+                        tree.template push_dyn<kLogR>(leaf, sub);
                         if (sub == kNB - 1) {             // leaf[] is the block partial
                             if (has_vec) {
                                 float *dst = p.ws.block_partial + int64_t(block) * H + my_col;
-                                st_global_f32x4(dst, leaf[0], leaf[1], leaf[2], leaf[3]);
-                                st_global_f32x4(dst + 4, leaf[4], leaf[5], leaf[6], leaf[7]);
+                                st_global_f32x4(dst, leaf[0].x, leaf[0].y, leaf[1].x, leaf[1].y);
+                                st_global_f32x4(dst + 4, leaf[2].x, leaf[2].y, leaf[3].x, leaf[3].y);
                             }
                             if (tid == 0 && rank == 0) mark_whole_block(p.ws, block);
                         }
@@ -357,8 +400,8 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
                 } else if (kind == 1 && act) {
                     if (has_vec) {
                         float *dst = p.ws.spill + int64_t(m[r].lrow) * H + my_col;
-                        st_global_f32x4(dst, leaf[0], leaf[1], leaf[2], leaf[3]);
-                        st_global_f32x4(dst + 4, leaf[4], leaf[5], leaf[6], leaf[7]);
+                        st_global_f32x4(dst, leaf[0].x, leaf[0].y, leaf[1].x, leaf[1].y);
+                        st_global_f32x4(dst + 4, leaf[2].x, leaf[2].y, leaf[3].x, leaf[3].y);
                     }
                     if (tid == 0 && rank == 0) mark_spilled_row(p.ws, m[r].lrow);
                 }
