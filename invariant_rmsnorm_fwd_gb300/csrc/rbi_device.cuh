@@ -34,9 +34,9 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 struct WsView {                      // device addresses of the workspace regions
     WsHeader *hdr;
-    uint8_t *block_state;            // [nb]   1 = whole block partial written
+    uint8_t *block_state;            // [nb][4] per quarter: 0 none, 1 quarter partial, 2 whole-block partial
     uint8_t *leaf_flag;              // [N]    1 = row spilled
-    float *block_partial;            // [nb][H]
+    float *block_partial;            // [nb][4][H] quarter partials (slot 0 holds a whole-block partial)
     float *scratch_a;                // [ceil(nb/64)][H]
     float *scratch_b;                // [ceil(nb/64)][H]
     float *spill;                    // [N][H]
@@ -52,9 +52,9 @@ struct WsLayout {
         int64_t nb = (N + kBlockRows - 1) / kBlockRows;
         int64_t ng = (nb + kBlockRows - 1) / kBlockRows;
         off_state = 256;
-        off_flag = align256(off_state + nb);
+        off_flag = align256(off_state + nb * 4);
         off_partial = align256(off_flag + N);
-        off_sa = align256(off_partial + nb * H * 4);
+        off_sa = align256(off_partial + nb * 4 * H * 4);
         off_sb = align256(off_sa + ng * H * 4);
         off_spill = align256(off_sb + ng * H * 4);
         total = align256(off_spill + N * H * 4);
@@ -128,6 +128,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -140,15 +144,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns`
+// while the phase is incomplete, instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity; gives up after ~1 s of wall time.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (global_timer_ns() - t0 > 1000000000ull) return false;
     }
 }
@@ -429,14 +445,14 @@ struct TreeStack {
 // indices (the rows of one batch); push_dyn for a run-time index that is
 // uniform across the team (the batch within a block): the trailing one bits
 // of idx say how many pending partials the new subtree closes.
-template <int NC>
+template <int NC, int LEVELS = kBlockLevels>
 struct TreeStack2 {
-    float2 s[kBlockLevels][NC];
+    float2 s[LEVELS][NC];
 
     template <int LEVEL>
     __device__ __forceinline__ void push_static(float2 (&v)[NC], int idx) {
 #pragma unroll
-        for (int l = LEVEL; l < kBlockLevels; ++l) {
+        for (int l = LEVEL; l < LEVELS; ++l) {
             if ((idx >> (l - LEVEL)) & 1) {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) v[c] = add2(s[l][c], v[c]);
@@ -448,11 +464,13 @@ struct TreeStack2 {
         }
     }
 
+    // The subtree completed by the last item of a tree of 2^LEVELS leaves is
+    // returned in v and not stored.
     template <int LEVEL>
     __device__ __forceinline__ void push_dyn(float2 (&v)[NC], int idx) {
         const int t = __ffs(~idx) - 1;                   // trailing ones of idx
 #pragma unroll
-        for (int l = LEVEL; l < kBlockLevels; ++l) {
+        for (int l = LEVEL; l < LEVELS; ++l) {
             if (l - LEVEL < t) {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) v[c] = add2(s[l][c], v[c]);

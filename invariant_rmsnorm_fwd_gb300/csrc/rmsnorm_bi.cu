@@ -51,10 +51,14 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Shape {
     bool small = false;   // small_row_kernel
+    bool split = false;   // split_kernel (warp-specialised, one CTA per row team)
     int p2 = 0;           // lanes per row (small)
-    int k = 1;            // CTAs per team (large)
-    int threads = 0;      // threads per CTA (large)
+    int k = 1;            // CTAs per team (row_team_kernel)
+    int threads = 0;      // threads per CTA (row_team_kernel)
+    int nc = 0;           // column warps (split)
 };
+
+constexpr int kSplitStatsWarps = 2;
 
 bool hidden_shape(int64_t H, Shape *s) {
     if (H < 8 || H % 8 != 0 || H > 16384) return false;
@@ -66,9 +70,9 @@ bool hidden_shape(int64_t H, Shape *s) {
         s->p2 = p;
         return true;
     }
-    if (V <= 512) {
-        s->k = 1;
-        s->threads = int((V + 31) / 32 * 32);
+    if (V <= 640) {
+        s->split = true;
+        s->nc = int((V + 31) / 32);
         return true;
     }
     for (int k = 2; k <= 4; k *= 2) {
@@ -149,11 +153,42 @@ int launch_team(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStre
 template <int MODE, int R>
 int launch_team_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t s) {
     switch (sh.k) {
-        case 1: return launch_team<MODE, 1, R>(p, sh, d, s);
         case 2: return launch_team<MODE, 2, R>(p, sh, d, s);
         case 4: return launch_team<MODE, 4, R>(p, sh, d, s);
         default: return RMSNORM_ERR_HIDDEN;
     }
+}
+
+template <int MODE, int R, int MAXT>
+int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
+    constexpr int nt = ModeTraits<MODE>::kTensors;
+    const int64_t stage_bytes = int64_t(R) * nt * p.hidden * 2;
+    const int64_t off = split_stage_off(p.hidden);
+    int S = int((int64_t(d.max_smem) - off) / stage_bytes);
+    if (S > kSplitMaxStages) S = kSplitMaxStages;
+    if (S < 2) return RMSNORM_ERR_HIDDEN;
+    const int smem = int(off + S * stage_bytes);
+    const int threads = (sh.nc + kSplitStatsWarps + 1) * 32;
+    if (threads > MAXT) return RMSNORM_ERR_HIDDEN;
+    auto kern = split_kernel<MODE, R, MAXT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+        return RMSNORM_ERR_CUDA;
+    int64_t blocks = int64_t(per_sm) * d.sms;
+    if (blocks > p.n_units) blocks = p.n_units;
+    if (blocks < 1) return RMSNORM_OK;
+    kern<<<unsigned(blocks), threads, smem, stream>>>(p, S, sh.nc, kSplitStatsWarps);
+    if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return RMSNORM_OK;
+}
+
+template <int MODE, int R>
+int launch_split(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
+    if ((sh.nc + kSplitStatsWarps + 1) * 32 <= 608) return launch_split_t<MODE, R, 608>(p, sh, d, stream);
+    return launch_split_t<MODE, R, 768>(p, sh, d, stream);
 }
 
 template <int MODE, int P2>
@@ -191,11 +226,19 @@ int run_rows(KParams p, const Shape &sh, const rmsnorm_layout_t *L, cudaStream_t
     DeviceInfo *d = nullptr;
     int rc = device_info(&d);
     if (rc != RMSNORM_OK) return rc;
-    constexpr int R = (MODE == kFwd) ? 8 : 4;
+    constexpr bool leaves = ModeTraits<MODE>::kLeaves;
     const bool plan = p.use_plan != 0;
+    if (sh.split) {
+        constexpr int R = (MODE == kFwd) ? 4 : 2;
+        if (plan) p.n_units = leaves ? L->plan_items * 4 : L->plan_items * (kBlockRows / R);
+        else p.n_units = (p.n_rows + R - 1) / R;
+        if (p.n_units == 0) return RMSNORM_OK;
+        return launch_split<MODE, R>(p, sh, *d, stream);
+    }
+    constexpr int R = (MODE == kFwd) ? 8 : 4;
     if (plan) {
         // dweight modes work on whole plan items; the others on R-row batches of items
-        p.n_units = (ModeTraits<MODE>::kLeaves || sh.small) ? L->plan_items : L->plan_items * (kBlockRows / R);
+        p.n_units = (leaves || sh.small) ? L->plan_items : L->plan_items * (kBlockRows / R);
     } else if (sh.small) {
         p.n_units = (p.n_rows + kBlockRows - 1) / kBlockRows;
     } else {

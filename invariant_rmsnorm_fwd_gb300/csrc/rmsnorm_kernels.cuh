@@ -67,24 +67,47 @@ struct ModeTraits {
     static constexpr int kTensors = kNeedDy ? 2 : 1;
 };
 
-// Book-keeping of a whole block (one thread per team): it must not have been
-// contributed before, by a whole item or by spilled rows.
-__device__ __forceinline__ void mark_whole_block(const WsView &ws, int64_t b) {
-    bool dup = ws.block_state[b] != 0;
-    const uint64_t *f = reinterpret_cast<const uint64_t *>(ws.leaf_flag + b * kBlockRows);
-    const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
-    if (rows == kBlockRows) {
-#pragma unroll
-        for (int i = 0; i < kBlockRows / 8; ++i) dup |= f[i] != 0;
+// Book-keeping of contributions (one thread per team).  A block's four state
+// bytes say how it arrived: 2 2 2 2 = one whole-block partial (slot 0),
+// 1 1 1 1 = four quarter partials (slots 0..3), 0 0 0 0 = its rows were
+// spilled.  Any contribution that meets an earlier one is a double count.
+constexpr uint32_t kStateWhole = 0x02020202u;
+constexpr uint8_t kStateQuarter = 1;
+
+__device__ __forceinline__ bool leaf_flags_clear(const WsView &ws, int64_t r0, int64_t rows) {
+    bool clear = true;
+    if (rows == 16 && (r0 & 7) == 0) {
+        const uint64_t *f = reinterpret_cast<const uint64_t *>(ws.leaf_flag + r0);
+        clear = f[0] == 0 && f[1] == 0;
     } else {
-        for (int64_t i = 0; i < rows; ++i) dup |= ws.leaf_flag[b * kBlockRows + i] != 0;
+        for (int64_t i = 0; i < rows; ++i) clear &= ws.leaf_flag[r0 + i] == 0;
     }
+    return clear;
+}
+
+__device__ __forceinline__ void mark_whole_block(const WsView &ws, int64_t b) {
+    uint32_t *st = reinterpret_cast<uint32_t *>(ws.block_state) + b;
+    const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
+    bool dup = *st != 0;
+    for (int64_t r0 = 0; r0 < rows; r0 += 16) dup |= !leaf_flags_clear(ws, b * kBlockRows + r0, min64(16, rows - r0));
     if (dup) set_status(ws.hdr, kStDouble);
-    ws.block_state[b] = 1;
+    *st = kStateWhole;
+}
+
+__device__ __forceinline__ void mark_quarter(const WsView &ws, int64_t b, int q) {
+    uint8_t *st = ws.block_state + b * 4;
+    const int64_t r0 = b * kBlockRows + q * 16;
+    const int64_t rows = max64(0, min64(16, ws.n_rows - r0));
+    bool dup = st[q] != 0;
+    for (int i = 0; i < 4; ++i) dup |= st[i] == 2;
+    if (rows > 0) dup |= !leaf_flags_clear(ws, r0, rows);
+    if (dup) set_status(ws.hdr, kStDouble);
+    st[q] = kStateQuarter;
 }
 
 __device__ __forceinline__ void mark_spilled_row(const WsView &ws, int64_t lrow) {
-    if (ws.leaf_flag[lrow] != 0 || ws.block_state[lrow / kBlockRows] != 0) set_status(ws.hdr, kStDouble);
+    const uint32_t st = reinterpret_cast<const uint32_t *>(ws.block_state)[lrow / kBlockRows];
+    if (ws.leaf_flag[lrow] != 0 || st != 0) set_status(ws.hdr, kStDouble);
     ws.leaf_flag[lrow] = 1;
 }
 
@@ -347,7 +370,7 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
         }
 
         // ---- outputs and dweight leaves
-        TreeStack2<4> mini;            // levels < log2(R): the batch's own subtree
+        TreeStack2<4, (kLogR > 0 ? kLogR : 1)> mini;   // levels < log2(R): the batch's own subtree
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const bool act = m[r].off >= 0;
@@ -390,7 +413,7 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
                         tree.template push_dyn<kLogR>(leaf, sub);
                         if (sub == kNB - 1) {             // leaf[] is the block partial
                             if (has_vec) {
-                                float *dst = p.ws.block_partial + int64_t(block) * H + my_col;
+                                float *dst = p.ws.block_partial + int64_t(block) * 4 * H + my_col;
                                 st_global_f32x4(dst, leaf[0].x, leaf[0].y, leaf[1].x, leaf[1].y);
                                 st_global_f32x4(dst + 4, leaf[2].x, leaf[2].y, leaf[3].x, leaf[3].y);
                             }
@@ -409,6 +432,315 @@ __global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const
         }
     }
     if (K > 1) cluster_barrier();      // peers may still read our partials
+}
+
+// =====================================================================
+// Hidden sizes 264..5120: warp-specialised pipeline in one CTA
+// =====================================================================
+//
+// Warps [0, NC): column warps; thread t owns columns 8t..8t+7 of every row.
+// Warps [NC, NC+NS): stats warps; warp i handles the stages s with s % NS == i.
+// Warp NC+NS: producer; lane 0 issues the bulk copies.
+//
+// Per stage s (R rows of x, dy): full[s] completes when the copies land,
+// stats[s] when a stats warp has published rstd and mean(g*xhat) for its
+// rows, empty[s] when every column warp is done with it.  No CTA-wide
+// barrier is used after set-up.  Rows of the dweight modes are processed in
+// 16-row units (a quarter of a logical block): the column warps reduce the
+// unit's 16 leaves with the 64-leaf tree's lower four levels and store the
+// quarter partial; dweight_finalize adds the four quarters (levels 5, 6).
+//
+// Row sums (this family's canonical tree, which depends on H only): lane l
+// folds vectors l, l+32, l+64, ... in order, columns interleaved as two FMA
+// chains (columns 0,2,4,6 and 1,3,5,7 of each vector, one chain across all
+// of the lane's vectors), the chains are added, and the 32 lane sums are
+// added by a complete tree pairing lanes 16 apart first, then 8, 4, 2, 1.
+
+constexpr int kSplitMaxStages = 12;
+constexpr int kSplitUnitRows = 16;
+
+struct SplitStats {
+    float rstd;
+    float mg;
+};
+
+constexpr int kSplitMetaOff = 512;                                   // after 3 x 12 barriers (288 B) + flag
+constexpr int kSplitStatsOff = kSplitMetaOff + kSplitMaxStages * kMaxBatch * 16;
+constexpr int kSplitWOff = kSplitStatsOff + kSplitMaxStages * kMaxBatch * 8;   // FP32 weight [H]
+__host__ __device__ constexpr int split_stage_off(int H) { return ((kSplitWOff + H * 4) + 127) / 128 * 128; }
+
+template <int MODE, int R, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const int S, const int NC, const int NS) {
+    using T = ModeTraits<MODE>;
+    constexpr int kLogR = (R == 1) ? 0 : (R == 2) ? 1 : (R == 4) ? 2 : 3;
+    constexpr int kUnitBatches = kSplitUnitRows / R;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *stats_bar = full + kSplitMaxStages;
+    uint64_t *empty = stats_bar + kSplitMaxStages;
+    volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + 3 * kSplitMaxStages * 8);
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + kSplitMetaOff);   // [S][R]
+    SplitStats *stats = reinterpret_cast<SplitStats *>(smem + kSplitStatsOff);
+    float *wsm = reinterpret_cast<float *>(smem + kSplitWOff);
+    const int H = p.hidden;
+    const int V = H >> 3;
+    uint8_t *stages = smem + split_stage_off(H);
+    const uint32_t row_bytes = uint32_t(H) * 2u;
+    auto stage_ptr = [&](int s, int t, int r) -> uint8_t * {
+        return stages + ((int64_t(s) * T::kTensors + t) * R + r) * row_bytes;
+    };
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float Hf = float(H);
+    const bool item_units = p.use_plan && T::kLeaves;
+    const int64_t per_unit = item_units ? kUnitBatches : 1;
+    const int64_t my_units = p.n_units > blockIdx.x ? (p.n_units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int64_t n_batches = my_units * per_unit;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&stats_bar[s], 1);
+            mbar_init(&empty[s], NC);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (MODE != kDw && T::kNeedGx) {
+        for (int i = tid; i < H; i += blockDim.x) wsm[i] = __uint_as_float(uint32_t(p.w[i]) << 16);
+    }
+    __syncthreads();
+
+    // batch k of this CTA -> (plan item, slot base) or physical row base
+    auto batch_slots = [&](int64_t k, int64_t &item, int &slot0) {
+        if (item_units) {
+            const int64_t u = blockIdx.x + (k / kUnitBatches) * gridDim.x;      // quarter unit
+            item = u >> 2;
+            slot0 = int(u & 3) * kSplitUnitRows + int(k % kUnitBatches) * R;
+        } else {
+            const int64_t gb = blockIdx.x + k * gridDim.x;
+            if (p.use_plan) {
+                item = gb / (kBlockRows / R);
+                slot0 = int(gb % (kBlockRows / R)) * R;
+            } else {
+                item = gb;                                                     // physical batch index
+                slot0 = 0;
+            }
+        }
+    };
+
+    if (warp == NC + NS) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            for (int64_t k = 0; k < n_batches; ++k) {
+                const int s = int(k % S);
+                if (k >= S && !mbar_wait_bounded(&empty[s], uint32_t(((k / S) - 1) & 1))) {
+                    *abort_flag = 1;
+                    if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
+                }
+                if (*abort_flag) {
+                    // let copies already issued land (bounded) before leaving
+                    for (int64_t kk = (k > S ? k - S : 0); kk < k; ++kk)
+                        mbar_wait_bounded(&full[kk % S], uint32_t((kk / S) & 1));
+                    break;
+                }
+                int64_t item;
+                int slot0;
+                batch_slots(k, item, slot0);
+                StageMeta *m = meta + s * R;
+                int64_t offs[R];
+                uint32_t n_act = 0;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    int32_t pr = -1, lr = -1;
+                    if (p.use_plan) {
+                        const PlanItem *it = p.items + item;
+                        pr = it->prow[slot0 + r];
+                        lr = it->lrow[slot0 + r];
+                    } else {
+                        const int64_t row = item * R + r;
+                        if (row < p.n_rows && p.tok_id[row / p.rpt] >= 0) pr = int32_t(row);
+                    }
+                    bool act = pr >= 0;
+                    if (act && (pr >= p.n_rows || (T::kLeaves && (lr < 0 || lr >= p.ws.n_rows)))) {
+                        if (T::kLeaves) set_status(p.ws.hdr, kStPlan);
+                        act = false;
+                    }
+                    offs[r] = act ? row_offset(p, pr) : -1;
+                    m[r].off = offs[r];
+                    m[r].lrow = lr;
+                    m[r].prow = pr;
+                    n_act += act ? 1u : 0u;
+                }
+                mbar_arrive_expect_tx(&full[s], n_act * row_bytes * T::kTensors);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (offs[r] < 0) continue;
+                    bulk_copy_g2s(stage_ptr(s, 0, r), p.x + offs[r], row_bytes, &full[s]);
+                    if (T::kNeedDy) bulk_copy_g2s(stage_ptr(s, 1, r), p.dy + offs[r], row_bytes, &full[s]);
+                }
+            }
+        }
+        return;
+    }
+
+    if (warp >= NC) {
+        // ------------------------------------------------ stats warps
+        const int si = warp - NC;
+        for (int64_t k = 0; k < n_batches; ++k) {
+            const int s = int(k % S);
+            if (s % NS != si) continue;
+            if (*abort_flag) break;
+            if (!mbar_wait_bounded(&full[s], uint32_t((k / S) & 1))) {
+                *abort_flag = 1;
+                if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
+                break;
+            }
+            const StageMeta *m = meta + s * R;
+            float vals[2 * R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+                if (m[r].off >= 0) {
+                    const uint8_t *xr = stage_ptr(s, 0, r);
+                    const uint8_t *dr = stage_ptr(s, 1, r);
+#pragma unroll 4
+                    for (int v = lane; v < V; v += 32) {
+                        float2 xf[4];
+                        unpack8x2(ld_shared_v4(xr + v * 16), xf);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) a2 = fma2(xf[i], xf[i], a2);
+                        if (T::kNeedGx) {
+                            float2 df[4];
+                            unpack8x2(ld_shared_v4(dr + v * 16), df);
+                            const float4 w0 = *reinterpret_cast<const float4 *>(wsm + v * 8);
+                            const float4 w1 = *reinterpret_cast<const float4 *>(wsm + v * 8 + 4);
+                            const float2 wf[4] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
+                                                  make_float2(w1.x, w1.y), make_float2(w1.z, w1.w)};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) b2 = fma2(mul2(df[i], wf[i]), xf[i], b2);
+                        }
+                    }
+                }
+                vals[r] = __fadd_rn(a2.x, a2.y);
+                vals[R + r] = __fadd_rn(b2.x, b2.y);
+            }
+            // complete tree over the 32 lanes, pairing 16 apart first
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1)
+#pragma unroll
+                for (int j = 0; j < (T::kNeedGx ? 2 * R : R); ++j)
+                    vals[j] = __fadd_rn(vals[j], __shfl_xor_sync(kFull, vals[j], d));
+            if (lane < R) {
+                float ss = vals[0], gx = vals[R];
+#pragma unroll
+                for (int r = 1; r < R; ++r)
+                    if (lane == r) {
+                        ss = vals[r];
+                        gx = vals[R + r];
+                    }
+                const float rstd = row_rstd(ss, Hf, p.eps);
+                SplitStats st;
+                st.rstd = rstd;
+                st.mg = T::kNeedGx ? row_mean_gxhat(gx, rstd, Hf) : 0.f;
+                stats[s * R + lane] = st;
+                if (MODE == kFwd && p.rstd_out != nullptr && m[lane].off >= 0) p.rstd_out[m[lane].prow] = rstd;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&stats_bar[s]);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- column warps
+    const int t = tid;                                   // vector owned: columns 8t..8t+7
+    const bool has_vec = t < V;
+    float2 wv[4];
+    if (MODE != kDw && has_vec) unpack8x2(*reinterpret_cast<const uint4 *>(p.w + t * 8), wv);
+    TreeStack2<4, 4> tree;             // levels log2(R)..3 of the 16-leaf unit
+    int32_t kind = 0, block = -1, quarter = 0;
+    for (int64_t k = 0; k < n_batches; ++k) {
+        const int s = int(k % S);
+        const uint32_t parity = uint32_t((k / S) & 1);
+        const int sub = int(k % per_unit);
+        if (item_units && sub == 0) {
+            const int64_t u = blockIdx.x + (k / kUnitBatches) * gridDim.x;
+            const PlanItem *it = p.items + (u >> 2);
+            quarter = int(u & 3);
+            kind = it->kind;
+            block = it->block;
+            if ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1)) {
+                if (t == 0) set_status(p.ws.hdr, kStPlan);
+                kind = 2;
+            }
+        }
+        if (*abort_flag) break;
+        if (!mbar_wait_bounded(&stats_bar[s], parity) || !mbar_wait_bounded(&full[s], parity)) {
+            *abort_flag = 1;
+            if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
+            break;
+        }
+        const StageMeta *m = meta + s * R;
+        TreeStack2<4, (kLogR > 0 ? kLogR : 1)> mini;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool act = m[r].off >= 0;
+            float2 leaf[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) leaf[i] = make_float2(0.f, 0.f);
+            if (act && has_vec) {
+                const SplitStats st = stats[s * R + r];
+                const float2 r2 = make_float2(st.rstd, st.rstd);
+                float2 xf[4], xh[4], o[4];
+                unpack8x2(ld_shared_v4(stage_ptr(s, 0, r) + t * 16), xf);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) xh[i] = mul2(xf[i], r2);
+                if (MODE == kFwd) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[i] = mul2(xh[i], wv[i]);
+                    st_global_v4(p.out + m[r].off + t * 8, pack8x2(o));
+                } else {
+                    float2 df[4];
+                    unpack8x2(ld_shared_v4(stage_ptr(s, 1, r) + t * 16), df);
+                    if (T::kNeedGx && p.out != nullptr) {
+                        const float2 nm2 = make_float2(-st.mg, -st.mg);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) o[i] = mul2(r2, fma2(xh[i], nm2, mul2(df[i], wv[i])));
+                        st_global_v4(p.out + m[r].off + t * 8, pack8x2(o));
+                    }
+                    if (T::kLeaves) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) leaf[i] = mul2(df[i], xh[i]);
+                    }
+                }
+            }
+            if (T::kLeaves) {
+                if (kind == 0) {
+                    if (R > 1) mini.template push_static<0>(leaf, r);
+                    if (r == R - 1) {
+                        tree.template push_dyn<kLogR>(leaf, sub);
+                        if (sub == kUnitBatches - 1) {           // leaf[] is the quarter partial
+                            if (has_vec) {
+                                float *dst = p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + t * 8;
+                                st_global_f32x4(dst, leaf[0].x, leaf[0].y, leaf[1].x, leaf[1].y);
+                                st_global_f32x4(dst + 4, leaf[2].x, leaf[2].y, leaf[3].x, leaf[3].y);
+                            }
+                            if (t == 0) mark_quarter(p.ws, block, quarter);
+                        }
+                    }
+                } else if (kind == 1 && act) {
+                    if (has_vec) {
+                        float *dst = p.ws.spill + int64_t(m[r].lrow) * H + t * 8;
+                        st_global_f32x4(dst, leaf[0].x, leaf[0].y, leaf[1].x, leaf[1].y);
+                        st_global_f32x4(dst + 4, leaf[2].x, leaf[2].y, leaf[3].x, leaf[3].y);
+                    }
+                    if (t == 0) mark_spilled_row(p.ws, m[r].lrow);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
 }
 
 // =====================================================================
@@ -536,7 +868,7 @@ __global__ void __launch_bounds__(256) small_row_kernel(const KParams p) {
                             for (int i = 0; i < 8; ++i) leaf[i] = __fadd_rn(leaf[i], __shfl_xor_sync(kFull, leaf[i], kk));
                         tree.push(leaf, st0 + q, kLogTPW);
                         if (st0 + q == kSteps - 1 && team == 0 && has_vec) {
-                            float *dst = p.ws.block_partial + int64_t(block) * H + tl * 8;
+                            float *dst = p.ws.block_partial + int64_t(block) * 4 * H + tl * 8;
                             st_global_f32x4(dst, leaf[0], leaf[1], leaf[2], leaf[3]);
                             st_global_f32x4(dst + 4, leaf[4], leaf[5], leaf[6], leaf[7]);
                         }
@@ -611,7 +943,9 @@ __global__ void __launch_bounds__(256) tree_pass_kernel(WsView ws, const float *
         float val[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) val[c] = 0.f;
-        if (from_blocks && ws.block_state[b] == 0) {
+        const uint32_t state = from_blocks ? reinterpret_cast<const uint32_t *>(ws.block_state)[b] : kStateWhole;
+        if (state == 0) {
+            // cut block: rebuild from the spilled rows with the same 64-leaf tree
             const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
             if (vl == 0 && blockIdx.x == 0) {
                 bool missing = false;
@@ -631,8 +965,25 @@ __global__ void __launch_bounds__(256) tree_pass_kernel(WsView ws, const float *
                     for (int c = 0; c < 8; ++c) val[c] = leaf[c];
                 }
             }
-        } else if (has_vec) {
-            load8((from_blocks ? ws.block_partial : in) + b * int64_t(H) + int64_t(v) * 8, val);
+        } else if (state == 0x01010101u) {
+            // four quarter partials: levels 5 and 6 of the block tree
+            if (has_vec) {
+                float q0[8], q1[8], q2[8], q3[8];
+                const float *src = ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8;
+                load8(src, q0);
+                load8(src + H, q1);
+                load8(src + 2 * int64_t(H), q2);
+                load8(src + 3 * int64_t(H), q3);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) val[c] = __fadd_rn(__fadd_rn(q0[c], q1[c]), __fadd_rn(q2[c], q3[c]));
+            }
+        } else if (state == kStateWhole) {
+            if (has_vec) {
+                const float *src = from_blocks ? ws.block_partial + b * 4 * int64_t(H) : in + b * int64_t(H);
+                load8(src + int64_t(v) * 8, val);
+            }
+        } else {
+            if (vl == 0 && blockIdx.x == 0) set_status(ws.hdr, kStMissing);   // partly contributed block
         }
         st.push(val, i, 0);
     }

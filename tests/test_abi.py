@@ -51,7 +51,8 @@ def test_host_side_errors_need_no_gpu():
     L = _layout()
     assert lib.rmsnorm_fwd(good, good, 12, 1e-6, ctypes.byref(L), good, None, None) == -2      # H % 8
     assert lib.rmsnorm_fwd(good, good, 24576, 1e-6, ctypes.byref(L), good, None, None) == -2   # too big
-    assert lib.rmsnorm_fwd(good, good, 4104, 1e-6, ctypes.byref(_layout(stride=4104)), good, None, None) == -2
+    assert lib.rmsnorm_fwd(good, good, 5128, 1e-6, ctypes.byref(_layout(stride=5128)), good, None, None) == -2
+    assert lib.rmsnorm_fwd(good, good, 8200, 1e-6, ctypes.byref(_layout(stride=8200)), good, None, None) == -2
     assert lib.rmsnorm_fwd(good, good, 8, 1e-6, None, good, None, None) == -1
     assert lib.rmsnorm_fwd(None, good, 8, 1e-6, ctypes.byref(L), good, None, None) == -1
     assert lib.rmsnorm_fwd(P(258), good, 8, 1e-6, ctypes.byref(L), good, None, None) == -3

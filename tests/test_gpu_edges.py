@@ -67,7 +67,7 @@ def test_constant_rows_map_to_w_times_sign_bitwise():
 
 # ------------------------------------------------------------------ hidden sizes
 
-@pytest.mark.parametrize("hidden", [8, 16, 24, 64, 128, 136, 256, 264, 512, 1024, 4096, 5120, 6144, 8192,
+@pytest.mark.parametrize("hidden", [8, 16, 24, 64, 128, 136, 256, 264, 512, 1024, 4096, 4104, 5120, 6144, 8192,
                                     12288, 16384])
 def test_hidden_sweep_invariance_and_accuracy(hidden):
     wl = _workload([70, 3, 130, 1, 64, 9], hidden, seed=hidden)
