@@ -340,6 +340,110 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[NV], int lane)
     return r;
 }
 
+// ----------------------------------------------------------------- f2: FP32 pairs in 64-bit registers
+//
+// The same packed arithmetic as add2/mul2/fma2, but the pair lives in one
+// 64-bit register from the bf16 unpack to the bf16 pack, so no moves are
+// needed to assemble or split register pairs around each operation.
+
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+    f2_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+    f2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+    f2_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_make(float lo, float hi) {
+    f2_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ float f2_lo(f2_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo;
+}
+__device__ __forceinline__ float f2_hi(f2_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return hi;
+}
+// two bf16 (low half = even column) -> FP32 pair, exact
+__device__ __forceinline__ f2_t f2_from_bf16x2(uint32_t w) {
+    f2_t d;
+    asm("{\n\t.reg .b32 lo, hi;\n\tshl.b32 lo, %1, 16;\n\tand.b32 hi, %1, 0xffff0000;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(d)
+        : "r"(w));
+    return d;
+}
+// FP32 pair -> two bf16, round-to-nearest-even (even column in the low half)
+__device__ __forceinline__ uint32_t f2_to_bf16x2(f2_t v) {
+    uint32_t r;
+    asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(r)
+        : "l"(v));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack8(const uint4 &v, f2_t (&f)[4]) {
+    f[0] = f2_from_bf16x2(v.x);
+    f[1] = f2_from_bf16x2(v.y);
+    f[2] = f2_from_bf16x2(v.z);
+    f[3] = f2_from_bf16x2(v.w);
+}
+__device__ __forceinline__ uint4 f2_pack8(const f2_t (&f)[4]) {
+    return make_uint4(f2_to_bf16x2(f[0]), f2_to_bf16x2(f[1]), f2_to_bf16x2(f[2]), f2_to_bf16x2(f[3]));
+}
+__device__ __forceinline__ void st_global_f2x4(float *p, const f2_t (&f)[4]) {
+    asm volatile("st.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(f[0]), "l"(f[1]) : "memory");
+    asm volatile("st.global.v2.b64 [%0], {%1, %2};" ::"l"(p + 4), "l"(f[2]), "l"(f[3]) : "memory");
+}
+
+template <int NC, int LEVELS>
+struct TreeStackF2 {
+    f2_t s[LEVELS][NC];
+
+    template <int LEVEL>
+    __device__ __forceinline__ void push_static(f2_t (&v)[NC], int idx) {
+#pragma unroll
+        for (int l = LEVEL; l < LEVELS; ++l) {
+            if ((idx >> (l - LEVEL)) & 1) {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) v[c] = f2_add(s[l][c], v[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) s[l][c] = v[c];
+                break;
+            }
+        }
+    }
+
+    template <int LEVEL>
+    __device__ __forceinline__ void push_dyn(f2_t (&v)[NC], int idx) {
+        const int t = __ffs(~idx) - 1;
+#pragma unroll
+        for (int l = LEVEL; l < LEVELS; ++l) {
+            if (l - LEVEL < t) {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) v[c] = f2_add(s[l][c], v[c]);
+            } else if (l - LEVEL == t) {
+#pragma unroll
+                for (int c = 0; c < NC; ++c) s[l][c] = v[c];
+            }
+        }
+    }
+};
+
 // ----------------------------------------------------------------- row sums
 //
 // Canonical row-sum trees.  The sum of squares (and, in the backward, the

@@ -170,7 +170,7 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
     const int smem = int(off + S * stage_bytes);
     const int threads = (sh.nc + kSplitStatsWarps + 1) * 32;
     if (threads > MAXT) return RMSNORM_ERR_HIDDEN;
-    auto kern = split_kernel<MODE, R, MAXT>;
+    auto kern = split_kernel<MODE, R, MAXT, kSplitStatsWarps>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
     int per_sm = 0;
@@ -179,7 +179,7 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
     int64_t blocks = int64_t(per_sm) * d.sms;
     if (blocks > p.n_units) blocks = p.n_units;
     if (blocks < 1) return RMSNORM_OK;
-    kern<<<unsigned(blocks), threads, smem, stream>>>(p, S, sh.nc, kSplitStatsWarps);
+    kern<<<unsigned(blocks), threads, smem, stream>>>(p, S, sh.nc);
     if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return RMSNORM_OK;

@@ -469,8 +469,8 @@ constexpr int kSplitStatsOff = kSplitMetaOff + kSplitMaxStages * kMaxBatch * 16;
 constexpr int kSplitWOff = kSplitStatsOff + kSplitMaxStages * kMaxBatch * 8;   // FP32 weight [H]
 __host__ __device__ constexpr int split_stage_off(int H) { return ((kSplitWOff + H * 4) + 127) / 128 * 128; }
 
-template <int MODE, int R, int MAXT>
-__global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const int S, const int NC, const int NS) {
+template <int MODE, int R, int MAXT, int NS>
+__global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const int S, const int NC) {
     using T = ModeTraits<MODE>;
     constexpr int kLogR = (R == 1) ? 0 : (R == 2) ? 1 : (R == 4) ? 2 : 3;
     constexpr int kUnitBatches = kSplitUnitRows / R;
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     const bool item_units = p.use_plan && T::kLeaves;
     const int64_t per_unit = item_units ? kUnitBatches : 1;
     const int64_t my_units = p.n_units > blockIdx.x ? (p.n_units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    const int64_t n_batches = my_units * per_unit;
+    const int n_batches = int(my_units * per_unit);      // < 2^31: units are bounded by rows / 2
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     __syncthreads();
 
     // batch k of this CTA -> (plan item, slot base) or physical row base
-    auto batch_slots = [&](int64_t k, int64_t &item, int &slot0) {
+    auto batch_slots = [&](int k, int64_t &item, int &slot0) {
         if (item_units) {
             const int64_t u = blockIdx.x + (k / kUnitBatches) * gridDim.x;      // quarter unit
             item = u >> 2;
@@ -532,16 +532,24 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     if (warp == NC + NS) {
         // ------------------------------------------------ producer
         if (lane == 0) {
-            for (int64_t k = 0; k < n_batches; ++k) {
-                const int s = int(k % S);
-                if (k >= S && !mbar_wait_bounded(&empty[s], uint32_t(((k / S) - 1) & 1))) {
+            int s = 0;
+            uint32_t ph = 0;                             // parity of the current use of stage s
+            for (int k = 0; k < n_batches; ++k) {
+                if (k >= S && !mbar_wait_bounded(&empty[s], ph ^ 1u)) {
                     *abort_flag = 1;
                     if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
                 }
                 if (*abort_flag) {
                     // let copies already issued land (bounded) before leaving
-                    for (int64_t kk = (k > S ? k - S : 0); kk < k; ++kk)
-                        mbar_wait_bounded(&full[kk % S], uint32_t((kk / S) & 1));
+                    int ss = s;
+                    uint32_t pp = ph;
+                    for (int kk = k - 1; kk >= 0 && kk >= k - S; --kk) {
+                        if (--ss < 0) {
+                            ss = S - 1;
+                            pp ^= 1u;
+                        }
+                        mbar_wait_bounded(&full[ss], pp);
+                    }
                     break;
                 }
                 int64_t item;
@@ -579,6 +587,10 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     bulk_copy_g2s(stage_ptr(s, 0, r), p.x + offs[r], row_bytes, &full[s]);
                     if (T::kNeedDy) bulk_copy_g2s(stage_ptr(s, 1, r), p.dy + offs[r], row_bytes, &full[s]);
                 }
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
         return;
@@ -587,11 +599,12 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     if (warp >= NC) {
         // ------------------------------------------------ stats warps
         const int si = warp - NC;
-        for (int64_t k = 0; k < n_batches; ++k) {
-            const int s = int(k % S);
+        int s = 0;
+        uint32_t ph = 0;
+        for (int k = 0; k < n_batches; ++k, ph ^= (s == S - 1) ? 1u : 0u, s = (s == S - 1) ? 0 : s + 1) {
             if (s % NS != si) continue;
             if (*abort_flag) break;
-            if (!mbar_wait_bounded(&full[s], uint32_t((k / S) & 1))) {
+            if (!mbar_wait_bounded(&full[s], ph)) {
                 *abort_flag = 1;
                 if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
                 break;
@@ -600,30 +613,27 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
             float vals[2 * R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+                f2_t a2 = 0ull, b2 = 0ull;                      // +0.0 in both lanes
                 if (m[r].off >= 0) {
                     const uint8_t *xr = stage_ptr(s, 0, r);
                     const uint8_t *dr = stage_ptr(s, 1, r);
 #pragma unroll 4
                     for (int v = lane; v < V; v += 32) {
-                        float2 xf[4];
-                        unpack8x2(ld_shared_v4(xr + v * 16), xf);
+                        f2_t xf[4];
+                        f2_unpack8(ld_shared_v4(xr + v * 16), xf);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) a2 = fma2(xf[i], xf[i], a2);
+                        for (int i = 0; i < 4; ++i) a2 = f2_fma(xf[i], xf[i], a2);
                         if (T::kNeedGx) {
-                            float2 df[4];
-                            unpack8x2(ld_shared_v4(dr + v * 16), df);
-                            const float4 w0 = *reinterpret_cast<const float4 *>(wsm + v * 8);
-                            const float4 w1 = *reinterpret_cast<const float4 *>(wsm + v * 8 + 4);
-                            const float2 wf[4] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
-                                                  make_float2(w1.x, w1.y), make_float2(w1.z, w1.w)};
+                            f2_t df[4];
+                            f2_unpack8(ld_shared_v4(dr + v * 16), df);
+                            const f2_t *wf = reinterpret_cast<const f2_t *>(wsm + v * 8);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) b2 = fma2(mul2(df[i], wf[i]), xf[i], b2);
+                            for (int i = 0; i < 4; ++i) b2 = f2_fma(f2_mul(df[i], wf[i]), xf[i], b2);
                         }
                     }
                 }
-                vals[r] = __fadd_rn(a2.x, a2.y);
-                vals[R + r] = __fadd_rn(b2.x, b2.y);
+                vals[r] = __fadd_rn(f2_lo(a2), f2_hi(a2));
+                vals[R + r] = __fadd_rn(f2_lo(b2), f2_hi(b2));
             }
             // complete tree over the 32 lanes, pairing 16 apart first
 #pragma unroll
@@ -655,16 +665,25 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     // ---------------------------------------------------- column warps
     const int t = tid;                                   // vector owned: columns 8t..8t+7
     const bool has_vec = t < V;
-    float2 wv[4];
-    if (MODE != kDw && has_vec) unpack8x2(*reinterpret_cast<const uint4 *>(p.w + t * 8), wv);
-    TreeStack2<4, 4> tree;             // levels log2(R)..3 of the 16-leaf unit
+    f2_t wv[4];
+    if (MODE != kDw && has_vec) f2_unpack8(*reinterpret_cast<const uint4 *>(p.w + t * 8), wv);
+    TreeStackF2<4, 4> tree;            // levels log2(R)..3 of the 16-leaf unit
     int32_t kind = 0, block = -1, quarter = 0;
-    for (int64_t k = 0; k < n_batches; ++k) {
-        const int s = int(k % S);
-        const uint32_t parity = uint32_t((k / S) & 1);
-        const int sub = int(k % per_unit);
+    int s = 0, sub = 0;
+    uint32_t parity = 0;
+    int64_t u = blockIdx.x;                               // current quarter unit
+    for (int k = 0; k < n_batches; ++k) {
+        if (k > 0) {
+            if (++s == S) {
+                s = 0;
+                parity ^= 1u;
+            }
+            if (++sub == per_unit) {
+                sub = 0;
+                u += gridDim.x;
+            }
+        }
         if (item_units && sub == 0) {
-            const int64_t u = blockIdx.x + (k / kUnitBatches) * gridDim.x;
             const PlanItem *it = p.items + (u >> 2);
             quarter = int(u & 3);
             kind = it->kind;
@@ -681,36 +700,35 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
             break;
         }
         const StageMeta *m = meta + s * R;
-        TreeStack2<4, (kLogR > 0 ? kLogR : 1)> mini;
+        TreeStackF2<4, (kLogR > 0 ? kLogR : 1)> mini;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const bool act = m[r].off >= 0;
-            float2 leaf[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) leaf[i] = make_float2(0.f, 0.f);
+            const int64_t off = m[r].off;
+            const bool act = off >= 0;
+            f2_t leaf[4] = {0ull, 0ull, 0ull, 0ull};
             if (act && has_vec) {
                 const SplitStats st = stats[s * R + r];
-                const float2 r2 = make_float2(st.rstd, st.rstd);
-                float2 xf[4], xh[4], o[4];
-                unpack8x2(ld_shared_v4(stage_ptr(s, 0, r) + t * 16), xf);
+                const f2_t r2 = f2_make(st.rstd, st.rstd);
+                f2_t xf[4], xh[4], o[4];
+                f2_unpack8(ld_shared_v4(stage_ptr(s, 0, r) + t * 16), xf);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) xh[i] = mul2(xf[i], r2);
+                for (int i = 0; i < 4; ++i) xh[i] = f2_mul(xf[i], r2);
                 if (MODE == kFwd) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) o[i] = mul2(xh[i], wv[i]);
-                    st_global_v4(p.out + m[r].off + t * 8, pack8x2(o));
+                    for (int i = 0; i < 4; ++i) o[i] = f2_mul(xh[i], wv[i]);
+                    st_global_v4(p.out + off + t * 8, f2_pack8(o));
                 } else {
-                    float2 df[4];
-                    unpack8x2(ld_shared_v4(stage_ptr(s, 1, r) + t * 16), df);
+                    f2_t df[4];
+                    f2_unpack8(ld_shared_v4(stage_ptr(s, 1, r) + t * 16), df);
                     if (T::kNeedGx && p.out != nullptr) {
-                        const float2 nm2 = make_float2(-st.mg, -st.mg);
+                        const f2_t nm2 = f2_make(-st.mg, -st.mg);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) o[i] = mul2(r2, fma2(xh[i], nm2, mul2(df[i], wv[i])));
-                        st_global_v4(p.out + m[r].off + t * 8, pack8x2(o));
+                        for (int i = 0; i < 4; ++i) o[i] = f2_mul(r2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
+                        st_global_v4(p.out + off + t * 8, f2_pack8(o));
                     }
                     if (T::kLeaves) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) leaf[i] = mul2(df[i], xh[i]);
+                        for (int i = 0; i < 4; ++i) leaf[i] = f2_mul(df[i], xh[i]);
                     }
                 }
             }
@@ -720,20 +738,13 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     if (r == R - 1) {
                         tree.template push_dyn<kLogR>(leaf, sub);
                         if (sub == kUnitBatches - 1) {           // leaf[] is the quarter partial
-                            if (has_vec) {
-                                float *dst = p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + t * 8;
-                                st_global_f32x4(dst, leaf[0].x, leaf[0].y, leaf[1].x, leaf[1].y);
-                                st_global_f32x4(dst + 4, leaf[2].x, leaf[2].y, leaf[3].x, leaf[3].y);
-                            }
+                            if (has_vec)
+                                st_global_f2x4(p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + t * 8, leaf);
                             if (t == 0) mark_quarter(p.ws, block, quarter);
                         }
                     }
                 } else if (kind == 1 && act) {
-                    if (has_vec) {
-                        float *dst = p.ws.spill + int64_t(m[r].lrow) * H + t * 8;
-                        st_global_f32x4(dst, leaf[0].x, leaf[0].y, leaf[1].x, leaf[1].y);
-                        st_global_f32x4(dst + 4, leaf[2].x, leaf[2].y, leaf[3].x, leaf[3].y);
-                    }
+                    if (has_vec) st_global_f2x4(p.ws.spill + int64_t(m[r].lrow) * H + t * 8, leaf);
                     if (t == 0) mark_spilled_row(p.ws, m[r].lrow);
                 }
             }
