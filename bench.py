@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
     return ap.parse_args()
 
 
@@ -154,20 +155,13 @@ class Step:
         self.n_active = wl.n_tokens
         self.bwd_events = []
 
-    def run(self, stream, time_bwd=False):
-        import torch
+    def run(self, stream):
         rb = self.rb
         for cl, xp, dp, yp, dxp in self.calls:
             rb.rmsnorm_fwd(xp, self.w, cl, self.eps, y=yp, stream=stream)
         self.ws.begin(stream)
         for cl, xp, dp, yp, dxp in self.calls:
-            if time_bwd:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
             rb.rmsnorm_bwd_dx(xp, self.w, dp, cl, self.eps, dx=dxp, workspace=self.ws, stream=stream)
-            if time_bwd:
-                e1.record(stream)
-                self.bwd_events.append((e0, e1))
         self.ws.finalize(self.dw, stream)
 
     def time_fwd_only(self, stream):
@@ -191,29 +185,60 @@ class Step:
         return y, dx, self.dw.clone()
 
 
-def time_steps(step, stream, steps, warmup, flush, dist=None, time_bwd=False):
+def time_steps(step, stream, steps, warmup, flush, dist=None, graph=True):
+    """W eager warm-up steps, then K timed steps (CUDA-graph replays of one whole
+    step when graph=True), each preceded by an untimed L2 flush; returns ms per step."""
     import torch
     for _ in range(warmup):
         step.run(stream)
     torch.cuda.synchronize()
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            step.run(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        g.replay()                               # one untimed replay
+        torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     times = []
-    step.bwd_events = []
     for _ in range(steps):
         flush.fill_(1)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        step.run(stream, time_bwd=time_bwd)
+        if g is not None:
+            g.replay()
+        else:
+            step.run(stream)
         e1.record(stream)
         times.append((e0, e1))
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    ms = [a.elapsed_time(b) for a, b in times]
-    bwd_ms = [a.elapsed_time(b) for a, b in step.bwd_events]
-    return ms, bwd_ms
+    return [a.elapsed_time(b) for a, b in times], g
+
+
+def time_bwd_kernel(step_objs, stream, reps, flush):
+    """Duration of each fused-backward launch (CUDA events on the launching stream)."""
+    import torch
+    per = []
+    for _ in range(reps):
+        for so in step_objs:
+            so.ws.begin(stream)
+            for cl, xp, dp, yp, dxp in so.calls:
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                so.rb.rmsnorm_bwd_dx(xp, so.w, dp, cl, so.eps, dx=dxp, workspace=so.ws, stream=stream)
+                e1.record(stream)
+                per.append((e0, e1))
+            so.ws.finalize(so.dw, stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in per]
 
 
 def e2e_steps(wl, lay, x_log_host, dy_log_host, w, rpt, steps, warmup, device):
@@ -345,25 +370,30 @@ def main():
     class Multi:
         def __init__(self, steps):
             self.steps = steps
-            self.bwd_events = []
 
-        def run(self, stream, time_bwd=False):
+        def run(self, stream):
             for s in self.steps:
-                s.bwd_events = []
-                s.run(stream, time_bwd)
-            self.bwd_events = [e for s in self.steps for e in s.bwd_events]
+                s.run(stream)
 
     multi = Multi(step_objs)
+    # kernels of one step (counted on an eager step)
+    multi.run(stream)
+    torch.cuda.synchronize()
+    l0 = rb.kernel_launches()
+    multi.run(stream)
+    torch.cuda.synchronize()
+    launches = rb.kernel_launches() - l0
     clocks = ClockSampler(local)
-    launches0 = rb.kernel_launches()
     clocks.start()
-    ms, bwd_ms = time_steps(multi, stream, args.steps, args.warmup, flush, dist, time_bwd=True)
-    launches = (rb.kernel_launches() - launches0) // (args.steps + args.warmup)
+    ms, graph = time_steps(multi, stream, args.steps, args.warmup, flush, dist, graph=not args.no_graph)
     # keep the same step running (untimed) so the clock samples cover the load
     t_end = time.time() + 0.6
     while time.time() < t_end:
         for _ in range(20):
-            multi.run(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                multi.run(stream)
         torch.cuda.synchronize()
     clk = clocks.stop()
     ms_step = statistics.mean(ms)
@@ -371,6 +401,7 @@ def main():
         t = torch.tensor([ms_step], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_step = float(t.item())
+    bwd_ms = time_bwd_kernel(step_objs, stream, max(3, args.steps // 2), flush)
 
     H = wl.hidden
     heff = H * sum(rpt_list)
@@ -408,17 +439,19 @@ def main():
         "config": {"workload": workload_desc(wl, lay_name, lay.n_physical), "hidden": H,
                    "heads": list(wl.heads), "tokens": n_act, "layout": lay_name, "calls": len(lay.calls),
                    "l2": "flushed before every timed step (256 MB write); inputs already in HBM",
+                   "launch": "one CUDA graph replay per step" if graph is not None else "eager launches",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm_gbs_step": round(alg_step / (ms_step * 1e-3) / 1e9, 1),
         "frac_step": round(alg_step / (ms_step * 1e-3) / 1e9 / hbm_peak, 4),
         "fwd_gbs": round(fwd_gbs, 1),
-        "roofline": {"bound": "hbm", "kernel": "row_team_kernel<dx+dweight> (fused backward)",
+        "roofline": {"bound": "hbm", "kernel": "fused backward (dx + dweight leaves), rmsnorm_bwd_dx",
                      "achieved": round(achieved_bwd, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved_bwd / hbm_peak, 4), "traffic": None,
                      "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": alg_bwd_launch,
                      "launch_ms": round(bwd_per_launch_ms, 5)},
-        "gpu_launches": int(launches),
+        "gpu_launches": int(launches) * args.steps,
+        "gpu_launches_per_step": int(launches),
         "clocks": clk,
     }
 
@@ -429,7 +462,7 @@ def main():
         for k, v in L.workload_layouts(wl).items():
             so = [Step(wl, v, x, dy, w, rpt, device) for rpt, x, dy, w in steps_data]
             m = Multi(so)
-            t, _ = time_steps(m, stream, max(3, args.steps // 2), 2, flush)
+            t, _ = time_steps(m, stream, max(3, args.steps // 2), 2, flush, graph=not args.no_graph)
             per[k] = {"ms": round(statistics.mean(t), 4), "calls": len(v.calls),
                       "tokens_per_s": round(n_act / (statistics.mean(t) * 1e-3), 1)}
             outs = [s.gather(wl.n_tokens) for s in so]

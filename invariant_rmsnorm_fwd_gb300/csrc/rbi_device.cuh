@@ -37,8 +37,8 @@ struct WsView {                      // device addresses of the workspace region
     uint8_t *block_state;            // [nb][4] per quarter: 0 none, 1 quarter partial, 2 whole-block partial
     uint8_t *leaf_flag;              // [N]    1 = row spilled
     float *block_partial;            // [nb][4][H] quarter partials (slot 0 holds a whole-block partial)
-    float *scratch_a;                // [ceil(nb/64)][H]
-    float *scratch_b;                // [ceil(nb/64)][H]
+    float *scratch_a;                // [ceil(nb/32)][H]
+    float *scratch_b;                // [ceil(nb/32)][H]
     float *spill;                    // [N][H]
     int64_t n_rows, hidden, n_blocks;
 };
@@ -50,7 +50,7 @@ struct WsLayout {
     int64_t off_state, off_flag, off_partial, off_sa, off_sb, off_spill, total;
     __host__ __device__ WsLayout(int64_t N, int64_t H) {
         int64_t nb = (N + kBlockRows - 1) / kBlockRows;
-        int64_t ng = (nb + kBlockRows - 1) / kBlockRows;
+        int64_t ng = (nb + 31) / 32;                     // first-pass groups of 32 blocks
         off_state = 256;
         off_flag = align256(off_state + nb * 4);
         off_partial = align256(off_flag + N);

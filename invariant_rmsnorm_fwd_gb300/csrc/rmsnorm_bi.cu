@@ -374,23 +374,24 @@ extern "C" int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     WsView ws = ws_view(workspace, n_logical_rows, hidden);
     const int V = int(hidden / 8);
-    const unsigned gx = unsigned((V + 31) / 32);
+    const unsigned gy = unsigned((V + kTreeWarps - 1) / kTreeWarps);
     if (ws.n_blocks == 0) {
         zero_f32_kernel<<<1, 256, 0, s>>>(dweight, hidden);
         if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
         g_launches.fetch_add(1, std::memory_order_relaxed);
         return RMSNORM_OK;
     }
-    // pass 1 reads the block partials (rebuilding cut blocks); later passes
-    // ping-pong between the two scratch areas; the last pass writes dweight.
+    // pass 1 forms the block partials and reduces groups of 32; later passes
+    // reduce groups of 32 group results, ping-ponging between the scratch
+    // areas; the pass that leaves one value writes dweight.
     int64_t n = ws.n_blocks;
     const float *in = nullptr;
     bool first = true;
     int flip = 0;
     while (true) {
-        const int64_t groups = (n + kBlockRows - 1) / kBlockRows;
+        const int64_t groups = (n + 31) / 32;
         float *out = groups == 1 ? dweight : (flip ? ws.scratch_b : ws.scratch_a);
-        tree_pass_kernel<<<dim3(gx, unsigned(groups)), 256, 0, s>>>(ws, in, out, n, first ? 1 : 0);
+        tree_pass_kernel<<<dim3(unsigned(groups), gy), kTreeWarps * 32, 0, s>>>(ws, in, out, n, first ? 1 : 0);
         if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
         g_launches.fetch_add(1, std::memory_order_relaxed);
         if (groups == 1) break;

@@ -919,106 +919,109 @@ __global__ void ws_begin_kernel(WsView ws) {
     }
 }
 
-// One pass of the carry tree over `n_in` partials [n_in][H]: group j of 64
-// consecutive inputs is reduced to out[j] (complete 64-tree for a full group,
-// carry tree for a last partial group).  Thread (v, q) reduces the inputs
-// [8q, 8q+8) of the group for columns 8v..8v+7 (levels 1-3); one thread per
-// vector then reduces the up to 8 subgroup results (levels 4-6).  Splitting
-// at aligned power-of-two subgroups leaves the tree unchanged.  In the first
-// pass (from_blocks) an input block cut by a call boundary is rebuilt from
-// its spilled rows with the same 64-leaf tree as the in-kernel path.
+// One pass of the block-partial tree.  Warp (g, v) reduces the partials
+// [32g, 32g+32) of columns 8v..8v+7: lane b holds partial 32g+b, and the 32
+// lanes are combined by butterflies xor 1, 2, 4, 8, 16 where a pair is added
+// only if its right half is non-empty, which is exactly the pairwise tree
+// with odd carry restricted to an aligned group of 32 (later passes reduce
+// the group results the same way).  In the first pass (from_blocks) lane b
+// first forms block b's partial: the four quarter partials as
+// (q0 + q1) + (q2 + q3) (levels 5 and 6 of the 64-leaf tree), a whole-block
+// partial as is, or, for a block cut by a call boundary, the 64-leaf tree
+// over its spilled rows, computed by the whole warp (lane l adds rows 2l and
+// 2l+1, then butterflies xor 1..16): the same tree as the in-kernel path.
 __device__ __forceinline__ void load8(const float *src, float (&v)[8]) {
     const float4 a = ld_global_f32x4(src), b = ld_global_f32x4(src + 4);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-__global__ void __launch_bounds__(256) tree_pass_kernel(WsView ws, const float *in, float *out, int64_t n_in,
-                                                        int from_blocks) {
-    __shared__ float part[8][32][8];                     // [q][vector in CTA][column]
+constexpr int kTreeWarps = 8;                            // warps (vectors) per CTA
+
+__global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, const float *in, float *out,
+                                                                    int64_t n_in, int from_blocks) {
     const int H = int(ws.hidden), V = H >> 3;
-    const int vl = threadIdx.x & 31, q = threadIdx.x >> 5;
-    const int v = blockIdx.x * 32 + vl;
-    const bool has_vec = v < V;
-    const int64_t j = blockIdx.y;
-    const int64_t g0 = j * kBlockRows;
-    const int64_t m = min64(kBlockRows, n_in - g0);   // inputs in this group
+    const int lane = threadIdx.x & 31;
+    const int v = blockIdx.y * kTreeWarps + (threadIdx.x >> 5);
+    if (v >= V) return;                                  // whole warp leaves together
+    const int64_t g = blockIdx.x;
+    const int64_t b = g * 32 + lane;
+    const int m = int(min64(32, n_in - g * 32));          // inputs in this group
     if (from_blocks && !header_ok(ws)) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) set_status(ws.hdr, kStHeader);
-        return;                                          // uniform across the CTA
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) set_status(ws.hdr, kStHeader);
+        return;
     }
-    const int cnt = int(max64(0, min64(8, m - int64_t(q) * 8)));
-    TreeStack<8> st;
-    for (int i = 0; i < cnt; ++i) {
-        const int64_t b = g0 + int64_t(q) * 8 + i;
-        float val[8];
+    float val[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) val[c] = 0.f;
-        const uint32_t state = from_blocks ? reinterpret_cast<const uint32_t *>(ws.block_state)[b] : kStateWhole;
-        if (state == 0) {
-            // cut block: rebuild from the spilled rows with the same 64-leaf tree
-            const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
-            if (vl == 0 && blockIdx.x == 0) {
-                bool missing = false;
-                for (int64_t r = 0; r < rows; ++r) missing |= ws.leaf_flag[b * kBlockRows + r] == 0;
-                if (missing) set_status(ws.hdr, kStMissing);
-            }
-            TreeStack<8> lt;
-#pragma unroll 1
-            for (int r = 0; r < kBlockRows; ++r) {
-                float leaf[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) leaf[c] = 0.f;
-                if (r < rows && has_vec) load8(ws.spill + (b * kBlockRows + r) * int64_t(H) + int64_t(v) * 8, leaf);
-                lt.push(leaf, r, 0);
-                if (r == kBlockRows - 1) {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) val[c] = leaf[c];
-                }
-            }
+    for (int c = 0; c < 8; ++c) val[c] = 0.f;
+    const bool present = lane < m;
+    uint32_t state = kStateWhole;
+    if (present && from_blocks) state = reinterpret_cast<const uint32_t *>(ws.block_state)[b];
+    if (present) {
+        if (!from_blocks) {
+            load8(in + b * int64_t(H) + int64_t(v) * 8, val);
         } else if (state == 0x01010101u) {
-            // four quarter partials: levels 5 and 6 of the block tree
-            if (has_vec) {
-                float q0[8], q1[8], q2[8], q3[8];
-                const float *src = ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8;
-                load8(src, q0);
-                load8(src + H, q1);
-                load8(src + 2 * int64_t(H), q2);
-                load8(src + 3 * int64_t(H), q3);
+            float q0[8], q1[8], q2[8], q3[8];
+            const float *src = ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8;
+            load8(src, q0);
+            load8(src + H, q1);
+            load8(src + 2 * int64_t(H), q2);
+            load8(src + 3 * int64_t(H), q3);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) val[c] = __fadd_rn(__fadd_rn(q0[c], q1[c]), __fadd_rn(q2[c], q3[c]));
-            }
+            for (int c = 0; c < 8; ++c) val[c] = __fadd_rn(__fadd_rn(q0[c], q1[c]), __fadd_rn(q2[c], q3[c]));
         } else if (state == kStateWhole) {
-            if (has_vec) {
-                const float *src = from_blocks ? ws.block_partial + b * 4 * int64_t(H) : in + b * int64_t(H);
-                load8(src + int64_t(v) * 8, val);
-            }
-        } else {
-            if (vl == 0 && blockIdx.x == 0) set_status(ws.hdr, kStMissing);   // partly contributed block
+            load8(ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8, val);
+        } else if (state != 0) {
+            if (v == 0) set_status(ws.hdr, kStMissing);  // partly contributed block
         }
-        st.push(val, i, 0);
     }
-    if (cnt > 0) {
-        float acc[8];
-        st.fold(cnt, acc);
+    // blocks cut by a call boundary: rebuilt by the whole warp, one at a time
+    uint32_t cut = __ballot_sync(kFull, present && from_blocks && state == 0);
+    while (cut) {
+        const int bb = __ffs(cut) - 1;
+        cut &= cut - 1;
+        const int64_t blk = g * 32 + bb;
+        const int64_t rows = min64(kBlockRows, ws.n_rows - blk * kBlockRows);
+        const int64_t r0 = blk * kBlockRows + 2 * lane;
+        float a[8], c2[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) part[q][vl][c] = acc[c];
-    }
-    __syncthreads();
-    if (q == 0 && has_vec) {
-        const int ns = int((m + 7) / 8);
-        TreeStack<8> st2;
-        for (int i = 0; i < ns; ++i) {
-            float val[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) val[c] = part[i][vl][c];
-            st2.push(val, i, 0);
+        for (int c = 0; c < 8; ++c) a[c] = c2[c] = 0.f;
+        bool missing = false;
+        if (2 * lane < rows) {
+            load8(ws.spill + r0 * int64_t(H) + int64_t(v) * 8, a);
+            missing |= ws.leaf_flag[r0] == 0;
         }
-        float res[8];
-        st2.fold(ns, res);
-        float *dst = out + j * int64_t(H) + int64_t(v) * 8;
-        st_global_f32x4(dst, res[0], res[1], res[2], res[3]);
-        st_global_f32x4(dst + 4, res[4], res[5], res[6], res[7]);
+        if (2 * lane + 1 < rows) {
+            load8(ws.spill + (r0 + 1) * int64_t(H) + int64_t(v) * 8, c2);
+            missing |= ws.leaf_flag[r0 + 1] == 0;
+        }
+        if (__any_sync(kFull, missing) && v == 0 && lane == 0) set_status(ws.hdr, kStMissing);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) a[c] = __fadd_rn(a[c], c2[c]);            // level 1: rows 2l, 2l+1
+#pragma unroll
+        for (int k = 1; k < 32; k <<= 1)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) a[c] = __fadd_rn(a[c], __shfl_xor_sync(kFull, a[c], k));
+        if (lane == bb) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) val[c] = a[c];
+        }
+    }
+    // carry tree over the group's (up to) 32 partials
+#pragma unroll
+    for (int k = 1; k < 32; k <<= 1) {
+        const int base = lane & ~(2 * k - 1);
+        const bool add = base + k < m;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float o = __shfl_xor_sync(kFull, val[c], k);
+            val[c] = add ? __fadd_rn(val[c], o) : val[c];
+        }
+    }
+    if (lane == 0) {
+        float *dst = out + g * int64_t(H) + int64_t(v) * 8;
+        st_global_f32x4(dst, val[0], val[1], val[2], val[3]);
+        st_global_f32x4(dst + 4, val[4], val[5], val[6], val[7]);
     }
 }
 
