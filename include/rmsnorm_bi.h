@@ -178,6 +178,38 @@ int rmsnorm_plan_build(const int32_t *host_tok_id, int64_t n_tokens, int32_t row
                        int64_t n_logical_tokens, void *host_plan, size_t capacity,
                        int64_t *plan_items, int64_t *whole_blocks, int64_t *spill_rows);
 
+/*
+ * Allocation-free backward (no counterpart in the paper; it exists for
+ * callers that cannot allocate device memory).  Some callers cannot call
+ * cudaMalloc or an allocating library routine at the point where they run
+ * the backward: code recorded into a CUDA graph without a memory pool,
+ * serving loops that forbid allocation after start-up, or plugins whose host
+ * framework owns all device memory.  This call runs the same kernels as
+ * rmsnorm_dweight_begin + rmsnorm_bwd_dx (with a workspace) +
+ * dweight_finalize, but its workspace is a file-scope device array of
+ * RMSNORM_NOALLOC_SCRATCH_BYTES (16 MiB) inside this library, which every GPU
+ * that loads the library holds until the process exits.
+ *  - The caller passes inputs and outputs only: x, weight, dy, dx (may be
+ *    NULL to skip dx), dweight (FP32 [hidden], required) and optionally
+ *    status (a DEVICE int32 that receives the status word; NULL to skip).
+ *  - The layout is one call that should hold every logical row of its
+ *    multiset; rows missing from it are reported in the status word.
+ *  - Returns RMSNORM_ERR_WORKSPACE, with nothing enqueued, if
+ *    rmsnorm_dweight_workspace_bytes(n_logical_tokens * rows_per_token,
+ *    hidden) exceeds RMSNORM_NOALLOC_SCRATCH_BYTES; other errors as for
+ *    rmsnorm_bwd_dx.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array and clears its flags and status first;
+ *    calls that overlap on the GPU (other streams, other host threads) race
+ *    and must be serialised by the caller.
+ */
+#define RMSNORM_NOALLOC_SCRATCH_BYTES (16u << 20)
+int rmsnorm_bwd_noalloc(const uint16_t *x, const uint16_t *weight, const uint16_t *dy, int64_t hidden,
+                        float eps, const rmsnorm_layout_t *layout, uint16_t *dx, float *dweight,
+                        int32_t *status, rmsnorm_stream_t stream);
+
 /* Static text for a return code. */
 const char *rmsnorm_strerror(int code);
 

@@ -74,6 +74,7 @@ def _load():
         "rmsnorm_plan_bytes": ([I64, I32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
         "rmsnorm_plan_build": ([P, I64, I32, I64, P, ctypes.c_size_t, ctypes.POINTER(I64),
                                 ctypes.POINTER(I64), ctypes.POINTER(I64)], ctypes.c_int),
+        "rmsnorm_bwd_noalloc": ([P, P, P, I64, F, LP, P, P, P, P], ctypes.c_int),
         "rmsnorm_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "rmsnorm_kernel_launches": ([], I64),
     }
@@ -240,3 +241,21 @@ class DweightWorkspace:
 
 def dweight_finalize(workspace: DweightWorkspace, dweight=None, stream=None):
     return workspace.finalize(dweight, stream)
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def rmsnorm_bwd_noalloc(x, weight, dy, lay: CallLayout, eps: float, dx=None, dweight=None, status=None,
+                        stream=None):
+    """Backward with dweight for one call, using the library's built-in scratch
+    instead of a workspace (see rmsnorm_bwd_noalloc in the C header)."""
+    import torch
+    H = weight.shape[0]
+    if dweight is None:
+        dweight = torch.empty(H, dtype=torch.float32, device=x.device)
+    stride = _rows_view(x, lay.rows_per_token, H)
+    L = lay.struct(stride)
+    _check(_load().rmsnorm_bwd_noalloc(_ptr(x), _ptr(weight), _ptr(dy), H, eps, ctypes.byref(L), _ptr(dx),
+                                       _ptr(dweight), _ptr(status), _stream(stream)), "rmsnorm_bwd_noalloc")
+    return dx, dweight

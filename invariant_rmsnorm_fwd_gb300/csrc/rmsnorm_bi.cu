@@ -433,3 +433,58 @@ extern "C" const char *rmsnorm_strerror(int code) {
 }
 
 extern "C" int64_t rmsnorm_kernel_launches(void) { return g_launches.load(); }
+
+// ==================================================================== allocation-free backward
+//
+// The workspace of rmsnorm_bwd_noalloc lives in this file-scope device array.
+// In host code the symbol is only a stand-in; its device address is looked up
+// once per device with cudaGetSymbolAddress and passed to the kernels.
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[RMSNORM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[64] = {nullptr};
+
+int noalloc_address(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RMSNORM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return RMSNORM_ERR_CUDA;
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return RMSNORM_OK;
+}
+}  // namespace
+
+extern "C" int rmsnorm_bwd_noalloc(const uint16_t *x, const uint16_t *weight, const uint16_t *dy, int64_t hidden,
+                                   float eps, const rmsnorm_layout_t *layout, uint16_t *dx, float *dweight,
+                                   int32_t *status, rmsnorm_stream_t stream) {
+    Shape sh;
+    if (!hidden_shape(hidden, &sh)) return RMSNORM_ERR_HIDDEN;
+    int rc = check_layout(layout, hidden);
+    if (rc) return rc;
+    if (!dweight) return RMSNORM_ERR_NULL;
+    const int64_t N = layout->n_logical_tokens * layout->rows_per_token;
+    const size_t need = rmsnorm_dweight_workspace_bytes(N, hidden);
+    if (need == 0) return RMSNORM_ERR_LAYOUT;
+    if (need > RMSNORM_NOALLOC_SCRATCH_BYTES) return RMSNORM_ERR_WORKSPACE;
+    if (layout->n_tokens > 0 && !layout->plan) return RMSNORM_ERR_PLAN;
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    void *ws = nullptr;
+    if ((rc = noalloc_address(&ws))) return rc;
+    if ((rc = rmsnorm_dweight_begin(ws, RMSNORM_NOALLOC_SCRATCH_BYTES, N, hidden, stream))) return rc;
+    if (layout->n_tokens > 0 && (rc = rmsnorm_bwd_dx(x, weight, dy, hidden, eps, layout, dx, ws, stream))) return rc;
+    if ((rc = dweight_finalize(ws, N, hidden, dweight, stream))) return rc;
+    if (status) {
+        const WsHeader *h = static_cast<const WsHeader *>(ws);
+        if (cudaMemcpyAsync(status, &h->status, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+    }
+    return RMSNORM_OK;
+}
