@@ -63,6 +63,32 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def source_sha256():
+    """Hash of the library sources, to tell whether a recorded ncu traffic still applies."""
+    import glob
+    import hashlib
+    files = sorted(glob.glob(os.path.join(ROOT, "invariant_rmsnorm_fwd_gb300", "csrc", "*")))
+    files += sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic(config: str, layout: str):
+    """DRAM bytes per launch of the fused backward from profiles/traffic.json, or None
+    if it was taken on another workload or the kernels changed since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    if d.get("workload") != config or d.get("layout") != layout or d.get("source_sha256") != source_sha256():
+        return None
+    return int(d["dram_bytes_read"]) + int(d["dram_bytes_write"])
+
+
 def workload_desc(wl, lay_name, n_phys):
     heads = "x".join(str(h) for h in wl.heads)
     return (f"{wl.name}: hidden={wl.hidden}, heads={heads}, {len(wl.lengths)} samples, "
@@ -446,7 +472,8 @@ def main():
         "fwd_gbs": round(fwd_gbs, 1),
         "roofline": {"bound": "hbm", "kernel": "fused backward (dx + dweight leaves), rmsnorm_bwd_dx",
                      "achieved": round(achieved_bwd, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved_bwd / hbm_peak, 4), "traffic": None,
+                     "frac": round(achieved_bwd / hbm_peak, 4),
+                     "traffic": (recorded_traffic(args.config, lay_name) if bwd_calls == 1 else None),
                      "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": alg_bwd_launch,
                      "launch_ms": round(bwd_per_launch_ms, 5)},
