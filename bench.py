@@ -5,8 +5,9 @@ One step = the whole hot path over one batch of the workload in one physical
 layout: rmsnorm_fwd on every call, rmsnorm_dweight_begin, rmsnorm_bwd_dx
 (dx fused with the dweight contribution) on every call, dweight_finalize.
 Inputs are resident in HBM when the timed region starts; L2 is flushed
-(256 MB write) before every timed step; each step is timed with CUDA events
-on the launching stream.  `value` is active tokens per second; the roofline
+before every timed step (a 256 MB write, then a 256 MB read so that no dirty
+lines are left to be written back inside the timed region); each step is
+timed with CUDA events on the launching stream.  `value` is active tokens per second; the roofline
 object reports the dominant kernel (the fused backward) against the measured
 HBM copy bandwidth.  `e2e` is the same metric through the public API with
 host buffers: plans built on the host, inputs copied in from pinned memory
@@ -156,6 +157,24 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ GPU arm
 
+class L2Flush:
+    """Runs between timed steps, untimed: writes a 256 MB buffer (twice the 129 MB L2),
+    then reads a second 256 MB buffer so that the dirty lines of the write are written
+    back before the timed region instead of during it.  L2 ends clean and holds none
+    of the workload's data."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        self.r = torch.ones(64 << 20, dtype=torch.int32, device=device)
+        self.sink = torch.empty((), dtype=torch.int32, device=device)
+
+    def __call__(self):
+        import torch
+        self.w.fill_(1)
+        torch.amax(self.r, dim=0, out=self.sink)
+
+
 class Step:
     """Device-resident buffers of one layout and the launch sequence of one step."""
 
@@ -182,13 +201,43 @@ class Step:
         self.bwd_events = []
 
     def run(self, stream):
+        """Calls of a multi-call layout are independent (they touch disjoint rows and
+        blocks of the workspace), so they are spread over up to four streams that
+        fork from and join back into `stream`; one-call layouts stay on `stream`."""
+        import torch
         rb = self.rb
-        for cl, xp, dp, yp, dxp in self.calls:
-            rb.rmsnorm_fwd(xp, self.w, cl, self.eps, y=yp, stream=stream)
+        lanes = self._lanes(stream)
+
+        def fan(fn):
+            if len(lanes) == 1:
+                for c in self.calls:
+                    fn(c, stream)
+                return
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            for i, c in enumerate(self.calls):
+                st = lanes[i % len(lanes)]
+                if i < len(lanes):
+                    st.wait_event(ev)
+                fn(c, st)
+            for st in lanes[:min(len(lanes), len(self.calls))]:
+                e = torch.cuda.Event()
+                e.record(st)
+                stream.wait_event(e)
+
+        fan(lambda c, st: rb.rmsnorm_fwd(c[1], self.w, c[0], self.eps, y=c[3], stream=st))
         self.ws.begin(stream)
-        for cl, xp, dp, yp, dxp in self.calls:
-            rb.rmsnorm_bwd_dx(xp, self.w, dp, cl, self.eps, dx=dxp, workspace=self.ws, stream=stream)
+        fan(lambda c, st: rb.rmsnorm_bwd_dx(c[1], self.w, c[2], c[0], self.eps, dx=c[4], workspace=self.ws,
+                                            stream=st))
         self.ws.finalize(self.dw, stream)
+
+    def _lanes(self, stream):
+        import torch
+        if len(self.calls) == 1:
+            return [stream]
+        if getattr(self, "_side", None) is None:
+            self._side = [torch.cuda.Stream(device=self.dw.device) for _ in range(4)]
+        return self._side
 
     def time_fwd_only(self, stream):
         import torch
@@ -233,7 +282,7 @@ def time_steps(step, stream, steps, warmup, flush, dist=None, graph=True):
     torch.cuda.synchronize()
     times = []
     for _ in range(steps):
-        flush.fill_(1)
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         if g is not None:
@@ -256,7 +305,7 @@ def time_bwd_kernel(step_objs, stream, reps, flush):
         for so in step_objs:
             so.ws.begin(stream)
             for cl, xp, dp, yp, dxp in so.calls:
-                flush.fill_(1)
+                flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 so.rb.rmsnorm_bwd_dx(xp, so.w, dp, cl, so.eps, dx=dxp, workspace=so.ws, stream=stream)
@@ -378,7 +427,7 @@ def main():
     lay_name = args.layout or wl.headline
     rpt_list = list(wl.heads)
     hbm_peak, peak_kind = measured_peaks()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     stream = torch.cuda.current_stream()
 
     steps_data = []
@@ -442,7 +491,7 @@ def main():
     # forward alone, for the record
     fwd_ms = []
     for _ in range(max(3, args.steps // 2)):
-        flush.fill_(1)
+        flush()
         evs = [s.time_fwd_only(stream) for s in step_objs]
         torch.cuda.synchronize()
         fwd_ms.append(sum(a.elapsed_time(b) for a, b in evs))
@@ -464,7 +513,7 @@ def main():
         "data": "synthetic (seeded SplitMix64/Box-Muller, keyed by logical token id)",
         "config": {"workload": workload_desc(wl, lay_name, lay.n_physical), "hidden": H,
                    "heads": list(wl.heads), "tokens": n_act, "layout": lay_name, "calls": len(lay.calls),
-                   "l2": "flushed before every timed step (256 MB write); inputs already in HBM",
+                   "l2": "flushed before every timed step (256 MB write, then a 256 MB read so no dirty lines remain); inputs already in HBM",
                    "launch": "one CUDA graph replay per step" if graph is not None else "eager launches",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm_gbs_step": round(alg_step / (ms_step * 1e-3) / 1e9, 1),

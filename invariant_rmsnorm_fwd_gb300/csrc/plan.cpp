@@ -15,7 +15,7 @@
 #include <utility>
 #include <vector>
 
-#include "../../include/rmsnorm_bi.h"
+#include "rmsnorm_bi.h"
 
 namespace {
 

@@ -159,12 +159,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 }
 
 // Waits for the phase with the given parity; gives up after ~1 s of wall time.
+// Between polls the warp sleeps (32 ns, doubling to 256 ns) so that waiting
+// warps leave the issue slots to the warps that have work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+    uint32_t ns = 32;
 #pragma unroll 1
     while (true) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        __nanosleep(ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (ns < 256) ns <<= 1;
         if (global_timer_ns() - t0 > 1000000000ull) return false;
     }
 }

@@ -8,7 +8,7 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/rmsnorm_bi.h"
+#include "rmsnorm_bi.h"
 #include "rmsnorm_kernels.cuh"
 
 using namespace rbi;
@@ -159,7 +159,7 @@ int launch_team_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaSt
     }
 }
 
-template <int MODE, int R, int MAXT>
+template <int MODE, int R, int MAXT, int NS>
 int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
     constexpr int nt = ModeTraits<MODE>::kTensors;
     const int64_t stage_bytes = int64_t(R) * nt * p.hidden * 2;
@@ -168,9 +168,9 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
     if (S > kSplitMaxStages) S = kSplitMaxStages;
     if (S < 2) return RMSNORM_ERR_HIDDEN;
     const int smem = int(off + S * stage_bytes);
-    const int threads = (sh.nc + kSplitStatsWarps + 1) * 32;
+    const int threads = (sh.nc + NS + 1) * 32;
     if (threads > MAXT) return RMSNORM_ERR_HIDDEN;
-    auto kern = split_kernel<MODE, R, MAXT, kSplitStatsWarps>;
+    auto kern = split_kernel<MODE, R, MAXT, NS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
     int per_sm = 0;
@@ -187,8 +187,8 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
 
 template <int MODE, int R>
 int launch_split(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
-    if ((sh.nc + kSplitStatsWarps + 1) * 32 <= 608) return launch_split_t<MODE, R, 608>(p, sh, d, stream);
-    return launch_split_t<MODE, R, 768>(p, sh, d, stream);
+    if ((sh.nc + kSplitStatsWarps + 1) * 32 <= 608) return launch_split_t<MODE, R, 608, kSplitStatsWarps>(p, sh, d, stream);
+    return launch_split_t<MODE, R, 768, kSplitStatsWarps>(p, sh, d, stream);
 }
 
 template <int MODE, int P2>
@@ -229,7 +229,7 @@ int run_rows(KParams p, const Shape &sh, const rmsnorm_layout_t *L, cudaStream_t
     constexpr bool leaves = ModeTraits<MODE>::kLeaves;
     const bool plan = p.use_plan != 0;
     if (sh.split) {
-        constexpr int R = (MODE == kFwd) ? 4 : 2;
+        constexpr int R = (MODE == kFwd) ? 4 : 2;        // rows per pipeline stage (measured best)
         if (plan) p.n_units = leaves ? L->plan_items * 4 : L->plan_items * (kBlockRows / R);
         else p.n_units = (p.n_rows + R - 1) / R;
         if (p.n_units == 0) return RMSNORM_OK;

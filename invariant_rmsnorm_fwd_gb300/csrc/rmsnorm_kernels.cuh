@@ -125,6 +125,7 @@ template <int R>
 struct SlotBatch {                   // metadata of one batch, held by the producer thread
     int32_t prow[R];
     int32_t lrow[R];
+    int32_t kind, block;             // plan item header (split kernel)
 };
 
 // Shared-memory header of row_team_kernel: barriers, abort flag, per-stage
@@ -464,6 +465,7 @@ struct SplitStats {
     float mg;
 };
 
+constexpr int kSplitItemOff = 320;                                   // [kSplitMaxStages] int2 item headers
 constexpr int kSplitMetaOff = 512;                                   // after 3 x 12 barriers (288 B) + flag
 constexpr int kSplitStatsOff = kSplitMetaOff + kSplitMaxStages * kMaxBatch * 16;
 constexpr int kSplitWOff = kSplitStatsOff + kSplitMaxStages * kMaxBatch * 8;   // FP32 weight [H]
@@ -480,6 +482,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     uint64_t *empty = stats_bar + kSplitMaxStages;
     volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + 3 * kSplitMaxStages * 8);
     StageMeta *meta = reinterpret_cast<StageMeta *>(smem + kSplitMetaOff);   // [S][R]
+    int2 *item_hdr = reinterpret_cast<int2 *>(smem + kSplitItemOff);          // [S] (kind, block)
     SplitStats *stats = reinterpret_cast<SplitStats *>(smem + kSplitStatsOff);
     float *wsm = reinterpret_cast<float *>(smem + kSplitWOff);
     const int H = p.hidden;
@@ -531,10 +534,47 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
 
     if (warp == NC + NS) {
         // ------------------------------------------------ producer
+        // The slot metadata of batch k comes from global memory (plan or
+        // tok_id); it is loaded kPrefetch batches ahead so that issuing the
+        // copies never waits on it.
         if (lane == 0) {
+            constexpr int kPrefetch = 3;
+            SlotBatch<R> ring[kPrefetch];
+            auto load = [&](int k, SlotBatch<R> &mb) {
+                if (k >= n_batches) return;
+                int64_t item;
+                int slot0;
+                batch_slots(k, item, slot0);
+                mb.kind = 0;
+                mb.block = -1;
+                if (item_units) {
+                    mb.kind = p.items[item].kind;
+                    mb.block = p.items[item].block;
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    int32_t pr = -1, lr = -1;
+                    if (p.use_plan) {
+                        const PlanItem *it = p.items + item;
+                        pr = it->prow[slot0 + r];
+                        lr = it->lrow[slot0 + r];
+                    } else {
+                        const int64_t row = item * R + r;
+                        if (row < p.n_rows) pr = p.tok_id[row / p.rpt] >= 0 ? int32_t(row) : -1;
+                    }
+                    mb.prow[r] = pr;
+                    mb.lrow[r] = lr;
+                }
+            };
+#pragma unroll
+            for (int i = 0; i < kPrefetch; ++i) load(i, ring[i]);
             int s = 0;
             uint32_t ph = 0;                             // parity of the current use of stage s
             for (int k = 0; k < n_batches; ++k) {
+                const SlotBatch<R> cur = ring[0];
+#pragma unroll
+                for (int i = 0; i + 1 < kPrefetch; ++i) ring[i] = ring[i + 1];
+                load(k + kPrefetch, ring[kPrefetch - 1]);
                 if (k >= S && !mbar_wait_bounded(&empty[s], ph ^ 1u)) {
                     *abort_flag = 1;
                     if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
@@ -552,23 +592,13 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     }
                     break;
                 }
-                int64_t item;
-                int slot0;
-                batch_slots(k, item, slot0);
                 StageMeta *m = meta + s * R;
+                item_hdr[s] = make_int2(cur.kind, cur.block);
                 int64_t offs[R];
                 uint32_t n_act = 0;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    int32_t pr = -1, lr = -1;
-                    if (p.use_plan) {
-                        const PlanItem *it = p.items + item;
-                        pr = it->prow[slot0 + r];
-                        lr = it->lrow[slot0 + r];
-                    } else {
-                        const int64_t row = item * R + r;
-                        if (row < p.n_rows && p.tok_id[row / p.rpt] >= 0) pr = int32_t(row);
-                    }
+                    const int32_t pr = cur.prow[r], lr = cur.lrow[r];
                     bool act = pr >= 0;
                     if (act && (pr >= p.n_rows || (T::kLeaves && (lr < 0 || lr >= p.ws.n_rows)))) {
                         if (T::kLeaves) set_status(p.ws.hdr, kStPlan);
@@ -683,21 +713,21 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                 u += gridDim.x;
             }
         }
-        if (item_units && sub == 0) {
-            const PlanItem *it = p.items + (u >> 2);
-            quarter = int(u & 3);
-            kind = it->kind;
-            block = it->block;
-            if ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1)) {
-                if (t == 0) set_status(p.ws.hdr, kStPlan);
-                kind = 2;
-            }
-        }
         if (*abort_flag) break;
         if (!mbar_wait_bounded(&stats_bar[s], parity) || !mbar_wait_bounded(&full[s], parity)) {
             *abort_flag = 1;
             if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
             break;
+        }
+        if (item_units && sub == 0) {                    // item header, staged by the producer
+            const int2 hd = item_hdr[s];
+            quarter = int(u & 3);
+            kind = hd.x;
+            block = hd.y;
+            if ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1)) {
+                if (t == 0) set_status(p.ws.hdr, kStPlan);
+                kind = 2;
+            }
         }
         const StageMeta *m = meta + s * R;
         TreeStackF2<4, (kLogR > 0 ? kLogR : 1)> mini;
