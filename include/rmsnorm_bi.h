@@ -42,8 +42,8 @@
  *    logical row contributed twice or never, a workspace set up for other
  *    sizes, a pipeline wait that timed out) set bits in the workspace's
  *    status word (rmsnorm_dweight_status); no kernel ever traps.
- *  - Supported hidden sizes: multiples of 8 up to 5120, multiples of 512
- *    up to 8192, and multiples of 1024 up to 16384.
+ *  - Supported hidden sizes: multiples of 8 up to 5120, multiples of 16 up
+ *    to 10240, and multiples of 32 up to 16384.
  */
 #ifndef RMSNORM_BI_H
 #define RMSNORM_BI_H

@@ -184,6 +184,42 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
+// Cluster-scope variants used by the cross-CTA exchange of row-sum partials.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t ns = 32;
+#pragma unroll 1
+    while (true) {
+        __nanosleep(ns);
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (ns < 256) ns <<= 1;
+        if (global_timer_ns() - t0 > 1000000000ull) return false;
+    }
+}
+
+// Arrive on the mbarrier at shared::cluster address `addr` (possibly another
+// CTA's), releasing this thread's earlier shared-memory stores at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -454,17 +490,14 @@ struct TreeStackF2 {
 // Canonical row-sum trees.  The sum of squares (and, in the backward, the
 // sum of dy*w*x) of a row is formed by a tree that depends on H only:
 //
-//  hidden <= 256 (small_row_kernel): each 8-column vector is folded in
-//   column order with fused multiply-adds (s = a0*b0; s = fma(ai, bi, s)),
-//   then the V = H/8 vector sums, zero-padded to P = next_pow2(V), are added
-//   by a complete tree with adjacent pairing: (0,1), (2,3), ... (xor
-//   butterflies 1, 2, 4, ...).
-//  hidden > 256 (row_team_kernel): each vector is folded as two chains
-//   (columns 0,2,4,6 and 1,3,5,7, see dot8x2) that are then added; the 32
-//   vectors of warp w (vectors 32w..32w+31, absent ones +0) by a complete
-//   tree pairing lanes 16 apart first, then 8, 4, 2, 1; the W warp sums by
-//   adding warp w+32 to warp w when W > 32, then the same tree over the 32
-//   slots (absent warps +0).
+//  hidden <= 256 (small_row_kernel): each 8-column vector is folded as two
+//   FMA chains (columns 0,2,4,6 and 1,3,5,7) that are then added, and the
+//   V = H/8 vector sums, zero-padded to P = next_pow2(V), are added by a
+//   complete tree with adjacent pairing: (0,1), (2,3), ... (xor butterflies
+//   1, 2, 4, ...).
+//  hidden > 256 (split_kernel): see the description above split_kernel in
+//   rmsnorm_kernels.cuh (lane folds within each column slice, a lane tree
+//   pairing 16 apart first, then the slice sums in a fixed order).
 //
 // The forward and the backward use the same kernel family for a given H, so
 // rstd is bitwise the same in both.

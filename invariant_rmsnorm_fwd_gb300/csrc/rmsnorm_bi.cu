@@ -51,14 +51,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Shape {
     bool small = false;   // small_row_kernel
-    bool split = false;   // split_kernel (warp-specialised, one CTA per row team)
     int p2 = 0;           // lanes per row (small)
-    int k = 1;            // CTAs per team (row_team_kernel)
-    int threads = 0;      // threads per CTA (row_team_kernel)
-    int nc = 0;           // column warps (split)
+    int k = 1;            // CTAs per row team (split_kernel), a cluster when > 1
+    int nc = 0;           // column warps per CTA (split_kernel)
 };
 
 constexpr int kSplitStatsWarps = 2;
+constexpr int kSliceMaxVectors = 640;                    // columns per CTA <= 5120
 
 bool hidden_shape(int64_t H, Shape *s) {
     if (H < 8 || H % 8 != 0 || H > 16384) return false;
@@ -70,15 +69,10 @@ bool hidden_shape(int64_t H, Shape *s) {
         s->p2 = p;
         return true;
     }
-    if (V <= 640) {
-        s->split = true;
-        s->nc = int((V + 31) / 32);
-        return true;
-    }
-    for (int k = 2; k <= 4; k *= 2) {
-        if (V % (32 * k) == 0 && V / k <= 512) {
+    for (int k = 1; k <= kSplitMaxK; k *= 2) {
+        if (V % k == 0 && V / k <= kSliceMaxVectors) {
             s->k = k;
-            s->threads = int(V / k);
+            s->nc = int((V / k + 31) / 32);
             return true;
         }
     }
@@ -101,28 +95,27 @@ int check_layout(const rmsnorm_layout_t *L, int64_t H) {
 
 // ---------------------------------------------------------------- launches
 
-constexpr int kHeaderSmem = kSmemStageOff;
-
-template <int MODE, int K, int R>
-int launch_team(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
+template <int MODE, int R, int MAXT, int NS, int K>
+int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
     constexpr int nt = ModeTraits<MODE>::kTensors;
-    const int64_t slice = (p.hidden / 8 / K) * 16;
-    const int64_t stage_bytes = slice * nt * R;
-    const int64_t budget = int64_t(d.max_smem) - kHeaderSmem;
-    int S = int(budget / stage_bytes);
-    if (S > kMaxStages) S = kMaxStages;
+    const int slice = p.hidden / K;
+    const int64_t stage_bytes = int64_t(R) * nt * slice * 2;
+    const int64_t off = split_stage_off(slice);
+    int S = int((int64_t(d.max_smem) - off) / stage_bytes);
+    if (S > kSplitMaxStages) S = kSplitMaxStages;
     if (S < 2) return RMSNORM_ERR_HIDDEN;
-    const int smem = int(kHeaderSmem + S * stage_bytes);
-    auto kern = row_team_kernel<MODE, K, R>;
+    const int smem = int(off + S * stage_bytes);
+    const int threads = (sh.nc + NS + 1) * 32;
+    if (threads > MAXT) return RMSNORM_ERR_HIDDEN;
+    auto kern = split_kernel<MODE, R, MAXT, NS, K>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
-
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(sh.threads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    int64_t clusters;
+    int64_t teams;
     if (K > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = K;
@@ -132,77 +125,52 @@ int launch_team(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStre
         cfg.numAttrs = 1;
         cfg.gridDim = dim3(K * d.sms);
         int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1)
-            return RMSNORM_ERR_CUDA;
-        clusters = active;
+        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) return RMSNORM_ERR_CUDA;
+        teams = active;
     } else {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, sh.threads, smem) != cudaSuccess ||
-            per_sm < 1)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
             return RMSNORM_ERR_CUDA;
-        clusters = int64_t(per_sm) * d.sms;
+        teams = int64_t(per_sm) * d.sms;
     }
-    if (clusters > p.n_units) clusters = p.n_units;
-    if (clusters < 1) return RMSNORM_OK;
-    cfg.gridDim = dim3(unsigned(clusters * K));
-    if (cudaLaunchKernelEx(&cfg, kern, p, S) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (teams > p.n_units) teams = p.n_units;
+    if (teams < 1) return RMSNORM_OK;
+    cfg.gridDim = dim3(unsigned(teams * K));
+    if (cudaLaunchKernelEx(&cfg, kern, p, S, sh.nc) != cudaSuccess) return RMSNORM_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return RMSNORM_OK;
 }
 
-template <int MODE, int R>
-int launch_team_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t s) {
-    switch (sh.k) {
-        case 2: return launch_team<MODE, 2, R>(p, sh, d, s);
-        case 4: return launch_team<MODE, 4, R>(p, sh, d, s);
-        default: return RMSNORM_ERR_HIDDEN;
-    }
-}
-
-template <int MODE, int R, int MAXT, int NS>
-int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
-    constexpr int nt = ModeTraits<MODE>::kTensors;
-    const int64_t stage_bytes = int64_t(R) * nt * p.hidden * 2;
-    const int64_t off = split_stage_off(p.hidden);
-    int S = int((int64_t(d.max_smem) - off) / stage_bytes);
-    if (S > kSplitMaxStages) S = kSplitMaxStages;
-    if (S < 2) return RMSNORM_ERR_HIDDEN;
-    const int smem = int(off + S * stage_bytes);
-    const int threads = (sh.nc + NS + 1) * 32;
-    if (threads > MAXT) return RMSNORM_ERR_HIDDEN;
-    auto kern = split_kernel<MODE, R, MAXT, NS>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return RMSNORM_ERR_CUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
-        return RMSNORM_ERR_CUDA;
-    int64_t blocks = int64_t(per_sm) * d.sms;
-    if (blocks > p.n_units) blocks = p.n_units;
-    if (blocks < 1) return RMSNORM_OK;
-    kern<<<unsigned(blocks), threads, smem, stream>>>(p, S, sh.nc);
-    if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return RMSNORM_OK;
+template <int MODE, int R, int K>
+int launch_split_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
+    if ((sh.nc + kSplitStatsWarps + 1) * 32 <= 608)
+        return launch_split_t<MODE, R, 608, kSplitStatsWarps, K>(p, sh, d, stream);
+    return launch_split_t<MODE, R, 768, kSplitStatsWarps, K>(p, sh, d, stream);
 }
 
 template <int MODE, int R>
 int launch_split(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
-    if ((sh.nc + kSplitStatsWarps + 1) * 32 <= 608) return launch_split_t<MODE, R, 608, kSplitStatsWarps>(p, sh, d, stream);
-    return launch_split_t<MODE, R, 768, kSplitStatsWarps>(p, sh, d, stream);
+    switch (sh.k) {
+        case 1: return launch_split_k<MODE, R, 1>(p, sh, d, stream);
+        case 2: return launch_split_k<MODE, R, 2>(p, sh, d, stream);
+        case 4: return launch_split_k<MODE, R, 4>(p, sh, d, stream);
+        default: return RMSNORM_ERR_HIDDEN;
+    }
 }
 
 template <int MODE, int P2>
 int launch_small(const KParams &p, const DeviceInfo &d, cudaStream_t stream) {
-    constexpr int U = 4;
+    constexpr int U = ModeTraits<MODE>::kLeaves ? 4 : 8;   // warp steps loaded together
+    constexpr int threads = kSmallWarps * 32;
     auto kern = small_row_kernel<MODE, P2, U>;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess || per_sm < 1)
         return RMSNORM_ERR_CUDA;
     int64_t blocks = int64_t(per_sm) * d.sms;
-    const int64_t need = (p.n_units + 7) / 8;            // 8 warps per block, one unit per warp
+    const int64_t need = (p.n_units + kSmallWarps - 1) / kSmallWarps;   // one unit per warp at least
     if (blocks > need) blocks = need;
     if (blocks < 1) return RMSNORM_OK;
-    kern<<<unsigned(blocks), 256, 0, stream>>>(p);
+    kern<<<unsigned(blocks), threads, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return RMSNORM_OK;
@@ -228,25 +196,16 @@ int run_rows(KParams p, const Shape &sh, const rmsnorm_layout_t *L, cudaStream_t
     if (rc != RMSNORM_OK) return rc;
     constexpr bool leaves = ModeTraits<MODE>::kLeaves;
     const bool plan = p.use_plan != 0;
-    if (sh.split) {
-        constexpr int R = (MODE == kFwd) ? 4 : 2;        // rows per pipeline stage (measured best)
-        if (plan) p.n_units = leaves ? L->plan_items * 4 : L->plan_items * (kBlockRows / R);
-        else p.n_units = (p.n_rows + R - 1) / R;
+    if (sh.small) {
+        p.n_units = plan ? L->plan_items : (p.n_rows + kBlockRows - 1) / kBlockRows;
         if (p.n_units == 0) return RMSNORM_OK;
-        return launch_split<MODE, R>(p, sh, *d, stream);
+        return launch_small_p<MODE>(p, sh, *d, stream);
     }
-    constexpr int R = (MODE == kFwd) ? 8 : 4;
-    if (plan) {
-        // dweight modes work on whole plan items; the others on R-row batches of items
-        p.n_units = (leaves || sh.small) ? L->plan_items : L->plan_items * (kBlockRows / R);
-    } else if (sh.small) {
-        p.n_units = (p.n_rows + kBlockRows - 1) / kBlockRows;
-    } else {
-        p.n_units = (p.n_rows + R - 1) / R;
-    }
+    constexpr int R = (MODE == kFwd) ? 4 : 2;            // rows per pipeline stage (measured best)
+    if (plan) p.n_units = leaves ? L->plan_items * 4 : L->plan_items * (kBlockRows / R);
+    else p.n_units = (p.n_rows + R - 1) / R;
     if (p.n_units == 0) return RMSNORM_OK;
-    if (sh.small) return launch_small_p<MODE>(p, sh, *d, stream);
-    return launch_team_k<MODE, R>(p, sh, *d, stream);
+    return launch_split<MODE, R>(p, sh, *d, stream);
 }
 
 KParams base_params(const rmsnorm_layout_t *L, int64_t H, float eps) {
@@ -255,6 +214,9 @@ KParams base_params(const rmsnorm_layout_t *L, int64_t H, float eps) {
     p.n_rows = L->n_tokens * L->rows_per_token;
     p.token_stride = L->token_stride;
     p.rpt = L->rows_per_token;
+    p.rpt_shift = -1;
+    for (int sh = 0; sh < 31; ++sh)
+        if ((int64_t(1) << sh) == int64_t(p.rpt)) p.rpt_shift = sh;
     p.hidden = int32_t(H);
     p.eps = eps;
     p.items = static_cast<const PlanItem *>(L->plan);

@@ -2,16 +2,11 @@
 //
 // Two kernel families share the numeric helpers of rbi_device.cuh:
 //
-//  * row_team_kernel (hidden > 256): a "team" of K CTAs (a thread-block
-//    cluster when K > 1) owns one row at a time; every thread owns one
-//    16-byte vector of 8 columns.  Rows are staged into shared memory by 1-D
-//    bulk copies (cp.async.bulk + mbarrier transaction counts) issued S
-//    batches ahead by one elected thread; each batch holds R rows.  Per batch
-//    the team forms the row sums (lane butterfly, then a butterfly over the
-//    warp partials, exchanged through distributed shared memory when K > 1),
-//    then writes y or dx and feeds the dweight leaves of the batch into the
-//    64-leaf tree held in registers.  CTAs are persistent: cluster c takes
-//    work units c, c + n_clusters, ...
+//  * split_kernel (hidden > 256): a warp-specialised pipeline per row team
+//    of K CTAs (a thread-block cluster when K > 1).  A producer warp stages
+//    rows into shared memory with 1-D bulk copies (cp.async.bulk, mbarrier
+//    transaction counts), stats warps publish each row's rstd and mean, and
+//    column warps write y or dx and reduce the dweight leaves.
 //
 //  * small_row_kernel (hidden <= 256): a team is P2 = next_pow2(hidden/8)
 //    lanes of one warp, so a warp works on 32/P2 rows at once with 16-byte
@@ -20,10 +15,9 @@
 //
 // Work units are either plan items (64 row slots: a whole logical block in
 // logical order, or rows of blocks cut by a call boundary) or, without a
-// plan, 64 consecutive physical rows / R-row batches whose tok_id says
-// whether a row is active.  Which unit a CTA processes never changes a
-// value: every output depends only on its row (y, dx, the leaf) or on the
-// fixed trees.
+// plan, groups of consecutive physical rows whose tok_id says whether a row
+// is active.  Which CTA processes which unit never changes a value: every
+// output depends only on its row (y, dx, the leaf) or on the fixed trees.
 #pragma once
 #include "rbi_device.cuh"
 
@@ -44,6 +38,7 @@ struct KParams {
     int64_t n_rows;                  // physical rows of the call = n_tokens * rpt
     int64_t token_stride;            // elements
     int32_t rpt;                     // rows per token
+    int32_t rpt_shift;               // log2(rpt) if rpt is a power of two, else -1
     int32_t hidden;
     float eps;
     int32_t use_plan;                // 1: units are plan items
@@ -54,8 +49,9 @@ struct KParams {
 
 __device__ __forceinline__ int64_t row_offset(const KParams &p, int64_t prow) {
     if (p.rpt == 1) return prow * p.token_stride;
-    const int64_t t = prow / p.rpt;
-    return t * p.token_stride + (prow - t * p.rpt) * int64_t(p.hidden);
+    const uint32_t r = uint32_t(prow);                  // rows of a call are < 2^31
+    const uint32_t t = p.rpt_shift >= 0 ? (r >> p.rpt_shift) : r / uint32_t(p.rpt);
+    return int64_t(t) * p.token_stride + int64_t(r - t * uint32_t(p.rpt)) * int64_t(p.hidden);
 }
 
 template <int MODE>
@@ -112,7 +108,7 @@ __device__ __forceinline__ void mark_spilled_row(const WsView &ws, int64_t lrow)
 }
 
 // =====================================================================
-// Large hidden sizes: team = K CTAs, one vector per thread, bulk-copy staging
+// Per-stage row metadata
 // =====================================================================
 
 struct StageMeta {
@@ -128,350 +124,56 @@ struct SlotBatch {                   // metadata of one batch, held by the produ
     int32_t kind, block;             // plan item header (split kernel)
 };
 
-// Shared-memory header of row_team_kernel: barriers, abort flag, per-stage
-// row metadata, and the warp partials of the row sums.
-constexpr int kMaxStages = 8;
-constexpr int kMaxBatch = 8;                     // R <= 8
-constexpr int kMaxTeamWarps = 64;                // W <= 64
-constexpr int kMaxVals = 16;                     // row sums per batch <= 16
-constexpr int kSmemMetaOff = 128;
-constexpr int kSmemRedOff = kSmemMetaOff + kMaxStages * kMaxBatch * 16;
-constexpr int kSmemStageOff = kSmemRedOff + 2 * 16 * kMaxVals * 4;   // [2 parity][16 local warps][kMaxVals]
-static_assert(kSmemStageOff % 128 == 0, "stage buffers are 128-byte aligned");
-
-template <int MODE, int K, int R>
-__global__ void __launch_bounds__(512, 1) row_team_kernel(const KParams p, const int S) {
-    using T = ModeTraits<MODE>;
-    constexpr int kNB = kBlockRows / R;                 // batches per plan item
-    constexpr int kLogR = (R == 1) ? 0 : (R == 2) ? 1 : (R == 4) ? 2 : 3;
-    constexpr int NV = T::kNeedGx ? 2 * R : R;          // row sums reduced per batch
-    constexpr int kLogNV = (NV == 2) ? 1 : (NV == 4) ? 2 : (NV == 8) ? 3 : 4;
-    constexpr int kSh = 5 - kLogNV;                     // lane >> kSh = value index after reduce
-    static_assert(NV <= kMaxVals && R <= kMaxBatch, "batch too large");
-
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                       // [kMaxStages]
-    int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + 64);
-    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + kSmemMetaOff);      // [S][R]
-    float *red = reinterpret_cast<float *>(smem + kSmemRedOff);                // [2][16][NV]
-    uint8_t *stages = smem + kSmemStageOff;                                    // [S][T][R][slice]
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const uint32_t rank = (K > 1) ? cluster_rank() : 0u;
-    const int H = p.hidden;
-    const int V = H >> 3;
-    const int Vc = V / K;                                // vectors per CTA
-    const bool has_vec = tid < Vc;
-    const int W = nwarps * K;                            // warps in the team
-    const uint32_t slice_bytes = uint32_t(Vc) * 16u;
-    const int64_t col0 = int64_t(rank) * Vc * 8;        // first column of this CTA
-    const int64_t my_col = col0 + int64_t(tid) * 8;     // first column of this thread
-    const float Hf = float(H);
-
-    // Work units: plan items (64 slots) for the dweight modes; single R-row
-    // batches otherwise (a batch of a plan item, or R consecutive physical rows).
-    const bool item_units = p.use_plan && T::kLeaves;
-    const int64_t cluster_id = blockIdx.x / K;
-    const int64_t n_clusters = gridDim.x / K;
-    const int64_t my_units = p.n_units > cluster_id ? (p.n_units - cluster_id + n_clusters - 1) / n_clusters : 0;
-    const int64_t per_unit = item_units ? kNB : 1;
-    const int64_t n_batches = my_units * per_unit;
-
-    auto stage_ptr = [&](int s, int t, int r) -> uint8_t * {
-        return stages + ((int64_t(s) * T::kTensors + t) * R + r) * slice_bytes;
-    };
-
-    // ---- producer (thread 0): metadata of batch k, loaded one batch ahead
-    auto load_meta = [&](int64_t k, SlotBatch<R> &mb) {
-        if (k >= n_batches) return;
-        if (p.use_plan) {
-            int64_t item;
-            int sub;
-            if (item_units) {
-                item = cluster_id + (k / kNB) * n_clusters;
-                sub = int(k % kNB);
-            } else {
-                const int64_t gb = cluster_id + k * n_clusters;
-                item = gb / kNB;
-                sub = int(gb % kNB);
-            }
-            const PlanItem *it = p.items + item;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                mb.prow[r] = it->prow[sub * R + r];
-                mb.lrow[r] = it->lrow[sub * R + r];
-            }
-        } else {
-            const int64_t gb = cluster_id + k * n_clusters;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int64_t row = gb * R + r;
-                int32_t id = -1;
-                if (row < p.n_rows) id = p.tok_id[row / p.rpt];
-                mb.prow[r] = id >= 0 ? int32_t(row) : -1;
-                mb.lrow[r] = -1;
-            }
-        }
-    };
-    auto issue = [&](int64_t k, const SlotBatch<R> &mb) {
-        if (k >= n_batches) return;
-        const int s = int(k % S);
-        StageMeta *m = meta + s * R;
-        uint32_t n_act = 0;
-        int64_t offs[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int32_t pr = mb.prow[r], lr = mb.lrow[r];
-            bool act = pr >= 0;
-            if (act && (pr >= p.n_rows || (T::kLeaves && (lr < 0 || lr >= p.ws.n_rows)))) {
-                if (T::kLeaves) set_status(p.ws.hdr, kStPlan);
-                act = false;
-            }
-            offs[r] = act ? row_offset(p, pr) + col0 : -1;
-            m[r].off = offs[r];
-            m[r].lrow = lr;
-            m[r].prow = pr;
-            n_act += act ? 1u : 0u;
-        }
-        mbar_arrive_expect_tx(&bars[s], n_act * slice_bytes * T::kTensors);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (offs[r] < 0) continue;
-            bulk_copy_g2s(stage_ptr(s, 0, r), p.x + offs[r], slice_bytes, &bars[s]);
-            if (T::kNeedDy) bulk_copy_g2s(stage_ptr(s, 1, r), p.dy + offs[r], slice_bytes, &bars[s]);
-        }
-    };
-
-    SlotBatch<R> next_meta;
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (K > 1) cluster_barrier(); else __syncthreads();
-    if (tid == 0) {
-        SlotBatch<R> mb;
-        for (int64_t k = 0; k < S - 1; ++k) {
-            load_meta(k, mb);
-            issue(k, mb);
-        }
-        load_meta(S - 1, next_meta);
-    }
-
-    float2 wv[4];
-    if (MODE != kDw && has_vec) unpack8x2(*reinterpret_cast<const uint4 *>(p.w + my_col), wv);
-
-    TreeStack2<4> tree;                 // levels >= log2(R): partials of the current block
-    int32_t kind = 0, block = -1;
-
-#pragma unroll 1
-    for (int64_t k = 0; k < n_batches; ++k) {
-        const int s = int(k % S);
-        const uint32_t parity = uint32_t((k / S) & 1);
-        const int sub = int(k % per_unit);
-        if (item_units && sub == 0) {
-            const PlanItem *it = p.items + (cluster_id + (k / kNB) * n_clusters);
-            kind = it->kind;
-            block = it->block;
-            if ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1)) {
-                if (tid == 0 && rank == 0) set_status(p.ws.hdr, kStPlan);
-                kind = 2;                                  // malformed item: contributes nothing
-            }
-        }
-        if (!mbar_wait_bounded(&bars[s], parity)) {
-            *abort_flag = 1;
-            if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
-        }
-        const StageMeta *m = meta + s * R;
-
-        // ---- per-thread partial row sums, then the warp transpose-reduce
-        float val[NV];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float a = 0.f, b = 0.f;
-            if (m[r].off >= 0 && has_vec) {
-                float2 xf[4];
-                unpack8x2(ld_shared_v4(stage_ptr(s, 0, r) + tid * 16), xf);
-                a = dot8x2(xf, xf);
-                if (T::kNeedGx) {
-                    float2 df[4], gf[4];
-                    unpack8x2(ld_shared_v4(stage_ptr(s, 1, r) + tid * 16), df);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) gf[i] = mul2(df[i], wv[i]);
-                    b = dot8x2(gf, xf);
-                }
-            }
-            val[r] = a;
-            if (T::kNeedGx) val[R + r] = b;
-        }
-        const float wsum = warp_transpose_reduce<NV>(val, lane);
-        float *rb = red + (k & 1) * (16 * kMaxVals);     // [16 local warps][NV] per parity
-        if ((lane & ((1 << kSh) - 1)) == 0) rb[warp * kMaxVals + (lane >> kSh)] = wsum;
-        if (K > 1) cluster_barrier(); else __syncthreads();
-        {
-            int ab = *abort_flag;
-            if (K > 1) {
-#pragma unroll
-                for (int q = 0; q < K; ++q)
-                    ab |= __float_as_int(ld_cluster_f32(map_to_rank(smem_addr(abort_flag), uint32_t(q))));
-            }
-            if (ab) {
-                // give copies still in flight into our stages a bounded time to land
-                if (tid == 0)
-                    for (int64_t kk = k + 1; kk < k + S - 1 && kk < n_batches; ++kk)
-                        mbar_wait_bounded(&bars[kk % S], uint32_t((kk / S) & 1));
-                break;
-            }
-        }
-        if (tid == 0) {
-            SlotBatch<R> cur = next_meta;
-            issue(k + S - 1, cur);
-            load_meta(k + S, next_meta);
-        }
-
-        // ---- team sums: lane w takes warp w (+ warp w+32), then the same
-        // transpose-reduce over the 32 slots; every warp does it redundantly.
-        {
-            float tv[NV];
-#pragma unroll
-            for (int j = 0; j < NV; ++j) tv[j] = 0.f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int w = lane + 32 * half;
-                if (w < W) {
-                    const int cta = w / nwarps, lw = w - cta * nwarps;
-                    const float *src = rb + lw * kMaxVals;
-#pragma unroll
-                    for (int j = 0; j < NV; ++j) {
-                        float v;
-                        if (K == 1) v = src[j];
-                        else v = ld_cluster_f32(map_to_rank(smem_addr(src + j), uint32_t(cta)));
-                        tv[j] = half ? __fadd_rn(tv[j], v) : v;
-                    }
-                }
-            }
-            const float tsum = warp_transpose_reduce<NV>(tv, lane);
-            // lane l now holds team sum j = l >> kSh: ss_j (j < R) or gx_{j-R}
-            const int j = lane >> kSh;
-            const float rs = row_rstd(tsum, Hf, p.eps);               // meaningful for j < R
-            if (T::kNeedGx) {
-                const int src_lane = (j >= R ? j - R : j) << kSh;
-                const float rs_row = __shfl_sync(kFull, rs, src_lane);
-                const float mg = row_mean_gxhat(tsum, rs_row, Hf);    // meaningful for j >= R
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    val[r] = __shfl_sync(kFull, rs, r << kSh);
-                    val[R + r] = __shfl_sync(kFull, mg, (R + r) << kSh);
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < R; ++r) val[r] = __shfl_sync(kFull, rs, r << kSh);
-            }
-        }
-
-        // ---- outputs and dweight leaves
-        TreeStack2<4, (kLogR > 0 ? kLogR : 1)> mini;   // levels < log2(R): the batch's own subtree
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const bool act = m[r].off >= 0;
-            const float rstd = val[r];
-            float2 leaf[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) leaf[i] = make_float2(0.f, 0.f);
-            if (act && has_vec) {
-                const float2 r2 = make_float2(rstd, rstd);
-                float2 xf[4], xh[4], o[4];
-                unpack8x2(ld_shared_v4(stage_ptr(s, 0, r) + tid * 16), xf);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) xh[i] = mul2(xf[i], r2);
-                if (MODE == kFwd) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) o[i] = mul2(xh[i], wv[i]);
-                    st_global_v4(p.out + m[r].off + tid * 8, pack8x2(o));
-                } else {
-                    float2 df[4];
-                    unpack8x2(ld_shared_v4(stage_ptr(s, 1, r) + tid * 16), df);
-                    if (T::kNeedGx && p.out != nullptr) {
-                        const float nm = -val[R + r];
-                        const float2 nm2 = make_float2(nm, nm);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) o[i] = mul2(r2, fma2(xh[i], nm2, mul2(df[i], wv[i])));
-                        st_global_v4(p.out + m[r].off + tid * 8, pack8x2(o));
-                    }
-                    if (T::kLeaves) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) leaf[i] = mul2(df[i], xh[i]);
-                    }
-                }
-            }
-            if (MODE == kFwd && act && p.rstd_out != nullptr && tid == 0 && rank == 0)
-                p.rstd_out[m[r].prow] = rstd;
-            if (T::kLeaves) {
-                if (kind == 0) {
-                    if (R > 1) mini.template push_static<0>(leaf, r);
-                    if (r == R - 1) {
-                        tree.template push_dyn<kLogR>(leaf, sub);
-                        if (sub == kNB - 1) {             // leaf[] is the block partial
-                            if (has_vec) {
-                                float *dst = p.ws.block_partial + int64_t(block) * 4 * H + my_col;
-                                st_global_f32x4(dst, leaf[0].x, leaf[0].y, leaf[1].x, leaf[1].y);
-                                st_global_f32x4(dst + 4, leaf[2].x, leaf[2].y, leaf[3].x, leaf[3].y);
-                            }
-                            if (tid == 0 && rank == 0) mark_whole_block(p.ws, block);
-                        }
-                    }
-                } else if (kind == 1 && act) {
-                    if (has_vec) {
-                        float *dst = p.ws.spill + int64_t(m[r].lrow) * H + my_col;
-                        st_global_f32x4(dst, leaf[0].x, leaf[0].y, leaf[1].x, leaf[1].y);
-                        st_global_f32x4(dst + 4, leaf[2].x, leaf[2].y, leaf[3].x, leaf[3].y);
-                    }
-                    if (tid == 0 && rank == 0) mark_spilled_row(p.ws, m[r].lrow);
-                }
-            }
-        }
-    }
-    if (K > 1) cluster_barrier();      // peers may still read our partials
-}
+constexpr int kMaxBatch = 8;                     // rows per pipeline stage <= 8
 
 // =====================================================================
-// Hidden sizes 264..5120: warp-specialised pipeline in one CTA
+// Hidden sizes above 256: warp-specialised pipeline, one CTA or a K-CTA cluster per row
 // =====================================================================
 //
-// Warps [0, NC): column warps; thread t owns columns 8t..8t+7 of every row.
-// Warps [NC, NC+NS): stats warps; warp i handles the stages s with s % NS == i.
-// Warp NC+NS: producer; lane 0 issues the bulk copies.
-//
+// A row team is K CTAs (a thread-block cluster when K > 1); CTA q owns the
+// columns [q*H/K, (q+1)*H/K).  In each CTA:
+//   warps [0, NC): column warps; thread t owns columns 8t..8t+7 of the slice;
+//   warps [NC, NC+NS): stats warps; warp i handles the stages s with s % NS == i;
+//   warp NC+NS: producer; lane 0 issues the bulk copies of the CTA's slice.
 // Per stage s (R rows of x, dy): full[s] completes when the copies land,
-// stats[s] when a stats warp has published rstd and mean(g*xhat) for its
-// rows, empty[s] when every column warp is done with it.  No CTA-wide
-// barrier is used after set-up.  Rows of the dweight modes are processed in
-// 16-row units (a quarter of a logical block): the column warps reduce the
-// unit's 16 leaves with the 64-leaf tree's lower four levels and store the
-// quarter partial; dweight_finalize adds the four quarters (levels 5, 6).
+// stats[s] when the stats warp has published rstd and mean(g*xhat) of its
+// rows, empty[s] when every column warp is done with it.  With K > 1 the
+// stats warps exchange their slice partials through distributed shared
+// memory: each stores its partials into every CTA of the cluster and arrives
+// on that CTA's xchg[s] barrier, then waits for all K arrivals on its own.
+// No CTA-wide barrier is used after set-up.  Rows of the dweight modes are
+// processed in 16-row units (a quarter of a logical block): the column warps
+// reduce the unit's 16 leaves with the 64-leaf tree's lower four levels and
+// store the quarter partial; dweight_finalize adds the four quarters.
 //
-// Row sums (this family's canonical tree, which depends on H only): lane l
-// folds vectors l, l+32, l+64, ... in order, columns interleaved as two FMA
-// chains (columns 0,2,4,6 and 1,3,5,7 of each vector, one chain across all
-// of the lane's vectors), the chains are added, and the 32 lane sums are
-// added by a complete tree pairing lanes 16 apart first, then 8, 4, 2, 1.
+// Row sums (this family's canonical tree, which depends on H only): in each
+// slice, lane l folds vectors l, l+32, l+64, ... in order, columns
+// interleaved as two FMA chains (columns 0,2,4,6 and 1,3,5,7 of each vector,
+// one chain across all of the lane's vectors), the chains are added, and the
+// 32 lane sums are added by a complete tree pairing lanes 16 apart first, then
+// 8, 4, 2, 1.  The K slice sums are then added in order: p0 + p1 for K = 2,
+// (p0 + p1) + (p2 + p3) for K = 4.
 
 constexpr int kSplitMaxStages = 12;
 constexpr int kSplitUnitRows = 16;
+constexpr int kSplitMaxK = 4;
 
 struct SplitStats {
     float rstd;
     float mg;
 };
 
-constexpr int kSplitItemOff = 320;                                   // [kSplitMaxStages] int2 item headers
-constexpr int kSplitMetaOff = 512;                                   // after 3 x 12 barriers (288 B) + flag
+constexpr int kSplitFlagOff = 384;                                   // after 4 x 12 barriers (384 B)
+constexpr int kSplitItemOff = 400;                                   // [kSplitMaxStages] int2 item headers
+constexpr int kSplitMetaOff = 512;
 constexpr int kSplitStatsOff = kSplitMetaOff + kSplitMaxStages * kMaxBatch * 16;
-constexpr int kSplitWOff = kSplitStatsOff + kSplitMaxStages * kMaxBatch * 8;   // FP32 weight [H]
-__host__ __device__ constexpr int split_stage_off(int H) { return ((kSplitWOff + H * 4) + 127) / 128 * 128; }
+constexpr int kSplitXbufOff = kSplitStatsOff + kSplitMaxStages * kMaxBatch * 8;   // [S][2][K][R] float2
+constexpr int kSplitWOff = kSplitXbufOff + kSplitMaxStages * 2 * kSplitMaxK * kMaxBatch * 8;
+__host__ __device__ constexpr int split_stage_off(int slice_cols) {
+    return ((kSplitWOff + slice_cols * 4) + 127) / 128 * 128;
+}
 
-template <int MODE, int R, int MAXT, int NS>
+template <int MODE, int R, int MAXT, int NS, int K>
 __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const int S, const int NC) {
     using T = ModeTraits<MODE>;
     constexpr int kLogR = (R == 1) ? 0 : (R == 2) ? 1 : (R == 4) ? 2 : 3;
@@ -480,24 +182,31 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *stats_bar = full + kSplitMaxStages;
     uint64_t *empty = stats_bar + kSplitMaxStages;
-    volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + 3 * kSplitMaxStages * 8);
-    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + kSplitMetaOff);   // [S][R]
+    uint64_t *xchg = empty + kSplitMaxStages;
+    volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + kSplitFlagOff);
     int2 *item_hdr = reinterpret_cast<int2 *>(smem + kSplitItemOff);          // [S] (kind, block)
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + kSplitMetaOff);   // [S][R]
     SplitStats *stats = reinterpret_cast<SplitStats *>(smem + kSplitStatsOff);
+    float2 *xbuf = reinterpret_cast<float2 *>(smem + kSplitXbufOff);          // [S][2][K][R]
     float *wsm = reinterpret_cast<float *>(smem + kSplitWOff);
     const int H = p.hidden;
-    const int V = H >> 3;
-    uint8_t *stages = smem + split_stage_off(H);
-    const uint32_t row_bytes = uint32_t(H) * 2u;
+    const int HS = H / K;                                 // columns of this CTA's slice
+    const int VS = HS >> 3;                               // vectors of the slice
+    uint8_t *stages = smem + split_stage_off(HS);
+    const uint32_t row_bytes = uint32_t(HS) * 2u;
     auto stage_ptr = [&](int s, int t, int r) -> uint8_t * {
         return stages + ((int64_t(s) * T::kTensors + t) * R + r) * row_bytes;
     };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = (K > 1) ? cluster_rank() : 0u;
+    const int64_t col0 = int64_t(rank) * HS;
     const float Hf = float(H);
     const bool item_units = p.use_plan && T::kLeaves;
     const int64_t per_unit = item_units ? kUnitBatches : 1;
-    const int64_t my_units = p.n_units > blockIdx.x ? (p.n_units - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int64_t cluster_id = blockIdx.x / K;
+    const int64_t n_clusters = gridDim.x / K;
+    const int64_t my_units = p.n_units > cluster_id ? (p.n_units - cluster_id + n_clusters - 1) / n_clusters : 0;
     const int n_batches = int(my_units * per_unit);      // < 2^31: units are bounded by rows / 2
 
     if (tid == 0) {
@@ -505,28 +214,29 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
             mbar_init(&full[s], 1);
             mbar_init(&stats_bar[s], 1);
             mbar_init(&empty[s], NC);
+            mbar_init(&xchg[s], K);
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (MODE != kDw && T::kNeedGx) {
-        for (int i = tid; i < H; i += blockDim.x) wsm[i] = __uint_as_float(uint32_t(p.w[i]) << 16);
+        for (int i = tid; i < HS; i += blockDim.x) wsm[i] = __uint_as_float(uint32_t(p.w[col0 + i]) << 16);
     }
-    __syncthreads();
+    if (K > 1) cluster_barrier(); else __syncthreads();
 
-    // batch k of this CTA -> (plan item, slot base) or physical row base
+    // batch k of this team -> (plan item, slot base) or physical batch index
     auto batch_slots = [&](int k, int64_t &item, int &slot0) {
         if (item_units) {
-            const int64_t u = blockIdx.x + (k / kUnitBatches) * gridDim.x;      // quarter unit
+            const int64_t u = cluster_id + (k / kUnitBatches) * n_clusters;   // quarter unit
             item = u >> 2;
             slot0 = int(u & 3) * kSplitUnitRows + int(k % kUnitBatches) * R;
         } else {
-            const int64_t gb = blockIdx.x + k * gridDim.x;
+            const int64_t gb = cluster_id + int64_t(k) * n_clusters;
             if (p.use_plan) {
                 item = gb / (kBlockRows / R);
                 slot0 = int(gb % (kBlockRows / R)) * R;
             } else {
-                item = gb;                                                     // physical batch index
+                item = gb;
                 slot0 = 0;
             }
         }
@@ -601,7 +311,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     const int32_t pr = cur.prow[r], lr = cur.lrow[r];
                     bool act = pr >= 0;
                     if (act && (pr >= p.n_rows || (T::kLeaves && (lr < 0 || lr >= p.ws.n_rows)))) {
-                        if (T::kLeaves) set_status(p.ws.hdr, kStPlan);
+                        if (T::kLeaves && rank == 0) set_status(p.ws.hdr, kStPlan);
                         act = false;
                     }
                     offs[r] = act ? row_offset(p, pr) : -1;
@@ -614,8 +324,8 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (offs[r] < 0) continue;
-                    bulk_copy_g2s(stage_ptr(s, 0, r), p.x + offs[r], row_bytes, &full[s]);
-                    if (T::kNeedDy) bulk_copy_g2s(stage_ptr(s, 1, r), p.dy + offs[r], row_bytes, &full[s]);
+                    bulk_copy_g2s(stage_ptr(s, 0, r), p.x + offs[r] + col0, row_bytes, &full[s]);
+                    if (T::kNeedDy) bulk_copy_g2s(stage_ptr(s, 1, r), p.dy + offs[r] + col0, row_bytes, &full[s]);
                 }
                 if (++s == S) {
                     s = 0;
@@ -623,10 +333,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                 }
             }
         }
-        return;
-    }
-
-    if (warp >= NC) {
+    } else if (warp >= NC) {
         // ------------------------------------------------ stats warps
         const int si = warp - NC;
         int s = 0;
@@ -648,7 +355,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     const uint8_t *xr = stage_ptr(s, 0, r);
                     const uint8_t *dr = stage_ptr(s, 1, r);
 #pragma unroll 4
-                    for (int v = lane; v < V; v += 32) {
+                    for (int v = lane; v < VS; v += 32) {
                         f2_t xf[4];
                         f2_unpack8(ld_shared_v4(xr + v * 16), xf);
 #pragma unroll
@@ -671,6 +378,34 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
 #pragma unroll
                 for (int j = 0; j < (T::kNeedGx ? 2 * R : R); ++j)
                     vals[j] = __fadd_rn(vals[j], __shfl_xor_sync(kFull, vals[j], d));
+            if (K > 1) {
+                // send this slice's partials to every CTA of the cluster
+                float2 *xb = xbuf + ((s * 2 + int(ph)) * K) * R;   // [K][R] for this use of stage s
+                if (lane < K) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        st_cluster_f32x2(map_to_rank(smem_addr(xb + rank * R + r), uint32_t(lane)), vals[r], vals[R + r]);
+                    mbar_arrive_remote(map_to_rank(smem_addr(&xchg[s]), uint32_t(lane)));
+                }
+                if (!mbar_wait_bounded_cluster(&xchg[s], ph)) {
+                    *abort_flag = 1;
+                    if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
+                    break;
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float2 q[kSplitMaxK];
+#pragma unroll
+                    for (int c = 0; c < K; ++c) q[c] = xb[c * R + r];
+                    if (K == 2) {
+                        vals[r] = __fadd_rn(q[0].x, q[1].x);
+                        vals[R + r] = __fadd_rn(q[0].y, q[1].y);
+                    } else {
+                        vals[r] = __fadd_rn(__fadd_rn(q[0].x, q[1].x), __fadd_rn(q[2].x, q[3].x));
+                        vals[R + r] = __fadd_rn(__fadd_rn(q[0].y, q[1].y), __fadd_rn(q[2].y, q[3].y));
+                    }
+                }
+            }
             if (lane < R) {
                 float ss = vals[0], gx = vals[R];
 #pragma unroll
@@ -684,118 +419,127 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                 st.rstd = rstd;
                 st.mg = T::kNeedGx ? row_mean_gxhat(gx, rstd, Hf) : 0.f;
                 stats[s * R + lane] = st;
-                if (MODE == kFwd && p.rstd_out != nullptr && m[lane].off >= 0) p.rstd_out[m[lane].prow] = rstd;
+                if (MODE == kFwd && rank == 0 && p.rstd_out != nullptr && m[lane].off >= 0)
+                    p.rstd_out[m[lane].prow] = rstd;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&stats_bar[s]);
         }
-        return;
-    }
-
-    // ---------------------------------------------------- column warps
-    const int t = tid;                                   // vector owned: columns 8t..8t+7
-    const bool has_vec = t < V;
-    f2_t wv[4];
-    if (MODE != kDw && has_vec) f2_unpack8(*reinterpret_cast<const uint4 *>(p.w + t * 8), wv);
-    TreeStackF2<4, 4> tree;            // levels log2(R)..3 of the 16-leaf unit
-    int32_t kind = 0, block = -1, quarter = 0;
-    int s = 0, sub = 0;
-    uint32_t parity = 0;
-    int64_t u = blockIdx.x;                               // current quarter unit
-    for (int k = 0; k < n_batches; ++k) {
-        if (k > 0) {
-            if (++s == S) {
-                s = 0;
-                parity ^= 1u;
-            }
-            if (++sub == per_unit) {
-                sub = 0;
-                u += gridDim.x;
-            }
-        }
-        if (*abort_flag) break;
-        if (!mbar_wait_bounded(&stats_bar[s], parity) || !mbar_wait_bounded(&full[s], parity)) {
-            *abort_flag = 1;
-            if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
-            break;
-        }
-        if (item_units && sub == 0) {                    // item header, staged by the producer
-            const int2 hd = item_hdr[s];
-            quarter = int(u & 3);
-            kind = hd.x;
-            block = hd.y;
-            if ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1)) {
-                if (t == 0) set_status(p.ws.hdr, kStPlan);
-                kind = 2;
-            }
-        }
-        const StageMeta *m = meta + s * R;
-        TreeStackF2<4, (kLogR > 0 ? kLogR : 1)> mini;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int64_t off = m[r].off;
-            const bool act = off >= 0;
-            f2_t leaf[4] = {0ull, 0ull, 0ull, 0ull};
-            if (act && has_vec) {
-                const SplitStats st = stats[s * R + r];
-                const f2_t r2 = f2_make(st.rstd, st.rstd);
-                f2_t xf[4], xh[4], o[4];
-                f2_unpack8(ld_shared_v4(stage_ptr(s, 0, r) + t * 16), xf);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) xh[i] = f2_mul(xf[i], r2);
-                if (MODE == kFwd) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) o[i] = f2_mul(xh[i], wv[i]);
-                    st_global_v4(p.out + off + t * 8, f2_pack8(o));
-                } else {
-                    f2_t df[4];
-                    f2_unpack8(ld_shared_v4(stage_ptr(s, 1, r) + t * 16), df);
-                    if (T::kNeedGx && p.out != nullptr) {
-                        const f2_t nm2 = f2_make(-st.mg, -st.mg);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) o[i] = f2_mul(r2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
-                        st_global_v4(p.out + off + t * 8, f2_pack8(o));
-                    }
-                    if (T::kLeaves) {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) leaf[i] = f2_mul(df[i], xh[i]);
-                    }
+    } else {
+        // ------------------------------------------------ column warps
+        const int t = tid;                                   // vector owned: slice columns 8t..8t+7
+        const bool has_vec = t < VS;
+        const int64_t my_col = col0 + int64_t(t) * 8;
+        f2_t wv[4];
+        if (MODE != kDw && has_vec) f2_unpack8(*reinterpret_cast<const uint4 *>(p.w + my_col), wv);
+        TreeStackF2<4, 4> tree;            // levels log2(R)..3 of the 16-leaf unit
+        int32_t kind = 0, block = -1, quarter = 0;
+        int s = 0, sub = 0;
+        uint32_t parity = 0;
+        int64_t u = cluster_id;                               // current quarter unit
+        for (int k = 0; k < n_batches; ++k) {
+            if (k > 0) {
+                if (++s == S) {
+                    s = 0;
+                    parity ^= 1u;
+                }
+                if (++sub == per_unit) {
+                    sub = 0;
+                    u += n_clusters;
                 }
             }
-            if (T::kLeaves) {
-                if (kind == 0) {
-                    if (R > 1) mini.template push_static<0>(leaf, r);
-                    if (r == R - 1) {
-                        tree.template push_dyn<kLogR>(leaf, sub);
-                        if (sub == kUnitBatches - 1) {           // leaf[] is the quarter partial
-                            if (has_vec)
-                                st_global_f2x4(p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + t * 8, leaf);
-                            if (t == 0) mark_quarter(p.ws, block, quarter);
+            if (*abort_flag) break;
+            if (!mbar_wait_bounded(&stats_bar[s], parity) || !mbar_wait_bounded(&full[s], parity)) {
+                *abort_flag = 1;
+                if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
+                break;
+            }
+            if (item_units && sub == 0) {                    // item header, staged by the producer
+                const int2 hd = item_hdr[s];
+                quarter = int(u & 3);
+                kind = hd.x;
+                block = hd.y;
+                if ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1)) {
+                    if (t == 0 && rank == 0) set_status(p.ws.hdr, kStPlan);
+                    kind = 2;
+                }
+            }
+            const StageMeta *m = meta + s * R;
+            TreeStackF2<4, (kLogR > 0 ? kLogR : 1)> mini;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int64_t off = m[r].off;
+                const bool act = off >= 0;
+                f2_t leaf[4] = {0ull, 0ull, 0ull, 0ull};
+                if (act && has_vec) {
+                    const SplitStats st = stats[s * R + r];
+                    const f2_t r2 = f2_make(st.rstd, st.rstd);
+                    f2_t xf[4], xh[4], o[4];
+                    f2_unpack8(ld_shared_v4(stage_ptr(s, 0, r) + t * 16), xf);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) xh[i] = f2_mul(xf[i], r2);
+                    if (MODE == kFwd) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) o[i] = f2_mul(xh[i], wv[i]);
+                        st_global_v4(p.out + off + my_col, f2_pack8(o));
+                    } else {
+                        f2_t df[4];
+                        f2_unpack8(ld_shared_v4(stage_ptr(s, 1, r) + t * 16), df);
+                        if (T::kNeedGx && p.out != nullptr) {
+                            const f2_t nm2 = f2_make(-st.mg, -st.mg);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) o[i] = f2_mul(r2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
+                            st_global_v4(p.out + off + my_col, f2_pack8(o));
+                        }
+                        if (T::kLeaves) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) leaf[i] = f2_mul(df[i], xh[i]);
                         }
                     }
-                } else if (kind == 1 && act) {
-                    if (has_vec) st_global_f2x4(p.ws.spill + int64_t(m[r].lrow) * H + t * 8, leaf);
-                    if (t == 0) mark_spilled_row(p.ws, m[r].lrow);
+                }
+                if (T::kLeaves) {
+                    if (kind == 0) {
+                        if (R > 1) mini.template push_static<0>(leaf, r);
+                        if (r == R - 1) {
+                            tree.template push_dyn<kLogR>(leaf, sub);
+                            if (sub == kUnitBatches - 1) {           // leaf[] is the quarter partial
+                                if (has_vec)
+                                    st_global_f2x4(p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + my_col, leaf);
+                                if (t == 0 && rank == 0) mark_quarter(p.ws, block, quarter);
+                            }
+                        }
+                    } else if (kind == 1 && act) {
+                        if (has_vec) st_global_f2x4(p.ws.spill + int64_t(m[r].lrow) * H + my_col, leaf);
+                        if (t == 0 && rank == 0) mark_spilled_row(p.ws, m[r].lrow);
+                    }
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
     }
+    if (K > 1) cluster_barrier();      // peers may still store into our exchange buffers
 }
 
-// =====================================================================
-// Small hidden sizes: team = P2 lanes of a warp, register-direct loads
-// =====================================================================
+__device__ __forceinline__ f2_t shfl_xor_f2(f2_t v, int k) {
+    return (f2_t(__shfl_xor_sync(kFull, uint32_t(v >> 32), k)) << 32) | __shfl_xor_sync(kFull, uint32_t(v), k);
+}
 
+constexpr int kSmallWarps = 8;                          // warps per CTA
+
+// Small hidden sizes: each warp works through its units in groups of U warp
+// steps; the 16-byte loads of a group are issued together into registers, then
+// the U steps are computed as independent chains (so they overlap).  The slot
+// metadata of a unit is fetched once by the whole warp (lane l holds slots
+// 2l, 2l+1) and handed out by shuffles.
 template <int MODE, int P2, int U>
-__global__ void __launch_bounds__(256) small_row_kernel(const KParams p) {
+__global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KParams p) {
     using T = ModeTraits<MODE>;
     constexpr int TPW = 32 / P2;                         // teams (rows) per warp step
     constexpr int kSteps = kBlockRows / TPW;             // steps per 64-slot unit
     constexpr int kLogTPW = (TPW == 1) ? 0 : (TPW == 2) ? 1 : (TPW == 4) ? 2 : (TPW == 8) ? 3 : (TPW == 16) ? 4 : 5;
-    static_assert(kSteps % U == 0 || U >= kSteps, "steps per unit must be a multiple of U");
     constexpr int kU = U < kSteps ? U : kSteps;
+    static_assert(kSteps % kU == 0, "steps per unit must be a multiple of the prefetch depth");
 
     const int lane = threadIdx.x & 31;
     const int team = lane / P2, tl = lane % P2;
@@ -805,39 +549,41 @@ __global__ void __launch_bounds__(256) small_row_kernel(const KParams p) {
     const int64_t gwarp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
 
-    float wv[8];
-    if (MODE != kDw && has_vec) unpack8(*reinterpret_cast<const uint4 *>(p.w + tl * 8), wv);
+    f2_t wv[4] = {0ull, 0ull, 0ull, 0ull};
+    if (MODE != kDw && has_vec) f2_unpack8(*reinterpret_cast<const uint4 *>(p.w + tl * 8), wv);
 
 #pragma unroll 1
     for (int64_t u = gwarp; u < p.n_units; u += nwarps) {
-        const PlanItem *it = p.use_plan ? p.items + u : nullptr;
+        int2 pr2 = make_int2(-1, -1), lr2 = make_int2(-1, -1);
         int32_t kind = 0, block = -1;
-        if (it) {
+        if (p.use_plan) {
+            const PlanItem *it = p.items + u;
+            pr2 = reinterpret_cast<const int2 *>(it->prow)[lane];
+            lr2 = reinterpret_cast<const int2 *>(it->lrow)[lane];
             kind = it->kind;
             block = it->block;
             if (T::kLeaves && ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1))) {
                 if (lane == 0) set_status(p.ws.hdr, kStPlan);
                 kind = 2;                                  // malformed item: contributes nothing
             }
+        } else {
+            const int64_t r0 = u * kBlockRows + 2 * lane;
+            if (r0 < p.n_rows && p.tok_id[r0 / p.rpt] >= 0) pr2.x = int32_t(r0);
+            if (r0 + 1 < p.n_rows && p.tok_id[(r0 + 1) / p.rpt] >= 0) pr2.y = int32_t(r0 + 1);
         }
-        TreeStack<8> tree;
+        TreeStackF2<4, kBlockLevels> tree;
 #pragma unroll 1
         for (int st0 = 0; st0 < kSteps; st0 += kU) {
-            // resolve slots and issue loads for kU steps
             int64_t off[kU];
             int32_t lrow[kU], prow[kU];
             uint4 xv[kU], dv[kU];
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
                 const int slot = (st0 + q) * TPW + team;
-                int32_t pr, lr = -1;
-                if (it) {
-                    pr = it->prow[slot];
-                    lr = it->lrow[slot];
-                } else {
-                    const int64_t row = u * kBlockRows + slot;
-                    pr = (row < p.n_rows && p.tok_id[row / p.rpt] >= 0) ? int32_t(row) : -1;
-                }
+                const int px = __shfl_sync(kFull, pr2.x, slot >> 1), py = __shfl_sync(kFull, pr2.y, slot >> 1);
+                const int lx = __shfl_sync(kFull, lr2.x, slot >> 1), ly = __shfl_sync(kFull, lr2.y, slot >> 1);
+                int32_t pr = (slot & 1) ? py : px;
+                const int32_t lr = (slot & 1) ? ly : lx;
                 bool act = pr >= 0;
                 if (act && (pr >= p.n_rows || (T::kLeaves && (lr < 0 || lr >= p.ws.n_rows)))) {
                     if (T::kLeaves && tl == 0) set_status(p.ws.hdr, kStPlan);
@@ -856,70 +602,63 @@ __global__ void __launch_bounds__(256) small_row_kernel(const KParams p) {
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
                 const bool act = off[q] >= 0;
-                float xf[8], df[8];
-                unpack8(xv[q], xf);
-                unpack8(dv[q], df);
-                float ss = 0.f, gx = 0.f;
-                if (act && has_vec) {
-                    ss = dot8(xf, xf);
-                    if (T::kNeedGx) {
-                        float gf[8];
+                f2_t xf[4], df[4];
+                f2_unpack8(xv[q], xf);
+                f2_unpack8(dv[q], df);
+                // row sums: two FMA chains (even / odd columns), then the team butterfly
+                f2_t a2 = 0ull, b2 = 0ull;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) gf[i] = __fmul_rn(df[i], wv[i]);
-                        gx = dot8(gf, xf);
-                    }
+                for (int i = 0; i < 4; ++i) a2 = f2_fma(xf[i], xf[i], a2);
+                float ss = __fadd_rn(f2_lo(a2), f2_hi(a2));
+                float gx = 0.f;
+                if (T::kNeedGx) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) b2 = f2_fma(f2_mul(df[i], wv[i]), xf[i], b2);
+                    gx = __fadd_rn(f2_lo(b2), f2_hi(b2));
                 }
                 ss = lane_tree(ss, P2);
                 if (T::kNeedGx) gx = lane_tree(gx, P2);
                 const float rstd = row_rstd(ss, Hf, p.eps);
-                float leaf[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) leaf[i] = 0.f;
+                f2_t leaf[4] = {0ull, 0ull, 0ull, 0ull};
                 if (act && has_vec) {
-                    float xh[8], o[8];
+                    const f2_t r2 = f2_make(rstd, rstd);
+                    f2_t xh[4], o[4];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) xh[i] = __fmul_rn(xf[i], rstd);
+                    for (int i = 0; i < 4; ++i) xh[i] = f2_mul(xf[i], r2);
                     if (MODE == kFwd) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) o[i] = __fmul_rn(xh[i], wv[i]);
-                        st_global_v4(p.out + off[q], pack8(o));
+                        for (int i = 0; i < 4; ++i) o[i] = f2_mul(xh[i], wv[i]);
+                        st_global_v4(p.out + off[q], f2_pack8(o));
                     } else {
                         if (T::kNeedGx && p.out != nullptr) {
                             const float mg = row_mean_gxhat(gx, rstd, Hf);
+                            const f2_t nm2 = f2_make(-mg, -mg);
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const float g = __fmul_rn(df[i], wv[i]);
-                                o[i] = __fmul_rn(rstd, __fmaf_rn(-xh[i], mg, g));
-                            }
-                            st_global_v4(p.out + off[q], pack8(o));
+                            for (int i = 0; i < 4; ++i) o[i] = f2_mul(r2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
+                            st_global_v4(p.out + off[q], f2_pack8(o));
                         }
                         if (T::kLeaves) {
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) leaf[i] = __fmul_rn(df[i], xh[i]);
+                            for (int i = 0; i < 4; ++i) leaf[i] = f2_mul(df[i], xh[i]);
                         }
                     }
                 }
                 if (MODE == kFwd && act && p.rstd_out != nullptr && tl == 0) p.rstd_out[prow[q]] = rstd;
                 if (T::kLeaves) {
                     if (kind == 0) {
-                        // combine the TPW rows of this step (adjacent teams first)
+                        // the TPW rows of this step: adjacent teams first
 #pragma unroll
                         for (int kk = P2; kk < 32; kk <<= 1)
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) leaf[i] = __fadd_rn(leaf[i], __shfl_xor_sync(kFull, leaf[i], kk));
-                        tree.push(leaf, st0 + q, kLogTPW);
-                        if (st0 + q == kSteps - 1 && team == 0 && has_vec) {
-                            float *dst = p.ws.block_partial + int64_t(block) * 4 * H + tl * 8;
-                            st_global_f32x4(dst, leaf[0], leaf[1], leaf[2], leaf[3]);
-                            st_global_f32x4(dst + 4, leaf[4], leaf[5], leaf[6], leaf[7]);
+                            for (int i = 0; i < 4; ++i) leaf[i] = f2_add(leaf[i], shfl_xor_f2(leaf[i], kk));
+                        tree.template push_dyn<kLogTPW>(leaf, st0 + q);
+                        if (st0 + q == kSteps - 1) {
+                            if (team == 0 && has_vec)
+                                st_global_f2x4(p.ws.block_partial + int64_t(block) * 4 * H + tl * 8, leaf);
+                            if (lane == 0) mark_whole_block(p.ws, block);
                         }
-                        if (st0 + q == kSteps - 1 && lane == 0) mark_whole_block(p.ws, block);
                     } else if (kind == 1 && act) {
-                        if (has_vec) {
-                            float *dst = p.ws.spill + int64_t(lrow[q]) * H + tl * 8;
-                            st_global_f32x4(dst, leaf[0], leaf[1], leaf[2], leaf[3]);
-                            st_global_f32x4(dst + 4, leaf[4], leaf[5], leaf[6], leaf[7]);
-                        }
+                        if (has_vec) st_global_f2x4(p.ws.spill + int64_t(lrow[q]) * H + tl * 8, leaf);
                         if (tl == 0) mark_spilled_row(p.ws, lrow[q]);
                     }
                 }
