@@ -161,6 +161,29 @@ int rmsnorm_dweight_begin(void *workspace, size_t bytes, int64_t n_logical_rows,
 int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t hidden, float *dweight,
                      rmsnorm_stream_t stream);
 
+/*
+ * Sharded finalize (several ranks, one logical multiset).  The block partials
+ * of the dweight tree are split into aligned power-of-two ranges: a range of
+ * block_count = 2^k blocks starting at block_lo (a multiple of block_count)
+ * is one node of the pairwise tree with odd carry, and
+ * dweight_finalize_range writes that node's value (FP32 [hidden]) to `root`.
+ * The last range may stop at the block count.  Splitting the blocks into
+ * consecutive ranges of one common block_count, gathering their nodes from all
+ * ranks in block order (root j = range [j*block_count, ...)) and reducing them
+ * with dweight_combine (the same carry tree over n_roots partials,
+ * 1 <= n_roots < 2048) gives dweight bitwise equal to a single
+ * dweight_finalize of all blocks.  A rank may keep its rows in a workspace of
+ * its own, numbered from its first range (local row = global row - 64 *
+ * block_lo of that range); dweight_finalize_range then takes local block
+ * numbers.  `roots` is FP32 [n_roots][hidden], device memory, read only.
+ * Errors: RMSNORM_ERR_LAYOUT for a range that is not such a node or a bad
+ * n_roots; the usual workspace, null, alignment and hidden-size errors.
+ */
+int dweight_finalize_range(void *workspace, int64_t n_logical_rows, int64_t hidden, int64_t block_lo,
+                           int64_t block_count, float *root, rmsnorm_stream_t stream);
+int dweight_combine(const float *roots, int64_t n_roots, int64_t hidden, float *dweight,
+                    rmsnorm_stream_t stream);
+
 /* Synchronises `stream` and copies the workspace's status word to *status. */
 int rmsnorm_dweight_status(const void *workspace, rmsnorm_stream_t stream, int32_t *status);
 

@@ -70,6 +70,8 @@ def _load():
         "rmsnorm_dweight_workspace_bytes": ([I64, I64], ctypes.c_size_t),
         "rmsnorm_dweight_begin": ([P, ctypes.c_size_t, I64, I64, P], ctypes.c_int),
         "dweight_finalize": ([P, I64, I64, P, P], ctypes.c_int),
+        "dweight_finalize_range": ([P, I64, I64, I64, I64, P, P], ctypes.c_int),
+        "dweight_combine": ([P, I64, I64, P, P], ctypes.c_int),
         "rmsnorm_dweight_status": ([P, P, ctypes.POINTER(I32)], ctypes.c_int),
         "rmsnorm_plan_bytes": ([I64, I32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
         "rmsnorm_plan_build": ([P, I64, I32, I64, P, ctypes.c_size_t, ctypes.POINTER(I64),
@@ -232,6 +234,17 @@ class DweightWorkspace:
                                         _stream(stream)), "dweight_finalize")
         return dweight
 
+    def finalize_range(self, block_lo: int, block_count: int, root=None, stream=None):
+        """Node of the dweight tree over blocks [block_lo, block_lo + block_count)
+        of this workspace (block_count a power of two, block_lo a multiple of it)."""
+        import torch
+        if root is None:
+            root = torch.empty(self.hidden, dtype=torch.float32, device=self.buf.device)
+        _check(_load().dweight_finalize_range(_ptr(self.buf), self.n_rows, self.hidden, int(block_lo),
+                                              int(block_count), _ptr(root), _stream(stream)),
+               "dweight_finalize_range")
+        return root
+
     def status(self, stream=None) -> int:
         out = ctypes.c_int32(0)
         _check(_load().rmsnorm_dweight_status(_ptr(self.buf), _stream(stream), ctypes.byref(out)),
@@ -241,6 +254,17 @@ class DweightWorkspace:
 
 def dweight_finalize(workspace: DweightWorkspace, dweight=None, stream=None):
     return workspace.finalize(dweight, stream)
+
+
+def dweight_combine(roots, dweight=None, stream=None):
+    """Carry tree over FP32 roots [n, H] (device), the top of the dweight tree."""
+    import torch
+    n, H = roots.shape
+    assert roots.is_contiguous() and roots.dtype == torch.float32
+    if dweight is None:
+        dweight = torch.empty(H, dtype=torch.float32, device=roots.device)
+    _check(_load().dweight_combine(_ptr(roots), n, H, _ptr(dweight), _stream(stream)), "dweight_combine")
+    return dweight
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -325,6 +325,32 @@ extern "C" int rmsnorm_dweight_begin(void *workspace, size_t bytes, int64_t n_lo
     return RMSNORM_OK;
 }
 
+namespace {
+// Tree passes over blocks [lo, lo + count) of the workspace, leaving one value in out.
+int finalize_blocks(const WsView &ws, int64_t lo, int64_t count, float *out, cudaStream_t s) {
+    const int V = int(ws.hidden / 8);
+    const unsigned gy = unsigned((V + kTreeVecs - 1) / kTreeVecs);
+    int64_t n = count;
+    const float *in = nullptr;
+    bool first = true;
+    int flip = 0;
+    while (true) {
+        const int64_t groups = (n + 31) / 32;
+        float *dst = groups == 1 ? out : (flip ? ws.scratch_b : ws.scratch_a);
+        tree_pass_kernel<<<dim3(unsigned(groups), gy), kTreeWarps * 32, 0, s>>>(ws, in, dst, n, first ? 1 : 0,
+                                                                                first ? lo : 0);
+        if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (groups == 1) break;
+        in = dst;
+        n = groups;
+        first = false;
+        flip ^= 1;
+    }
+    return RMSNORM_OK;
+}
+}  // namespace
+
 extern "C" int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t hidden, float *dweight,
                                 rmsnorm_stream_t stream) {
     int rc = ws_checks(workspace, n_logical_rows, hidden);
@@ -335,33 +361,47 @@ extern "C" int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t
     if ((rc = device_info(&d))) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     WsView ws = ws_view(workspace, n_logical_rows, hidden);
-    const int V = int(hidden / 8);
-    const unsigned gy = unsigned((V + kTreeWarps - 1) / kTreeWarps);
     if (ws.n_blocks == 0) {
         zero_f32_kernel<<<1, 256, 0, s>>>(dweight, hidden);
         if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
         g_launches.fetch_add(1, std::memory_order_relaxed);
         return RMSNORM_OK;
     }
-    // pass 1 forms the block partials and reduces groups of 32; later passes
-    // reduce groups of 32 group results, ping-ponging between the scratch
-    // areas; the pass that leaves one value writes dweight.
-    int64_t n = ws.n_blocks;
-    const float *in = nullptr;
-    bool first = true;
-    int flip = 0;
-    while (true) {
-        const int64_t groups = (n + 31) / 32;
-        float *out = groups == 1 ? dweight : (flip ? ws.scratch_b : ws.scratch_a);
-        tree_pass_kernel<<<dim3(unsigned(groups), gy), kTreeWarps * 32, 0, s>>>(ws, in, out, n, first ? 1 : 0);
-        if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
-        g_launches.fetch_add(1, std::memory_order_relaxed);
-        if (groups == 1) break;
-        in = out;
-        n = groups;
-        first = false;
-        flip ^= 1;
-    }
+    return finalize_blocks(ws, 0, ws.n_blocks, dweight, s);
+}
+
+extern "C" int dweight_finalize_range(void *workspace, int64_t n_logical_rows, int64_t hidden, int64_t block_lo,
+                                      int64_t block_count, float *root, rmsnorm_stream_t stream) {
+    int rc = ws_checks(workspace, n_logical_rows, hidden);
+    if (rc) return rc;
+    if (!root) return RMSNORM_ERR_NULL;
+    if (!aligned16(root)) return RMSNORM_ERR_ALIGN;
+    const int64_t nb = (n_logical_rows + kBlockRows - 1) / kBlockRows;
+    if (block_count < 1 || (block_count & (block_count - 1)) != 0 || block_lo < 0 || block_lo % block_count != 0 ||
+        block_lo >= nb)
+        return RMSNORM_ERR_LAYOUT;
+    DeviceInfo *d = nullptr;
+    if ((rc = device_info(&d))) return rc;
+    const int64_t count = block_lo + block_count > nb ? nb - block_lo : block_count;
+    return finalize_blocks(ws_view(workspace, n_logical_rows, hidden), block_lo, count, root,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int dweight_combine(const float *roots, int64_t n_roots, int64_t hidden, float *dweight,
+                               rmsnorm_stream_t stream) {
+    Shape sh;
+    if (!hidden_shape(hidden, &sh)) return RMSNORM_ERR_HIDDEN;
+    if (!roots || !dweight) return RMSNORM_ERR_NULL;
+    if (!aligned16(roots) || !aligned16(dweight)) return RMSNORM_ERR_ALIGN;
+    if (n_roots < 1 || n_roots >= 2048) return RMSNORM_ERR_LAYOUT;
+    DeviceInfo *d = nullptr;
+    int rc = device_info(&d);
+    if (rc) return rc;
+    const int V = int(hidden / 8);
+    combine_kernel<<<unsigned((V + 127) / 128), 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        roots, n_roots, int(hidden), dweight);
+    if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return RMSNORM_OK;
 }
 

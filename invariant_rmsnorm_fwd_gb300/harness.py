@@ -38,6 +38,10 @@ class LayoutRun:
 
 @dataclass
 class Diff:
+    """Drift of one tensor of one layout against the reference layout: bitwise
+    verdict plus the attribution metrics max / mean / p99 of |difference| and
+    the first mismatching logical row ("Phase 4: single-card operator
+    comparisons and drift attribution", Scope)."""
     tensor: str
     layout: str
     reference: str
@@ -46,6 +50,8 @@ class Diff:
     max_abs: float
     max_rel: float
     first_logical_index: int
+    mean_abs: float = 0.0
+    p99_abs: float = 0.0
 
 
 @dataclass
@@ -97,8 +103,11 @@ def bitwise_diff(name: str, a, b, layout: str, reference: str) -> Diff:
     rel = d / fb.abs().clamp_min(1e-30)
     first = int(torch.nonzero(neq)[0].item())
     row_len = a.reshape(a.shape[0], -1).shape[1] if a.dim() > 1 else 1
+    finite = d[torch.isfinite(d)].double()
+    mean = float(finite.mean().item()) if finite.numel() else float("inf")
+    p99 = float(torch.quantile(finite[:1 << 24], 0.99).item()) if finite.numel() else float("inf")
     return Diff(name, layout, reference, False, n, float(d.max().item()), float(rel.max().item()),
-                first // row_len)
+                first // row_len, mean, p99)
 
 
 def layouts_differ(ref: layout_mod.Layout, other: layout_mod.Layout) -> bool:

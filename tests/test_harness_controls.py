@@ -93,3 +93,18 @@ def test_nonzero_status_is_red():
     runs = {k: _run(k, tree_replay.dweight(leaves)) for k in lays}
     runs["chunked"].status = 2
     assert not harness.assert_batch_invariant(runs, lays).green
+
+
+def test_drift_attribution_metrics():
+    a = torch.tensor([[1.0, 2.0, 3.0, 4.0], [5.0, 6.0, 7.0, 8.0]])
+    b = a.clone()
+    b[1, 2] = 7.5                                          # one element of logical row 1 drifts by 0.5
+    d = harness.bitwise_diff("dweight", a, b, "chunked", "full")
+    assert not d.equal and d.mismatches == 1 and d.first_logical_index == 1
+    assert d.max_abs == 0.5 and abs(d.mean_abs - 0.5 / 8) < 1e-12
+    assert 0.0 <= d.p99_abs <= 0.5
+    same = harness.bitwise_diff("dweight", a, a.clone(), "chunked", "full")
+    assert same.equal and same.mismatches == 0 and same.max_abs == 0.0
+    # bit patterns decide: -0.0 differs from +0.0
+    z = harness.bitwise_diff("dweight", torch.tensor([-0.0]), torch.tensor([0.0]), "x", "y")
+    assert not z.equal and z.max_abs == 0.0
