@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
+    ap.add_argument("--chain", action="store_true",
+                    help="residual add + norm forward and its backward with the residual gradient and the "
+                         "loss seed's 1/D (D = active tokens of the multiset); no e2e or CPU legs")
     return ap.parse_args()
 
 
@@ -175,30 +178,64 @@ class L2Flush:
         torch.amax(self.r, dim=0, out=self.sink)
 
 
-class Step:
-    """Device-resident buffers of one layout and the launch sequence of one step."""
+class Call:
+    """Physical buffers of one call: x, dy, y, dx (and r, dres, h for the chain)."""
 
-    def __init__(self, wl, lay, x_log, dy_log, w, rpt, device):
+    def __init__(self, cl, xp, dp, yp, dxp, rp=None, drp=None, hp=None):
+        self.cl, self.xp, self.dp, self.yp, self.dxp = cl, xp, dp, yp, dxp
+        self.rp, self.drp, self.hp = rp, drp, hp
+
+
+class Step:
+    """Device-resident buffers of one layout and the launch sequence of one step.
+    With `chain`, the step is the residual add + norm forward and the backward
+    with the residual gradient, scaled by the loss seed's 1/D."""
+
+    def __init__(self, wl, lay, x_log, dy_log, w, rpt, device, r_log=None, dres_log=None):
         import torch
         import invariant_rmsnorm_fwd_gb300 as rb
         self.rb = rb
         H = wl.hidden
         self.H, self.rpt, self.eps = H, rpt, wl.eps
         self.w = w
+        self.chain = r_log is not None
+        self.scale = 1.0 / wl.n_tokens if self.chain else None
         self.calls = []
         for tok in lay.calls:
             cl = rb.call_layout(tok, rpt, lay.n_logical_tokens, device=device)
             tid = cl.tok_id.long()
             act = tid >= 0
-            xp = torch.zeros((tok.size, rpt, H), dtype=torch.bfloat16, device=device)
-            dp = torch.zeros_like(xp)
-            xp[act] = x_log[tid[act]]
-            dp[act] = dy_log[tid[act]]
-            self.calls.append((cl, xp, dp, torch.empty_like(xp), torch.empty_like(xp)))
+
+            def place(src):
+                t = torch.zeros((tok.size, rpt, H), dtype=torch.bfloat16, device=device)
+                t[act] = src[tid[act]]
+                return t
+            xp, dp = place(x_log), place(dy_log)
+            if self.chain:
+                self.calls.append(Call(cl, xp, dp, torch.empty_like(xp), torch.empty_like(xp), place(r_log),
+                                       place(dres_log), torch.empty_like(xp)))
+            else:
+                self.calls.append(Call(cl, xp, dp, torch.empty_like(xp), torch.empty_like(xp)))
         self.ws = rb.DweightWorkspace(wl.n_tokens * rpt, H, device=device)
         self.dw = torch.empty(H, dtype=torch.float32, device=device)
         self.n_active = wl.n_tokens
         self.bwd_events = []
+
+    def fwd_call(self, c, st):
+        if self.chain:
+            self.rb.rmsnorm_add_fwd(c.xp, c.rp, self.w, c.cl, self.eps, h=c.hp, y=c.yp, stream=st)
+        else:
+            self.rb.rmsnorm_fwd(c.xp, self.w, c.cl, self.eps, y=c.yp, stream=st)
+
+    def bwd_call(self, c, st):
+        if self.chain:
+            self.rb.rmsnorm_add_bwd(c.hp, self.w, c.dp, c.cl, self.eps, dres=c.drp, grad_scale=self.scale,
+                                    dx=c.dxp, workspace=self.ws, stream=st)
+        else:
+            self.rb.rmsnorm_bwd_dx(c.xp, self.w, c.dp, c.cl, self.eps, dx=c.dxp, workspace=self.ws, stream=st)
+
+    def finalize(self, st):
+        self.ws.finalize(self.dw, st, grad_scale=self.scale)
 
     def run(self, stream):
         """Calls of a multi-call layout are independent (they touch disjoint rows and
@@ -225,11 +262,10 @@ class Step:
                 e.record(st)
                 stream.wait_event(e)
 
-        fan(lambda c, st: rb.rmsnorm_fwd(c[1], self.w, c[0], self.eps, y=c[3], stream=st))
+        fan(self.fwd_call)
         self.ws.begin(stream)
-        fan(lambda c, st: rb.rmsnorm_bwd_dx(c[1], self.w, c[2], c[0], self.eps, dx=c[4], workspace=self.ws,
-                                            stream=st))
-        self.ws.finalize(self.dw, stream)
+        fan(self.bwd_call)
+        self.finalize(stream)
 
     def _lanes(self, stream):
         import torch
@@ -243,8 +279,8 @@ class Step:
         import torch
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for cl, xp, dp, yp, dxp in self.calls:
-            self.rb.rmsnorm_fwd(xp, self.w, cl, self.eps, y=yp, stream=stream)
+        for c in self.calls:
+            self.fwd_call(c, stream)
         e1.record(stream)
         return e0, e1
 
@@ -252,12 +288,15 @@ class Step:
         import torch
         y = torch.empty((n_tok, self.rpt, self.H), dtype=torch.bfloat16, device=self.dw.device)
         dx = torch.empty_like(y)
-        for cl, xp, dp, yp, dxp in self.calls:
-            tid = cl.tok_id.long()
+        h = torch.empty_like(y) if self.chain else None
+        for c in self.calls:
+            tid = c.cl.tok_id.long()
             act = tid >= 0
-            y[tid[act]] = yp[act]
-            dx[tid[act]] = dxp[act]
-        return y, dx, self.dw.clone()
+            y[tid[act]] = c.yp[act]
+            dx[tid[act]] = c.dxp[act]
+            if self.chain:
+                h[tid[act]] = c.hp[act]
+        return (y, dx, self.dw.clone()) + ((h,) if self.chain else ())
 
 
 def time_steps(step, stream, steps, warmup, flush, dist=None, graph=True):
@@ -304,14 +343,14 @@ def time_bwd_kernel(step_objs, stream, reps, flush):
     for _ in range(reps):
         for so in step_objs:
             so.ws.begin(stream)
-            for cl, xp, dp, yp, dxp in so.calls:
+            for c in so.calls:
                 flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                so.rb.rmsnorm_bwd_dx(xp, so.w, dp, cl, so.eps, dx=dxp, workspace=so.ws, stream=stream)
+                so.bwd_call(c, stream)
                 e1.record(stream)
                 per.append((e0, e1))
-            so.ws.finalize(so.dw, stream)
+            so.finalize(stream)
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in per]
 
@@ -436,11 +475,19 @@ def main():
         x = synth.logical_tensor(wl, synth.TAG_X, n_rows, wl.x_std, hs, device=device).reshape(wl.n_tokens, rpt, wl.hidden)
         dy = synth.logical_tensor(wl, synth.TAG_DY, n_rows, wl.dy_std, hs, device=device).reshape(wl.n_tokens, rpt, wl.hidden)
         w = synth.weight(wl, hs, device=device)
-        steps_data.append((rpt, x, dy, w))
+        extra = ()
+        if args.chain:
+            r = synth.logical_tensor(wl, synth.TAG_RES, n_rows, wl.x_std, hs, device=device)
+            dres = synth.logical_tensor(wl, synth.TAG_DRES, n_rows, wl.dy_std, hs, device=device)
+            extra = (r.reshape(wl.n_tokens, rpt, wl.hidden), dres.reshape(wl.n_tokens, rpt, wl.hidden))
+        steps_data.append((rpt, x, dy, w) + extra)
+
+    def make_steps(layout_):
+        return [Step(wl, layout_, d[1], d[2], d[3], d[0], device, *d[4:]) for d in steps_data]
 
     lays = L.workload_layouts(wl, kinds=[lay_name])
     lay = lays[lay_name]
-    step_objs = [Step(wl, lay, x, dy, w, rpt, device) for rpt, x, dy, w in steps_data]
+    step_objs = make_steps(lay)
 
     class Multi:
         def __init__(self, steps):
@@ -481,10 +528,13 @@ def main():
     H = wl.hidden
     heff = H * sum(rpt_list)
     n_act = wl.n_tokens
-    alg_step = 10.0 * heff * n_act                  # bytes: fwd x+y, bwd x+dy+dx (bf16)
+    # algorithmic bytes per token and width: fwd x+y, bwd x+dy+dx (bf16); the chain adds
+    # r and h to the forward and dres to the backward
+    fwd_b, bwd_b = (8.0, 8.0) if args.chain else (4.0, 6.0)
+    alg_step = (fwd_b + bwd_b) * heff * n_act
     bwd_calls = len(lay.calls) * len(rpt_list)
     bwd_per_launch_ms = statistics.mean(bwd_ms) if bwd_ms else float("nan")
-    alg_bwd_launch = 6.0 * heff * n_act / bwd_calls
+    alg_bwd_launch = bwd_b * heff * n_act / bwd_calls
     achieved_bwd = alg_bwd_launch / (bwd_per_launch_ms * 1e-3) / 1e9
     tokens_per_s = n_act / (ms_step * 1e-3) * world
 
@@ -495,7 +545,7 @@ def main():
         evs = [s.time_fwd_only(stream) for s in step_objs]
         torch.cuda.synchronize()
         fwd_ms.append(sum(a.elapsed_time(b) for a, b in evs))
-    fwd_gbs = 4.0 * heff * n_act / (statistics.mean(fwd_ms) * 1e-3) / 1e9
+    fwd_gbs = fwd_b * heff * n_act / (statistics.mean(fwd_ms) * 1e-3) / 1e9
 
     line = {
         "metric": METRIC,
@@ -519,10 +569,13 @@ def main():
         "hbm_gbs_step": round(alg_step / (ms_step * 1e-3) / 1e9, 1),
         "frac_step": round(alg_step / (ms_step * 1e-3) / 1e9 / hbm_peak, 4),
         "fwd_gbs": round(fwd_gbs, 1),
-        "roofline": {"bound": "hbm", "kernel": "fused backward (dx + dweight leaves), rmsnorm_bwd_dx",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("residual-add backward (dh + dweight leaves), rmsnorm_add_bwd" if args.chain
+                                else "fused backward (dx + dweight leaves), rmsnorm_bwd_dx"),
                      "achieved": round(achieved_bwd, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved_bwd / hbm_peak, 4),
-                     "traffic": (recorded_traffic(args.config, lay_name) if bwd_calls == 1 else None),
+                     "traffic": (recorded_traffic(args.config, lay_name) if bwd_calls == 1 and not args.chain
+                                 else None),
                      "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": alg_bwd_launch,
                      "launch_ms": round(bwd_per_launch_ms, 5)},
@@ -536,7 +589,7 @@ def main():
         ref_out = None
         bitwise = True
         for k, v in L.workload_layouts(wl).items():
-            so = [Step(wl, v, x, dy, w, rpt, device) for rpt, x, dy, w in steps_data]
+            so = make_steps(v)
             m = Multi(so)
             t, _ = time_steps(m, stream, max(3, args.steps // 2), 2, flush, graph=not args.no_graph)
             per[k] = {"ms": round(statistics.mean(t), 4), "calls": len(v.calls),
@@ -552,7 +605,10 @@ def main():
         line["layouts"] = per
         line["bitwise_across_layouts"] = bool(bitwise)
 
-    if rank == 0 and not args.no_e2e:
+    if args.chain:
+        line["config"]["chain"] = ("h = bf16(x + r), y = RMSNorm(h); dh = bf16(dx/D + dres), dweight/D; "
+                                   "D = active tokens of the multiset")
+    if rank == 0 and not args.no_e2e and not args.chain:
         x_h = [d[1].cpu() for d in steps_data]
         dy_h = [d[2].cpu() for d in steps_data]
         tot_ms, tot_in, tot_out = 0.0, 0, 0
@@ -565,8 +621,8 @@ def main():
                        "h2d_bytes_per_step": int(tot_in), "d2h_bytes_per_step": int(tot_out),
                        "ms_per_step": round(tot_ms, 3)}
 
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rpt, x, dy, w = steps_data[0]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.chain:
+        rpt, x, dy, w = steps_data[0][:4]
         n_cpu = min(x.shape[0], 4096)
         line["cpu_baseline"] = cpu_baseline(wl, x[:n_cpu].cpu(), dy[:n_cpu].cpu(), w.cpu(), rpt,
                                             args.cpu_seconds)

@@ -71,7 +71,8 @@ enum {
     RMSNORM_ERR_DUPLICATE = -9,   /* plan build: a logical token appears twice in one call */
     RMSNORM_ERR_CAPACITY = -10,   /* plan build: output buffer too small */
     RMSNORM_ERR_CUDA = -11,       /* a CUDA runtime call or kernel launch failed */
-    RMSNORM_ERR_DEVICE = -12      /* the current device is not sm_103 */
+    RMSNORM_ERR_DEVICE = -12,     /* the current device is not sm_103 */
+    RMSNORM_ERR_VALUE = -13       /* grad_scale is NaN or infinite */
 };
 
 /* Device status word bits (rmsnorm_dweight_status). */
@@ -135,6 +136,42 @@ int rmsnorm_bwd_dweight_contrib(const uint16_t *x, const uint16_t *dy, int64_t h
                                 rmsnorm_stream_t stream);
 
 /*
+ * The op's neighbours in a chain ("[WS1 Closeout][Backward] ..." issue #270,
+ * "Scope": the upstream gradient, the loss reduction and the active-token
+ * denominator are fixed across configurations; "WS1 C4 (#270) closeout
+ * evidence", "Acceptance map": the harness injects the active-token
+ * denominator and seeds the backward with an upstream that is a function of
+ * logical identity only).  Neither call has a counterpart kernel in the
+ * pages; both keep every output a function of the row and of fixed trees.
+ *
+ * rmsnorm_add_fwd: residual add fused with the norm.  h = bf16(x + residual)
+ * (one round-to-nearest-even of the exact sum) is written to h_out, and
+ * y = RMSNorm(h) * w exactly as rmsnorm_fwd would compute it from h.  x,
+ * residual, h_out and y share the layout (token_stride); h_out may alias x or
+ * residual, y may alias x or residual, h_out != y.  rstd as in rmsnorm_fwd.
+ *
+ * rmsnorm_add_bwd: backward of y = RMSNorm(h) * w when h also feeds the
+ * residual path.  x is the saved h.  With dx_n = rstd * (dy*w - xhat *
+ * mean(dy*w*xhat)) it writes dx = bf16(fl(grad_scale * rstd) * (...) + dres)
+ * in FP32 with one final rounding; dres (the gradient reaching h along the
+ * residual path) may be NULL (then dx = bf16(grad_scale * dx_n)).
+ * grad_scale is the loss seed's factor, 1/D for a mean over the multiset's D
+ * active tokens (the same D for every call of every layout), 1 for a sum.
+ * The dweight contribution (workspace non-NULL) stays c = dy * xhat,
+ * unscaled: the factor is applied once, to the root, by
+ * dweight_finalize_scaled / dweight_combine.  grad_scale = 1 and dres = NULL
+ * give exactly rmsnorm_bwd_dx.  dx may be NULL only with a workspace and no
+ * dres.  Errors: RMSNORM_ERR_VALUE for a non-finite grad_scale, otherwise as
+ * rmsnorm_bwd_dx.
+ */
+int rmsnorm_add_fwd(const uint16_t *x, const uint16_t *residual, const uint16_t *weight, int64_t hidden,
+                    float eps, const rmsnorm_layout_t *layout, uint16_t *h_out, uint16_t *y, float *rstd,
+                    rmsnorm_stream_t stream);
+int rmsnorm_add_bwd(const uint16_t *x, const uint16_t *weight, const uint16_t *dy, const uint16_t *dres,
+                    int64_t hidden, float eps, float grad_scale, const rmsnorm_layout_t *layout,
+                    uint16_t *dx, void *workspace, rmsnorm_stream_t stream);
+
+/*
  * Workspace for one dweight reduction over n_logical_rows = n_logical_tokens
  * * rows_per_token rows of width hidden: a header with the status word,
  * per-block and per-row flags, the block partials, finalize scratch, and a
@@ -161,6 +198,12 @@ int rmsnorm_dweight_begin(void *workspace, size_t bytes, int64_t n_logical_rows,
 int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t hidden, float *dweight,
                      rmsnorm_stream_t stream);
 
+/* dweight_finalize with the root multiplied once by grad_scale (FP32,
+ * round-to-nearest); grad_scale = 1 is exactly dweight_finalize.
+ * RMSNORM_ERR_VALUE for a non-finite grad_scale. */
+int dweight_finalize_scaled(void *workspace, int64_t n_logical_rows, int64_t hidden, float grad_scale,
+                            float *dweight, rmsnorm_stream_t stream);
+
 /*
  * Sharded finalize (several ranks, one logical multiset).  The block partials
  * of the dweight tree are split into aligned power-of-two ranges: a range of
@@ -171,8 +214,9 @@ int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t hidden, fl
  * consecutive ranges of one common block_count, gathering their nodes from all
  * ranks in block order (root j = range [j*block_count, ...)) and reducing them
  * with dweight_combine (the same carry tree over n_roots partials,
- * 1 <= n_roots < 2048) gives dweight bitwise equal to a single
- * dweight_finalize of all blocks.  A rank may keep its rows in a workspace of
+ * 1 <= n_roots < 2048, the root then multiplied by grad_scale as in
+ * dweight_finalize_scaled) gives dweight bitwise equal to a single
+ * dweight_finalize_scaled of all blocks.  A rank may keep its rows in a workspace of
  * its own, numbered from its first range (local row = global row - 64 *
  * block_lo of that range); dweight_finalize_range then takes local block
  * numbers.  `roots` is FP32 [n_roots][hidden], device memory, read only.
@@ -181,7 +225,7 @@ int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t hidden, fl
  */
 int dweight_finalize_range(void *workspace, int64_t n_logical_rows, int64_t hidden, int64_t block_lo,
                            int64_t block_count, float *root, rmsnorm_stream_t stream);
-int dweight_combine(const float *roots, int64_t n_roots, int64_t hidden, float *dweight,
+int dweight_combine(const float *roots, int64_t n_roots, int64_t hidden, float grad_scale, float *dweight,
                     rmsnorm_stream_t stream);
 
 /* Synchronises `stream` and copies the workspace's status word to *status. */

@@ -22,7 +22,7 @@ _lib = None
 OK = 0
 ERR_NAMES = {
     -1: "NULL", -2: "HIDDEN", -3: "ALIGN", -4: "STRIDE", -5: "LAYOUT", -6: "WORKSPACE",
-    -7: "PLAN", -8: "ID", -9: "DUPLICATE", -10: "CAPACITY", -11: "CUDA", -12: "DEVICE",
+    -7: "PLAN", -8: "ID", -9: "DUPLICATE", -10: "CAPACITY", -11: "CUDA", -12: "DEVICE", -13: "VALUE",
 }
 STATUS_DOUBLE, STATUS_MISSING, STATUS_HEADER, STATUS_PLAN, STATUS_TIMEOUT = 1, 2, 4, 8, 16
 PLAN_ITEM_BYTES = 528
@@ -71,7 +71,10 @@ def _load():
         "rmsnorm_dweight_begin": ([P, ctypes.c_size_t, I64, I64, P], ctypes.c_int),
         "dweight_finalize": ([P, I64, I64, P, P], ctypes.c_int),
         "dweight_finalize_range": ([P, I64, I64, I64, I64, P, P], ctypes.c_int),
-        "dweight_combine": ([P, I64, I64, P, P], ctypes.c_int),
+        "dweight_finalize_scaled": ([P, I64, I64, F, P, P], ctypes.c_int),
+        "dweight_combine": ([P, I64, I64, F, P, P], ctypes.c_int),
+        "rmsnorm_add_fwd": ([P, P, P, I64, F, LP, P, P, P, P], ctypes.c_int),
+        "rmsnorm_add_bwd": ([P, P, P, P, I64, F, F, LP, P, P, P], ctypes.c_int),
         "rmsnorm_dweight_status": ([P, P, ctypes.POINTER(I32)], ctypes.c_int),
         "rmsnorm_plan_bytes": ([I64, I32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
         "rmsnorm_plan_build": ([P, I64, I32, I64, P, ctypes.c_size_t, ctypes.POINTER(I64),
@@ -201,6 +204,42 @@ def rmsnorm_bwd_dx(x, weight, dy, lay: CallLayout, eps: float, dx=None, workspac
     return dx
 
 
+def rmsnorm_add_fwd(x, residual, weight, lay: CallLayout, eps: float, h=None, y=None, rstd=None, stream=None):
+    """Residual add fused with the norm: h = bf16(x + residual), y = RMSNorm(h) * w."""
+    import torch
+    H = weight.shape[0]
+    if h is None:
+        h = torch.empty_like(x)
+    if y is None:
+        y = torch.empty_like(x)
+    stride = _rows_view(x, lay.rows_per_token, H)
+    for t in (residual, h, y):
+        assert _rows_view(t, lay.rows_per_token, H) == stride
+    L = lay.struct(stride)
+    _check(_load().rmsnorm_add_fwd(_ptr(x), _ptr(residual), _ptr(weight), H, eps, ctypes.byref(L), _ptr(h),
+                                   _ptr(y), _ptr(rstd), _stream(stream)), "rmsnorm_add_fwd")
+    return h, y
+
+
+def rmsnorm_add_bwd(x, weight, dy, lay: CallLayout, eps: float, dres=None, grad_scale: float = 1.0, dx=None,
+                    workspace=None, stream=None):
+    """dx = bf16(grad_scale * (norm backward) + dres); x is the saved h.  The
+    dweight contribution to `workspace` stays unscaled (scale it at finalize)."""
+    import torch
+    H = weight.shape[0]
+    if dx is None:
+        dx = torch.empty_like(dy)
+    stride = _rows_view(x, lay.rows_per_token, H)
+    for t in (dy, dx) + (() if dres is None else (dres,)):
+        assert _rows_view(t, lay.rows_per_token, H) == stride
+    L = lay.struct(stride)
+    _check(_load().rmsnorm_add_bwd(_ptr(x), _ptr(weight), _ptr(dy), _ptr(dres), H, eps, float(grad_scale),
+                                   ctypes.byref(L), _ptr(dx),
+                                   None if workspace is None else _ptr(workspace.buf), _stream(stream)),
+           "rmsnorm_add_bwd")
+    return dx
+
+
 def rmsnorm_bwd_dweight_contrib(x, dy, hidden: int, lay: CallLayout, eps: float, workspace, stream=None):
     stride = _rows_view(x, lay.rows_per_token, hidden)
     L = lay.struct(stride)
@@ -226,12 +265,17 @@ class DweightWorkspace:
         _check(_load().rmsnorm_dweight_begin(_ptr(self.buf), self.bytes, self.n_rows, self.hidden,
                                              _stream(stream)), "rmsnorm_dweight_begin")
 
-    def finalize(self, dweight=None, stream=None):
+    def finalize(self, dweight=None, stream=None, grad_scale=None):
+        """dweight of the reduction; with grad_scale the root is multiplied by it once."""
         import torch
         if dweight is None:
             dweight = torch.empty(self.hidden, dtype=torch.float32, device=self.buf.device)
-        _check(_load().dweight_finalize(_ptr(self.buf), self.n_rows, self.hidden, _ptr(dweight),
-                                        _stream(stream)), "dweight_finalize")
+        if grad_scale is None:
+            _check(_load().dweight_finalize(_ptr(self.buf), self.n_rows, self.hidden, _ptr(dweight),
+                                            _stream(stream)), "dweight_finalize")
+        else:
+            _check(_load().dweight_finalize_scaled(_ptr(self.buf), self.n_rows, self.hidden, float(grad_scale),
+                                                   _ptr(dweight), _stream(stream)), "dweight_finalize_scaled")
         return dweight
 
     def finalize_range(self, block_lo: int, block_count: int, root=None, stream=None):
@@ -256,14 +300,16 @@ def dweight_finalize(workspace: DweightWorkspace, dweight=None, stream=None):
     return workspace.finalize(dweight, stream)
 
 
-def dweight_combine(roots, dweight=None, stream=None):
-    """Carry tree over FP32 roots [n, H] (device), the top of the dweight tree."""
+def dweight_combine(roots, dweight=None, stream=None, grad_scale: float = 1.0):
+    """Carry tree over FP32 roots [n, H] (device), the top of the dweight tree,
+    the result multiplied once by grad_scale."""
     import torch
     n, H = roots.shape
     assert roots.is_contiguous() and roots.dtype == torch.float32
     if dweight is None:
         dweight = torch.empty(H, dtype=torch.float32, device=roots.device)
-    _check(_load().dweight_combine(_ptr(roots), n, H, _ptr(dweight), _stream(stream)), "dweight_combine")
+    _check(_load().dweight_combine(_ptr(roots), n, H, float(grad_scale), _ptr(dweight), _stream(stream)),
+           "dweight_combine")
     return dweight
 
 

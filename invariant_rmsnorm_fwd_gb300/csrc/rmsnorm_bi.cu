@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "rmsnorm_bi.h"
@@ -160,7 +161,9 @@ int launch_split(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStr
 
 template <int MODE, int P2>
 int launch_small(const KParams &p, const DeviceInfo &d, cudaStream_t stream) {
-    constexpr int U = ModeTraits<MODE>::kLeaves ? 4 : 8;   // warp steps loaded together
+    // warp steps loaded together (fewer when three tensors or the leaf tree hold registers)
+    using T = ModeTraits<MODE>;
+    constexpr int U = (T::kLeaves && T::kTensors >= 3) ? 2 : (T::kLeaves || T::kTensors >= 3) ? 4 : 8;
     constexpr int threads = kSmallWarps * 32;
     auto kern = small_row_kernel<MODE, P2, U>;
     int per_sm = 0;
@@ -219,6 +222,7 @@ KParams base_params(const rmsnorm_layout_t *L, int64_t H, float eps) {
         if ((int64_t(1) << sh) == int64_t(p.rpt)) p.rpt_shift = sh;
     p.hidden = int32_t(H);
     p.eps = eps;
+    p.grad_scale = 1.f;
     p.items = static_cast<const PlanItem *>(L->plan);
     p.use_plan = L->plan != nullptr ? 1 : 0;
     return p;
@@ -279,6 +283,58 @@ extern "C" int rmsnorm_bwd_dx(const uint16_t *x, const uint16_t *weight, const u
     return run_rows<kDxDw>(p, sh, layout, s);
 }
 
+extern "C" int rmsnorm_add_fwd(const uint16_t *x, const uint16_t *residual, const uint16_t *weight,
+                               int64_t hidden, float eps, const rmsnorm_layout_t *layout, uint16_t *h_out,
+                               uint16_t *y, float *rstd, rmsnorm_stream_t stream) {
+    Shape sh;
+    if (!hidden_shape(hidden, &sh)) return RMSNORM_ERR_HIDDEN;
+    int rc = check_layout(layout, hidden);
+    if (rc) return rc;
+    if (layout->n_tokens == 0) return RMSNORM_OK;
+    if (!x || !residual || !weight || !h_out || !y) return RMSNORM_ERR_NULL;
+    if (h_out == y) return RMSNORM_ERR_LAYOUT;
+    if (!aligned16(x) || !aligned16(residual) || !aligned16(weight) || !aligned16(h_out) || !aligned16(y))
+        return RMSNORM_ERR_ALIGN;
+    KParams p = base_params(layout, hidden, eps);
+    p.x = x;
+    p.res = residual;
+    p.w = weight;
+    p.out = y;
+    p.out2 = h_out;
+    p.rstd_out = rstd;
+    return run_rows<kAddFwd>(p, sh, layout, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int rmsnorm_add_bwd(const uint16_t *x, const uint16_t *weight, const uint16_t *dy, const uint16_t *dres,
+                               int64_t hidden, float eps, float grad_scale, const rmsnorm_layout_t *layout,
+                               uint16_t *dx, void *workspace, rmsnorm_stream_t stream) {
+    Shape sh;
+    if (!hidden_shape(hidden, &sh)) return RMSNORM_ERR_HIDDEN;
+    int rc = check_layout(layout, hidden);
+    if (rc) return rc;
+    if (!std::isfinite(grad_scale)) return RMSNORM_ERR_VALUE;
+    if (!workspace && !dx) return RMSNORM_ERR_NULL;
+    if (dres && !dx) return RMSNORM_ERR_NULL;
+    if (workspace && !layout->plan && layout->n_tokens > 0) return RMSNORM_ERR_PLAN;
+    const int64_t N = layout->n_logical_tokens * layout->rows_per_token;
+    if (workspace && (rc = ws_checks(workspace, N, hidden))) return rc;
+    if (layout->n_tokens == 0) return RMSNORM_OK;
+    if (!x || !weight || !dy) return RMSNORM_ERR_NULL;
+    if (!aligned16(x) || !aligned16(weight) || !aligned16(dy) || (dx && !aligned16(dx)) || (dres && !aligned16(dres)))
+        return RMSNORM_ERR_ALIGN;
+    KParams p = base_params(layout, hidden, eps);
+    p.x = x;
+    p.w = weight;
+    p.dy = dy;
+    p.res = dres;
+    p.out = dx;
+    p.grad_scale = grad_scale;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (workspace) p.ws = ws_view(workspace, N, hidden);
+    if (dres) return workspace ? run_rows<kAddDxDw>(p, sh, layout, s) : run_rows<kAddDx>(p, sh, layout, s);
+    return workspace ? run_rows<kDxDw>(p, sh, layout, s) : run_rows<kDx>(p, sh, layout, s);
+}
+
 extern "C" int rmsnorm_bwd_dweight_contrib(const uint16_t *x, const uint16_t *dy, int64_t hidden, float eps,
                                            const rmsnorm_layout_t *layout, void *workspace,
                                            rmsnorm_stream_t stream) {
@@ -327,7 +383,7 @@ extern "C" int rmsnorm_dweight_begin(void *workspace, size_t bytes, int64_t n_lo
 
 namespace {
 // Tree passes over blocks [lo, lo + count) of the workspace, leaving one value in out.
-int finalize_blocks(const WsView &ws, int64_t lo, int64_t count, float *out, cudaStream_t s) {
+int finalize_blocks(const WsView &ws, int64_t lo, int64_t count, float *out, float scale, cudaStream_t s) {
     const int V = int(ws.hidden / 8);
     const unsigned gy = unsigned((V + kTreeVecs - 1) / kTreeVecs);
     int64_t n = count;
@@ -337,8 +393,8 @@ int finalize_blocks(const WsView &ws, int64_t lo, int64_t count, float *out, cud
     while (true) {
         const int64_t groups = (n + 31) / 32;
         float *dst = groups == 1 ? out : (flip ? ws.scratch_b : ws.scratch_a);
-        tree_pass_kernel<<<dim3(unsigned(groups), gy), kTreeWarps * 32, 0, s>>>(ws, in, dst, n, first ? 1 : 0,
-                                                                                first ? lo : 0);
+        tree_pass_kernel<<<dim3(unsigned(groups), gy), kTreeWarps * 32, 0, s>>>(
+            ws, in, dst, n, first ? 1 : 0, first ? lo : 0, groups == 1 ? scale : 1.f);
         if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
         g_launches.fetch_add(1, std::memory_order_relaxed);
         if (groups == 1) break;
@@ -353,6 +409,12 @@ int finalize_blocks(const WsView &ws, int64_t lo, int64_t count, float *out, cud
 
 extern "C" int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t hidden, float *dweight,
                                 rmsnorm_stream_t stream) {
+    return dweight_finalize_scaled(workspace, n_logical_rows, hidden, 1.f, dweight, stream);
+}
+
+extern "C" int dweight_finalize_scaled(void *workspace, int64_t n_logical_rows, int64_t hidden, float grad_scale,
+                                       float *dweight, rmsnorm_stream_t stream) {
+    if (!std::isfinite(grad_scale)) return RMSNORM_ERR_VALUE;
     int rc = ws_checks(workspace, n_logical_rows, hidden);
     if (rc) return rc;
     if (!dweight) return RMSNORM_ERR_NULL;
@@ -367,7 +429,7 @@ extern "C" int dweight_finalize(void *workspace, int64_t n_logical_rows, int64_t
         g_launches.fetch_add(1, std::memory_order_relaxed);
         return RMSNORM_OK;
     }
-    return finalize_blocks(ws, 0, ws.n_blocks, dweight, s);
+    return finalize_blocks(ws, 0, ws.n_blocks, dweight, grad_scale, s);
 }
 
 extern "C" int dweight_finalize_range(void *workspace, int64_t n_logical_rows, int64_t hidden, int64_t block_lo,
@@ -383,12 +445,13 @@ extern "C" int dweight_finalize_range(void *workspace, int64_t n_logical_rows, i
     DeviceInfo *d = nullptr;
     if ((rc = device_info(&d))) return rc;
     const int64_t count = block_lo + block_count > nb ? nb - block_lo : block_count;
-    return finalize_blocks(ws_view(workspace, n_logical_rows, hidden), block_lo, count, root,
+    return finalize_blocks(ws_view(workspace, n_logical_rows, hidden), block_lo, count, root, 1.f,
                            reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" int dweight_combine(const float *roots, int64_t n_roots, int64_t hidden, float *dweight,
-                               rmsnorm_stream_t stream) {
+extern "C" int dweight_combine(const float *roots, int64_t n_roots, int64_t hidden, float grad_scale,
+                               float *dweight, rmsnorm_stream_t stream) {
+    if (!std::isfinite(grad_scale)) return RMSNORM_ERR_VALUE;
     Shape sh;
     if (!hidden_shape(hidden, &sh)) return RMSNORM_ERR_HIDDEN;
     if (!roots || !dweight) return RMSNORM_ERR_NULL;
@@ -399,7 +462,7 @@ extern "C" int dweight_combine(const float *roots, int64_t n_roots, int64_t hidd
     if (rc) return rc;
     const int V = int(hidden / 8);
     combine_kernel<<<unsigned((V + 127) / 128), 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        roots, n_roots, int(hidden), dweight);
+        roots, n_roots, int(hidden), grad_scale, dweight);
     if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return RMSNORM_OK;
@@ -430,6 +493,7 @@ extern "C" const char *rmsnorm_strerror(int code) {
         case RMSNORM_ERR_CAPACITY: return "plan buffer too small";
         case RMSNORM_ERR_CUDA: return "CUDA runtime error";
         case RMSNORM_ERR_DEVICE: return "device is not sm_103";
+        case RMSNORM_ERR_VALUE: return "grad_scale is not finite";
         default: return "unknown error";
     }
 }

@@ -23,7 +23,11 @@
 
 namespace rbi {
 
-enum Mode : int { kFwd = 0, kDx = 1, kDxDw = 2, kDw = 3 };
+// kAdd*: the residual-add variants.  kAddFwd streams x and the residual r,
+// writes h = bf16(x + r) and y = RMSNorm(h); kAddDx / kAddDxDw stream the saved
+// h, dy and the gradient dres arriving at h along the residual path, and
+// write dh = bf16(grad_scale * dx + dres).
+enum Mode : int { kFwd = 0, kDx = 1, kDxDw = 2, kDw = 3, kAddFwd = 4, kAddDx = 5, kAddDxDw = 6 };
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
@@ -32,8 +36,11 @@ struct KParams {
     const uint16_t *x;
     const uint16_t *dy;
     const uint16_t *w;
-    uint16_t *out;                   // y (kFwd) or dx (kDx, kDxDw); may be null in kDxDw
-    float *rstd_out;                 // kFwd, optional
+    const uint16_t *res;             // kAddFwd: residual input r; kAddDx, kAddDxDw: dres
+    uint16_t *out;                   // y (forward modes) or dx (kDx, kDxDw, kAdd*); may be null in kDxDw
+    uint16_t *out2;                  // kAddFwd: h = bf16(x + r)
+    float *rstd_out;                 // forward modes, optional
+    float grad_scale;                // backward: dx is scaled by it (1 = no scaling)
     const int32_t *tok_id;
     int64_t n_rows;                  // physical rows of the call = n_tokens * rpt
     int64_t token_stride;            // elements
@@ -56,11 +63,14 @@ __device__ __forceinline__ int64_t row_offset(const KParams &p, int64_t prow) {
 
 template <int MODE>
 struct ModeTraits {
-    static constexpr bool kNeedDy = MODE != kFwd;
-    static constexpr bool kNeedGx = MODE == kDx || MODE == kDxDw;   // sum(g*x) for dx
-    static constexpr bool kLeaves = MODE == kDxDw || MODE == kDw;
+    static constexpr bool kFwdLike = MODE == kFwd || MODE == kAddFwd;
+    static constexpr bool kNeedDy = !kFwdLike;
+    static constexpr bool kNeedGx = MODE == kDx || MODE == kDxDw || MODE == kAddDx || MODE == kAddDxDw;
+    static constexpr bool kLeaves = MODE == kDxDw || MODE == kDw || MODE == kAddDxDw;
+    static constexpr bool kRes = MODE == kAddFwd || MODE == kAddDx || MODE == kAddDxDw;   // streams p.res
     static constexpr bool kWritesOut = MODE != kDw;
-    static constexpr int kTensors = kNeedDy ? 2 : 1;
+    static constexpr int kTensors = 1 + (kNeedDy ? 1 : 0) + (kRes ? 1 : 0);
+    static constexpr int kResSlot = kNeedDy ? 2 : 1;            // stage slot of p.res
 };
 
 // Book-keeping of contributions (one thread per team).  A block's four state
@@ -326,6 +336,8 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     if (offs[r] < 0) continue;
                     bulk_copy_g2s(stage_ptr(s, 0, r), p.x + offs[r] + col0, row_bytes, &full[s]);
                     if (T::kNeedDy) bulk_copy_g2s(stage_ptr(s, 1, r), p.dy + offs[r] + col0, row_bytes, &full[s]);
+                    if (T::kRes)
+                        bulk_copy_g2s(stage_ptr(s, T::kResSlot, r), p.res + offs[r] + col0, row_bytes, &full[s]);
                 }
                 if (++s == S) {
                     s = 0;
@@ -358,6 +370,13 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     for (int v = lane; v < VS; v += 32) {
                         f2_t xf[4];
                         f2_unpack8(ld_shared_v4(xr + v * 16), xf);
+                        if (MODE == kAddFwd) {                  // the row is h = bf16(x + r)
+                            f2_t rf[4];
+                            f2_unpack8(ld_shared_v4(stage_ptr(s, T::kResSlot, r) + v * 16), rf);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) xf[i] = f2_add(xf[i], rf[i]);
+                            f2_unpack8(f2_pack8(xf), xf);
+                        }
 #pragma unroll
                         for (int i = 0; i < 4; ++i) a2 = f2_fma(xf[i], xf[i], a2);
                         if (T::kNeedGx) {
@@ -419,7 +438,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                 st.rstd = rstd;
                 st.mg = T::kNeedGx ? row_mean_gxhat(gx, rstd, Hf) : 0.f;
                 stats[s * R + lane] = st;
-                if (MODE == kFwd && rank == 0 && p.rstd_out != nullptr && m[lane].off >= 0)
+                if (T::kFwdLike && rank == 0 && p.rstd_out != nullptr && m[lane].off >= 0)
                     p.rstd_out[m[lane].prow] = rstd;
             }
             __syncwarp();
@@ -432,6 +451,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
         const int64_t my_col = col0 + int64_t(t) * 8;
         f2_t wv[4];
         if (MODE != kDw && has_vec) f2_unpack8(*reinterpret_cast<const uint4 *>(p.w + my_col), wv);
+        const float gscale = p.grad_scale;
         TreeStackF2<4, 4> tree;            // levels log2(R)..3 of the 16-leaf unit
         int32_t kind = 0, block = -1, quarter = 0;
         int s = 0, sub = 0;
@@ -476,9 +496,18 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     const f2_t r2 = f2_make(st.rstd, st.rstd);
                     f2_t xf[4], xh[4], o[4];
                     f2_unpack8(ld_shared_v4(stage_ptr(s, 0, r) + t * 16), xf);
+                    if (MODE == kAddFwd) {                          // h = bf16(x + r), stored, then normed
+                        f2_t rf[4];
+                        f2_unpack8(ld_shared_v4(stage_ptr(s, T::kResSlot, r) + t * 16), rf);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) xf[i] = f2_add(xf[i], rf[i]);
+                        const uint4 hb = f2_pack8(xf);
+                        st_global_v4(p.out2 + off + my_col, hb);
+                        f2_unpack8(hb, xf);
+                    }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) xh[i] = f2_mul(xf[i], r2);
-                    if (MODE == kFwd) {
+                    if (T::kFwdLike) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) o[i] = f2_mul(xh[i], wv[i]);
                         st_global_v4(p.out + off + my_col, f2_pack8(o));
@@ -487,8 +516,16 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                         f2_unpack8(ld_shared_v4(stage_ptr(s, 1, r) + t * 16), df);
                         if (T::kNeedGx && p.out != nullptr) {
                             const f2_t nm2 = f2_make(-st.mg, -st.mg);
+                            const float rs = __fmul_rn(st.rstd, gscale);    // == rstd when unscaled
+                            const f2_t rs2 = f2_make(rs, rs);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) o[i] = f2_mul(r2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
+                            for (int i = 0; i < 4; ++i) o[i] = f2_mul(rs2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
+                            if (T::kRes) {
+                                f2_t rf[4];
+                                f2_unpack8(ld_shared_v4(stage_ptr(s, T::kResSlot, r) + t * 16), rf);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) o[i] = f2_add(o[i], rf[i]);
+                            }
                             st_global_v4(p.out + off + my_col, f2_pack8(o));
                         }
                         if (T::kLeaves) {
@@ -577,6 +614,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
             int64_t off[kU];
             int32_t lrow[kU], prow[kU];
             uint4 xv[kU], dv[kU];
+            constexpr int kRv = (T::kRes && T::kNeedDy) ? kU : 1;   // dres registers (kAddDx*)
+            uint4 rv[kRv];
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
                 const int slot = (st0 + q) * TPW + team;
@@ -594,9 +633,12 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                 prow[q] = pr;
                 xv[q] = make_uint4(0, 0, 0, 0);
                 dv[q] = make_uint4(0, 0, 0, 0);
+                if (kRv > 1) rv[q % kRv] = make_uint4(0, 0, 0, 0);
                 if (act && has_vec) {
                     xv[q] = ld_global_stream_v4(p.x + off[q]);
                     if (T::kNeedDy) dv[q] = ld_global_stream_v4(p.dy + off[q]);
+                    if (MODE == kAddFwd) dv[q] = ld_global_stream_v4(p.res + off[q]);   // r rides in dv
+                    if (kRv > 1) rv[q % kRv] = ld_global_stream_v4(p.res + off[q]);
                 }
             }
 #pragma unroll
@@ -605,6 +647,13 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                 f2_t xf[4], df[4];
                 f2_unpack8(xv[q], xf);
                 f2_unpack8(dv[q], df);
+                uint4 hb = make_uint4(0, 0, 0, 0);
+                if (MODE == kAddFwd) {                              // the row is h = bf16(x + r)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) xf[i] = f2_add(xf[i], df[i]);
+                    hb = f2_pack8(xf);
+                    f2_unpack8(hb, xf);
+                }
                 // row sums: two FMA chains (even / odd columns), then the team butterfly
                 f2_t a2 = 0ull, b2 = 0ull;
 #pragma unroll
@@ -625,16 +674,25 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                     f2_t xh[4], o[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) xh[i] = f2_mul(xf[i], r2);
-                    if (MODE == kFwd) {
+                    if (T::kFwdLike) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) o[i] = f2_mul(xh[i], wv[i]);
                         st_global_v4(p.out + off[q], f2_pack8(o));
+                        if (MODE == kAddFwd) st_global_v4(p.out2 + off[q], hb);
                     } else {
                         if (T::kNeedGx && p.out != nullptr) {
                             const float mg = row_mean_gxhat(gx, rstd, Hf);
                             const f2_t nm2 = f2_make(-mg, -mg);
+                            const float rs = __fmul_rn(rstd, p.grad_scale);    // == rstd when unscaled
+                            const f2_t rs2 = f2_make(rs, rs);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) o[i] = f2_mul(r2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
+                            for (int i = 0; i < 4; ++i) o[i] = f2_mul(rs2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
+                            if (kRv > 1) {
+                                f2_t rf[4];
+                                f2_unpack8(rv[q % kRv], rf);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) o[i] = f2_add(o[i], rf[i]);
+                            }
                             st_global_v4(p.out + off[q], f2_pack8(o));
                         }
                         if (T::kLeaves) {
@@ -643,7 +701,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                         }
                     }
                 }
-                if (MODE == kFwd && act && p.rstd_out != nullptr && tl == 0) p.rstd_out[prow[q]] = rstd;
+                if (T::kFwdLike && act && p.rstd_out != nullptr && tl == 0) p.rstd_out[prow[q]] = rstd;
                 if (T::kLeaves) {
                     if (kind == 0) {
                         // the TPW rows of this step: adjacent teams first
@@ -713,7 +771,7 @@ constexpr int kTreeVecs = 32;                            // vectors (8 columns) 
 
 __global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, const float *in, float *out,
                                                                     int64_t n_in, int from_blocks,
-                                                                    int64_t block_base) {
+                                                                    int64_t block_base, float scale) {
     __shared__ float part[kTreeWarps][8][kTreeVecs];      // [pair][column][vector]
     const int H = int(ws.hidden), V = H >> 3;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -799,6 +857,10 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, c
         }
         float res[8];
         st.fold(np, res);
+        if (scale != 1.f) {                              // only on the root of a scaled finalize
+#pragma unroll
+            for (int c = 0; c < 8; ++c) res[c] = __fmul_rn(res[c], scale);
+        }
         float *dst = out + g * int64_t(H) + int64_t(v) * 8;
         st_global_f32x4(dst, res[0], res[1], res[2], res[3]);
         st_global_f32x4(dst + 4, res[4], res[5], res[6], res[7]);
@@ -808,7 +870,8 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, c
 // Carry tree over n partials [n][H] (n <= 2^11), one lane per 8-column
 // vector, folded with the binary-counter stack: the top of the dweight tree
 // above aligned subtrees whose roots were gathered from several ranks.
-__global__ void __launch_bounds__(128) combine_kernel(const float *roots, int64_t n, int H, float *out) {
+__global__ void __launch_bounds__(128) combine_kernel(const float *roots, int64_t n, int H, float scale,
+                                                      float *out) {
     const int v = blockIdx.x * blockDim.x + threadIdx.x;
     if (v >= (H >> 3)) return;
     float s[11][8];
@@ -834,6 +897,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *roots, int64_
 #pragma unroll
         for (int c = 0; c < 8; ++c) res[c] = have ? __fadd_rn(s[l][c], res[c]) : s[l][c];
         have = true;
+    }
+    if (scale != 1.f) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) res[c] = __fmul_rn(res[c], scale);
     }
     st_global_f32x4(out + int64_t(v) * 8, res[0], res[1], res[2], res[3]);
     st_global_f32x4(out + int64_t(v) * 8 + 4, res[4], res[5], res[6], res[7]);

@@ -34,6 +34,7 @@ class LayoutRun:
     whole_blocks: int = 0
     spill_rows: int = 0
     untouched_padding: bool = True
+    h: object = None            # residual-add chain: h = bf16(x + r), logical order
 
 
 @dataclass
@@ -171,6 +172,55 @@ def run_layout(lay: layout_mod.Layout, x_log, dy_log, weight, eps: float, rows_p
                      untouched)
 
 
+def run_layout_chain(lay: layout_mod.Layout, x_log, r_log, dy_log, dres_log, weight, eps: float, grad_scale,
+                     rows_per_token: int = 1, device="cuda", stream=None) -> LayoutRun:
+    """Residual add + norm forward and its backward with the loss seed's scale,
+    through the library, for one layout; outputs in logical order.
+
+    grad_scale is a float (the same 1/D for every call: the multiset's
+    active-token denominator) or a callable taking a call's token ids and
+    returning that call's factor (used to show that a per-call denominator is
+    caught).  dweight is finalized with the float, or with 1 for a callable."""
+    import torch
+    import invariant_rmsnorm_fwd_gb300 as rb
+    H = weight.shape[0]
+    R = rows_per_token
+    views = [t.reshape(-1, R, H) for t in (x_log, r_log, dy_log, dres_log)]
+    n_tok = views[0].shape[0]
+    ws = rb.DweightWorkspace(n_tok * R, H, device=device)
+    outs = {k: torch.empty_like(views[0]) for k in ("h", "y", "dx")}
+    ws.begin(stream)
+    whole = spill = 0
+    untouched = True
+    sent = torch.tensor(SENTINEL_BITS, dtype=torch.int16, device=device)
+    for tok in lay.calls:
+        cl = rb.call_layout(tok, R, lay.n_logical_tokens, device=device)
+        whole += cl.whole_blocks
+        spill += cl.spill_rows
+        tid = cl.tok_id.long()
+        act = tid >= 0
+        phys = []
+        for v in views:
+            t = torch.full((tok.size, R, H), float("nan"), dtype=torch.bfloat16, device=device)
+            t[act] = v[tid[act]]
+            phys.append(t)
+        xp, rp, dp, drp = phys
+        hp = torch.empty((tok.size, R, H), dtype=torch.int16, device=device).fill_(SENTINEL_BITS).view(torch.bfloat16)
+        yp, dxp = hp.clone(), hp.clone()
+        rb.rmsnorm_add_fwd(xp, rp, weight, cl, eps, h=hp, y=yp, stream=stream)
+        s = grad_scale(tok) if callable(grad_scale) else grad_scale
+        rb.rmsnorm_add_bwd(hp, weight, dp, cl, eps, dres=drp, grad_scale=s, dx=dxp, workspace=ws, stream=stream)
+        outs["h"][tid[act]] = hp[act]
+        outs["y"][tid[act]] = yp[act]
+        outs["dx"][tid[act]] = dxp[act]
+        if bool((~act).any()):
+            pad = ~act
+            untouched &= all(bool((t[pad].view(torch.int16) == sent).all()) for t in (hp, yp, dxp))
+    dw = ws.finalize(stream=stream, grad_scale=1.0 if callable(grad_scale) else grad_scale)
+    return LayoutRun(lay.name, outs["y"], outs["dx"], dw, ws.status(stream), len(lay.calls), lay.rows_per_call,
+                     whole, spill, untouched, h=outs["h"])
+
+
 def assert_batch_invariant(runs: dict, layouts: dict, reference: str = "full") -> InvarianceReport:
     """Bitwise comparison of every layout's y, dx and dweight with the reference layout."""
     rep = InvarianceReport(reference)
@@ -180,6 +230,9 @@ def assert_batch_invariant(runs: dict, layouts: dict, reference: str = "full") -
         if name == reference:
             continue
         rep.distinct[name] = layouts_differ(layouts[reference], layouts[name])
-        for t in ("y", "dx", "dweight"):
-            rep.diffs.append(bitwise_diff(t, getattr(run, t), getattr(ref, t), name, reference))
+        for t in ("y", "dx", "dweight", "h"):
+            a, b = getattr(run, t), getattr(ref, t)
+            if a is None and b is None:
+                continue
+            rep.diffs.append(bitwise_diff(t, a, b, name, reference))
     return rep

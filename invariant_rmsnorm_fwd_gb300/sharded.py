@@ -143,12 +143,12 @@ def gather_status(status: int, group=None) -> int:
     return s
 
 
-def sharded_dweight(workspace, plan: ShardPlan, rank: int, group=None, stream=None):
+def sharded_dweight(workspace, plan: ShardPlan, rank: int, group=None, stream=None, grad_scale: float = 1.0):
     """dweight of the whole multiset on every rank, bitwise equal to one device's
-    dweight_finalize over all rows: local nodes, all-gather, combine."""
+    dweight_finalize_scaled over all rows: local nodes, all-gather, combine."""
     import torch
     from . import dweight_combine
     if plan.n_ranges == 0:
         return torch.zeros(workspace.hidden, dtype=torch.float32, device=workspace.buf.device)
     roots = gather_roots(local_roots(workspace, plan, rank, stream), plan, group)
-    return dweight_combine(roots.to(workspace.buf.device), stream=stream)
+    return dweight_combine(roots.to(workspace.buf.device), stream=stream, grad_scale=grad_scale)

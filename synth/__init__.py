@@ -22,6 +22,7 @@ import torch
 
 # tensor tags: independent streams per tensor
 TAG_X, TAG_W, TAG_DY, TAG_LEN, TAG_OUTLIER, TAG_PERM, TAG_WK = 1, 2, 3, 4, 5, 6, 7
+TAG_RES, TAG_DRES = 8, 9          # residual-add chain: the residual input and its gradient
 _GOLDEN = 0x9E3779B97F4A7C15
 _M1 = 0xBF58476D1CE4E5B9
 _M2 = 0x94D049BB133111EB

@@ -68,6 +68,20 @@ def test_host_side_errors_need_no_gpu():
     assert lib.rmsnorm_dweight_workspace_bytes(64, 12) == 0
     # an empty call is a no-op that needs no device
     assert lib.rmsnorm_fwd(good, good, 8, 1e-6, ctypes.byref(_layout(n_tokens=0, tok=None)), good, None, None) == 0
+    # residual-add chain and loss-seed scale
+    nan, inf = float("nan"), float("inf")
+    assert lib.rmsnorm_add_fwd(good, None, good, 8, 1e-6, ctypes.byref(L), good, good, None, None) == -1
+    assert lib.rmsnorm_add_fwd(good, good, good, 8, 1e-6, ctypes.byref(L), good, good, None, None) == -5   # h == y
+    assert lib.rmsnorm_add_fwd(good, P(264), good, 8, 1e-6, ctypes.byref(L), good, P(512), None, None) == -3
+    assert lib.rmsnorm_add_bwd(good, good, good, None, 8, 1e-6, nan, ctypes.byref(L), good, None, None) == -13
+    assert lib.rmsnorm_add_bwd(good, good, good, None, 8, 1e-6, inf, ctypes.byref(L), good, None, None) == -13
+    assert lib.rmsnorm_add_bwd(good, good, good, good, 8, 1e-6, 1.0, ctypes.byref(L), None, good, None) == -1
+    assert lib.rmsnorm_add_bwd(good, good, good, None, 8, 1e-6, 1.0, ctypes.byref(L), good, good, None) == -7
+    assert lib.dweight_finalize_scaled(good, 64, 8, nan, good, None) == -13
+    assert lib.dweight_combine(good, 2, 8, inf, good, None) == -13
+    assert lib.dweight_combine(good, 2048, 8, 1.0, good, None) == -5
+    assert lib.dweight_finalize_range(good, 640, 8, 1, 2, good, None) == -5    # not aligned
+    assert lib.dweight_finalize_range(good, 640, 8, 0, 3, good, None) == -5    # not a power of two
 
 
 def test_workspace_size_formula():
@@ -81,5 +95,5 @@ def test_workspace_size_formula():
 
 def test_strerror_covers_codes():
     lib = rb._load()
-    for c in range(0, -13, -1):
+    for c in range(0, -14, -1):
         assert lib.rmsnorm_strerror(c) not in (None, b"unknown error")
