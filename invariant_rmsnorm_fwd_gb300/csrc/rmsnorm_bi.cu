@@ -146,7 +146,7 @@ template <int MODE, int R, int K>
 int launch_split_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
     if ((sh.nc + kSplitStatsWarps + 1) * 32 <= 608)
         return launch_split_t<MODE, R, 608, kSplitStatsWarps, K>(p, sh, d, stream);
-    return launch_split_t<MODE, R, 768, kSplitStatsWarps, K>(p, sh, d, stream);
+    return launch_split_t<MODE, R, 736, kSplitStatsWarps, K>(p, sh, d, stream);
 }
 
 template <int MODE, int R>

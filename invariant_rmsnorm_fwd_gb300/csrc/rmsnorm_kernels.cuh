@@ -454,27 +454,29 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
         const float gscale = p.grad_scale;
         TreeStackF2<4, 4> tree;            // levels log2(R)..3 of the 16-leaf unit
         int32_t kind = 0, block = -1, quarter = 0;
-        int s = 0, sub = 0;
+        int s = 0;
         uint32_t parity = 0;
         int64_t u = cluster_id;                               // current quarter unit
-        for (int k = 0; k < n_batches; ++k) {
-            if (k > 0) {
-                if (++s == S) {
-                    s = 0;
-                    parity ^= 1u;
-                }
-                if (++sub == per_unit) {
-                    sub = 0;
-                    u += n_clusters;
-                }
+        // Leaf modes walk their 16-row units; the inner loop over the unit's
+        // batches (stages of R rows) is unrolled, so `sub`, the batch's place in
+        // the unit, is a compile-time constant and the tree positions are static.
+        constexpr int kInner = T::kLeaves ? kUnitBatches : 1;
+        const int64_t n_outer = n_batches / kInner;          // leaf modes: n_batches = units * kUnitBatches
+        bool stop = false;
+        for (int64_t j = 0; j < n_outer && !stop; ++j, u += n_clusters) {
+#pragma unroll
+          for (int sub = 0; sub < kInner; ++sub) {
+            if (*abort_flag) {
+                stop = true;
+                break;
             }
-            if (*abort_flag) break;
             if (!mbar_wait_bounded(&stats_bar[s], parity) || !mbar_wait_bounded(&full[s], parity)) {
                 *abort_flag = 1;
                 if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
+                stop = true;
                 break;
             }
-            if (item_units && sub == 0) {                    // item header, staged by the producer
+            if (T::kLeaves && sub == 0) {                    // item header, staged by the producer
                 const int2 hd = item_hdr[s];
                 quarter = int(u & 3);
                 kind = hd.x;
@@ -538,7 +540,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     if (kind == 0) {
                         if (R > 1) mini.template push_static<0>(leaf, r);
                         if (r == R - 1) {
-                            tree.template push_dyn<kLogR>(leaf, sub);
+                            tree.template push_static<kLogR>(leaf, sub);
                             if (sub == kUnitBatches - 1) {           // leaf[] is the quarter partial
                                 if (has_vec)
                                     st_global_f2x4(p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + my_col, leaf);
@@ -553,6 +555,11 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            if (++s == S) {
+                s = 0;
+                parity ^= 1u;
+            }
+          }
         }
     }
     if (K > 1) cluster_barrier();      // peers may still store into our exchange buffers
