@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fno-strict-aliasing", f"-I{INCLUDE}"]
-SOURCES = ["rmsnorm_bi.cu", "plan.cpp"]
+SOURCES = ["rmsnorm_bi.cu", "rows_fwd.cu", "rows_dx.cu", "rows_dxdw.cu", "rows_adddxdw.cu", "plan.cpp"]
 
 
 def nvcc() -> str:

@@ -1,0 +1,139 @@
+// Launch shapes of the row kernels.  They depend on the hidden size, the mode
+// and the device's SM count only; which CTA handles which row never changes a
+// value, so results are identical for every grid.
+#pragma once
+#include "host.cuh"
+
+namespace rbi {
+
+// ---------------------------------------------------------------- launches
+
+template <int MODE, int R, int MAXT, int NS, int K>
+int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
+    constexpr int nt = ModeTraits<MODE>::kTensors;
+    const int slice = p.hidden / K;
+    const int64_t stage_bytes = int64_t(R) * nt * slice * 2;
+    const int64_t off = split_stage_off(slice);
+    int S = int((int64_t(d.max_smem) - off) / stage_bytes);
+    if (S > kSplitMaxStages) S = kSplitMaxStages;
+    if (S < 2) return RMSNORM_ERR_HIDDEN;
+    const int smem = int(off + S * stage_bytes);
+    const int threads = (sh.nc + NS + 1) * 32;
+    if (threads > MAXT) return RMSNORM_ERR_HIDDEN;
+    auto kern = split_kernel<MODE, R, MAXT, NS, K>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    int64_t teams;
+    if (K > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = K;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(K * d.sms);
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) return RMSNORM_ERR_CUDA;
+        teams = active;
+    } else {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+            return RMSNORM_ERR_CUDA;
+        teams = int64_t(per_sm) * d.sms;
+    }
+    if (teams > p.n_units) teams = p.n_units;
+    if (teams < 1) return RMSNORM_OK;
+    cfg.gridDim = dim3(unsigned(teams * K));
+    if (cudaLaunchKernelEx(&cfg, kern, p, S, sh.nc) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    count_launch();
+    return RMSNORM_OK;
+}
+
+// The stats-warp count: a K-CTA team (K > 1) exchanges row partials through
+// distributed shared memory, and a stats warp waits for its peers on every
+// stage, so more stats warps keep more stages' exchanges in flight (measured
+// on hidden 8192: forward best with 3, backward with 6; a single CTA keeps 2).
+// Bounded by the 23 warps of the widest launch.  Thread counts up to 640 get
+// the 96-register budget, wider ones 80.
+template <int MODE, int R, int K, int NS>
+int launch_split_ns(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
+    if ((sh.nc + NS + 1) * 32 <= 640) return launch_split_t<MODE, R, 640, NS, K>(p, sh, d, stream);
+    return launch_split_t<MODE, R, 736, NS, K>(p, sh, d, stream);
+}
+
+template <int MODE, int R, int K>
+int launch_split_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
+    constexpr int kWant = K == 1 ? kSplitStatsWarps : (ModeTraits<MODE>::kFwdLike ? 3 : 6);
+    if (kWant > kSplitStatsWarps && sh.nc + kWant + 1 <= 736 / 32)
+        return launch_split_ns<MODE, R, K, kWant>(p, sh, d, stream);
+    return launch_split_ns<MODE, R, K, kSplitStatsWarps>(p, sh, d, stream);
+}
+
+template <int MODE, int R>
+int launch_split(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
+    switch (sh.k) {
+        case 1: return launch_split_k<MODE, R, 1>(p, sh, d, stream);
+        case 2: return launch_split_k<MODE, R, 2>(p, sh, d, stream);
+        case 4: return launch_split_k<MODE, R, 4>(p, sh, d, stream);
+        default: return RMSNORM_ERR_HIDDEN;
+    }
+}
+
+template <int MODE, int P2>
+int launch_small(const KParams &p, const DeviceInfo &d, cudaStream_t stream) {
+    // warp steps loaded together (fewer when three tensors or the leaf tree hold registers)
+    using T = ModeTraits<MODE>;
+    constexpr int U = (T::kLeaves && T::kTensors >= 3) ? 2 : (T::kLeaves || T::kTensors >= 3) ? 4 : 8;
+    constexpr int threads = kSmallWarps * 32;
+    auto kern = small_row_kernel<MODE, P2, U>;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess || per_sm < 1)
+        return RMSNORM_ERR_CUDA;
+    int64_t blocks = int64_t(per_sm) * d.sms;
+    const int64_t need = (p.n_units + kSmallWarps - 1) / kSmallWarps;   // one unit per warp at least
+    if (blocks > need) blocks = need;
+    if (blocks < 1) return RMSNORM_OK;
+    kern<<<unsigned(blocks), threads, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
+    count_launch();
+    return RMSNORM_OK;
+}
+
+template <int MODE>
+int launch_small_p(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t s) {
+    switch (sh.p2) {
+        case 1: return launch_small<MODE, 1>(p, d, s);
+        case 2: return launch_small<MODE, 2>(p, d, s);
+        case 4: return launch_small<MODE, 4>(p, d, s);
+        case 8: return launch_small<MODE, 8>(p, d, s);
+        case 16: return launch_small<MODE, 16>(p, d, s);
+        case 32: return launch_small<MODE, 32>(p, d, s);
+        default: return RMSNORM_ERR_HIDDEN;
+    }
+}
+
+template <int MODE>
+int run_rows(KParams p, const Shape &sh, const rmsnorm_layout_t *L, cudaStream_t stream) {
+    DeviceInfo *d = nullptr;
+    int rc = device_info(&d);
+    if (rc != RMSNORM_OK) return rc;
+    constexpr bool leaves = ModeTraits<MODE>::kLeaves;
+    const bool plan = p.use_plan != 0;
+    if (sh.small) {
+        p.n_units = plan ? L->plan_items : (p.n_rows + kBlockRows - 1) / kBlockRows;
+        if (p.n_units == 0) return RMSNORM_OK;
+        return launch_small_p<MODE>(p, sh, *d, stream);
+    }
+    constexpr int R = (MODE == kFwd) ? 4 : 2;            // rows per pipeline stage (measured best)
+    if (plan) p.n_units = leaves ? L->plan_items * 4 : L->plan_items * (kBlockRows / R);
+    else p.n_units = (p.n_rows + R - 1) / R;
+    if (p.n_units == 0) return RMSNORM_OK;
+    return launch_split<MODE, R>(p, sh, *d, stream);
+}
+
+}  // namespace rbi

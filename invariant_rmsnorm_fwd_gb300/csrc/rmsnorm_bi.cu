@@ -9,76 +9,19 @@
 #include <cmath>
 #include <mutex>
 
+#include "finalize_kernels.cuh"
+#include "host.cuh"
 #include "rmsnorm_bi.h"
-#include "rmsnorm_kernels.cuh"
 
 using namespace rbi;
 
 namespace {
 
 std::atomic<int64_t> g_launches{0};
-
-struct DeviceInfo {
-    bool ready = false;
-    int status = RMSNORM_OK;
-    int sms = 0;
-    int max_smem = 0;
-};
 std::mutex g_mu;
 DeviceInfo g_dev[64];
 
-int device_info(DeviceInfo **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RMSNORM_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_mu);
-    DeviceInfo &d = g_dev[dev];
-    if (!d.ready) {
-        int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-            return RMSNORM_ERR_CUDA;
-        d.status = (major == 10 && minor == 3) ? RMSNORM_OK : RMSNORM_ERR_DEVICE;
-        d.ready = true;
-    }
-    *out = &d;
-    return d.status;
-}
-
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// ---------------------------------------------------------------- shapes
-
-struct Shape {
-    bool small = false;   // small_row_kernel
-    int p2 = 0;           // lanes per row (small)
-    int k = 1;            // CTAs per row team (split_kernel), a cluster when > 1
-    int nc = 0;           // column warps per CTA (split_kernel)
-};
-
-constexpr int kSplitStatsWarps = 2;
-constexpr int kSliceMaxVectors = 640;                    // columns per CTA <= 5120
-
-bool hidden_shape(int64_t H, Shape *s) {
-    if (H < 8 || H % 8 != 0 || H > 16384) return false;
-    const int64_t V = H / 8;
-    if (V <= 32) {
-        s->small = true;
-        int p = 1;
-        while (p < V) p <<= 1;
-        s->p2 = p;
-        return true;
-    }
-    for (int k = 1; k <= kSplitMaxK; k *= 2) {
-        if (V % k == 0 && V / k <= kSliceMaxVectors) {
-            s->k = k;
-            s->nc = int((V / k + 31) / 32);
-            return true;
-        }
-    }
-    return false;
-}
 
 int check_layout(const rmsnorm_layout_t *L, int64_t H) {
     if (!L) return RMSNORM_ERR_NULL;
@@ -92,123 +35,6 @@ int check_layout(const rmsnorm_layout_t *L, int64_t H) {
     if (rows >= (int64_t(1) << 31) || L->n_logical_tokens * L->rows_per_token >= (int64_t(1) << 31))
         return RMSNORM_ERR_LAYOUT;
     return RMSNORM_OK;
-}
-
-// ---------------------------------------------------------------- launches
-
-template <int MODE, int R, int MAXT, int NS, int K>
-int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
-    constexpr int nt = ModeTraits<MODE>::kTensors;
-    const int slice = p.hidden / K;
-    const int64_t stage_bytes = int64_t(R) * nt * slice * 2;
-    const int64_t off = split_stage_off(slice);
-    int S = int((int64_t(d.max_smem) - off) / stage_bytes);
-    if (S > kSplitMaxStages) S = kSplitMaxStages;
-    if (S < 2) return RMSNORM_ERR_HIDDEN;
-    const int smem = int(off + S * stage_bytes);
-    const int threads = (sh.nc + NS + 1) * 32;
-    if (threads > MAXT) return RMSNORM_ERR_HIDDEN;
-    auto kern = split_kernel<MODE, R, MAXT, NS, K>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return RMSNORM_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    int64_t teams;
-    if (K > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = K;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cfg.gridDim = dim3(K * d.sms);
-        int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) return RMSNORM_ERR_CUDA;
-        teams = active;
-    } else {
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
-            return RMSNORM_ERR_CUDA;
-        teams = int64_t(per_sm) * d.sms;
-    }
-    if (teams > p.n_units) teams = p.n_units;
-    if (teams < 1) return RMSNORM_OK;
-    cfg.gridDim = dim3(unsigned(teams * K));
-    if (cudaLaunchKernelEx(&cfg, kern, p, S, sh.nc) != cudaSuccess) return RMSNORM_ERR_CUDA;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return RMSNORM_OK;
-}
-
-template <int MODE, int R, int K>
-int launch_split_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
-    if ((sh.nc + kSplitStatsWarps + 1) * 32 <= 608)
-        return launch_split_t<MODE, R, 608, kSplitStatsWarps, K>(p, sh, d, stream);
-    return launch_split_t<MODE, R, 736, kSplitStatsWarps, K>(p, sh, d, stream);
-}
-
-template <int MODE, int R>
-int launch_split(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
-    switch (sh.k) {
-        case 1: return launch_split_k<MODE, R, 1>(p, sh, d, stream);
-        case 2: return launch_split_k<MODE, R, 2>(p, sh, d, stream);
-        case 4: return launch_split_k<MODE, R, 4>(p, sh, d, stream);
-        default: return RMSNORM_ERR_HIDDEN;
-    }
-}
-
-template <int MODE, int P2>
-int launch_small(const KParams &p, const DeviceInfo &d, cudaStream_t stream) {
-    // warp steps loaded together (fewer when three tensors or the leaf tree hold registers)
-    using T = ModeTraits<MODE>;
-    constexpr int U = (T::kLeaves && T::kTensors >= 3) ? 2 : (T::kLeaves || T::kTensors >= 3) ? 4 : 8;
-    constexpr int threads = kSmallWarps * 32;
-    auto kern = small_row_kernel<MODE, P2, U>;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess || per_sm < 1)
-        return RMSNORM_ERR_CUDA;
-    int64_t blocks = int64_t(per_sm) * d.sms;
-    const int64_t need = (p.n_units + kSmallWarps - 1) / kSmallWarps;   // one unit per warp at least
-    if (blocks > need) blocks = need;
-    if (blocks < 1) return RMSNORM_OK;
-    kern<<<unsigned(blocks), threads, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return RMSNORM_OK;
-}
-
-template <int MODE>
-int launch_small_p(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t s) {
-    switch (sh.p2) {
-        case 1: return launch_small<MODE, 1>(p, d, s);
-        case 2: return launch_small<MODE, 2>(p, d, s);
-        case 4: return launch_small<MODE, 4>(p, d, s);
-        case 8: return launch_small<MODE, 8>(p, d, s);
-        case 16: return launch_small<MODE, 16>(p, d, s);
-        case 32: return launch_small<MODE, 32>(p, d, s);
-        default: return RMSNORM_ERR_HIDDEN;
-    }
-}
-
-template <int MODE>
-int run_rows(KParams p, const Shape &sh, const rmsnorm_layout_t *L, cudaStream_t stream) {
-    DeviceInfo *d = nullptr;
-    int rc = device_info(&d);
-    if (rc != RMSNORM_OK) return rc;
-    constexpr bool leaves = ModeTraits<MODE>::kLeaves;
-    const bool plan = p.use_plan != 0;
-    if (sh.small) {
-        p.n_units = plan ? L->plan_items : (p.n_rows + kBlockRows - 1) / kBlockRows;
-        if (p.n_units == 0) return RMSNORM_OK;
-        return launch_small_p<MODE>(p, sh, *d, stream);
-    }
-    constexpr int R = (MODE == kFwd) ? 4 : 2;            // rows per pipeline stage (measured best)
-    if (plan) p.n_units = leaves ? L->plan_items * 4 : L->plan_items * (kBlockRows / R);
-    else p.n_units = (p.n_rows + R - 1) / R;
-    if (p.n_units == 0) return RMSNORM_OK;
-    return launch_split<MODE, R>(p, sh, *d, stream);
 }
 
 KParams base_params(const rmsnorm_layout_t *L, int64_t H, float eps) {
@@ -238,6 +64,31 @@ int ws_checks(const void *ws, int64_t N, int64_t H) {
 }
 
 }  // namespace
+
+namespace rbi {
+
+int device_info(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RMSNORM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        d.status = (major == 10 && minor == 3) ? RMSNORM_OK : RMSNORM_ERR_DEVICE;
+        d.ready = true;
+    }
+    *out = &d;
+    return d.status;
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace rbi
 
 // ==================================================================== C ABI
 

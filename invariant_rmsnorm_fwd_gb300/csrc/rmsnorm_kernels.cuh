@@ -732,190 +732,4 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
     }
 }
 
-// =====================================================================
-// Workspace set-up and the final reduction
-// =====================================================================
-
-__global__ void ws_begin_kernel(WsView ws) {
-    const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nthr = int64_t(gridDim.x) * blockDim.x;
-    // block_state and leaf_flag are contiguous up to the partials: clear both
-    uint8_t *base = ws.block_state;
-    const int64_t bytes = reinterpret_cast<uint8_t *>(ws.block_partial) - base;   // multiple of 256
-    uint4 *b4 = reinterpret_cast<uint4 *>(base);
-    for (int64_t i = tid; i < bytes / 16; i += nthr) b4[i] = make_uint4(0, 0, 0, 0);
-    if (tid == 0) {
-        ws.hdr->n_rows = ws.n_rows;
-        ws.hdr->hidden = ws.hidden;
-        ws.hdr->n_blocks = ws.n_blocks;
-        ws.hdr->status = 0;
-        ws.hdr->magic = kWsMagic;
-    }
-}
-
-// One pass of the block-partial tree over groups of 32 inputs.  CTA (g, c)
-// reduces inputs [32g, 32g+32) for the 32 vectors (256 columns) of chunk c:
-// lane l owns vector 32c+l, so every load of a warp is one contiguous 512-byte
-// row piece.  Warp w forms inputs 2w and 2w+1 and adds them (level 1); the 16
-// pair results go through shared memory and warp 0 folds them with the
-// binary-counter stack (levels 2-5).  Pairs are added only when their right
-// half is non-empty, which is the pairwise tree with odd carry restricted to
-// an aligned group of 32; later passes reduce the group results the same way.
-// In the first pass (from_blocks) an input is a block partial: the four
-// quarter partials as (q0 + q1) + (q2 + q3) (levels 5 and 6 of the 64-leaf
-// tree), a whole-block partial as is, or, for a block cut by a call boundary,
-// the 64-leaf tree over its spilled rows, rebuilt by the whole warp (lane l
-// adds rows 2l and 2l+1, then butterflies xor 1..16): the same tree as the
-// in-kernel path.
-__device__ __forceinline__ void load8(const float *src, float (&v)[8]) {
-    const float4 a = ld_global_f32x4(src), b = ld_global_f32x4(src + 4);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-
-constexpr int kTreeWarps = 16;                           // warps per CTA: 2 inputs each
-constexpr int kTreeVecs = 32;                            // vectors (8 columns) per CTA
-
-__global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, const float *in, float *out,
-                                                                    int64_t n_in, int from_blocks,
-                                                                    int64_t block_base, float scale) {
-    __shared__ float part[kTreeWarps][8][kTreeVecs];      // [pair][column][vector]
-    const int H = int(ws.hidden), V = H >> 3;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int v = blockIdx.y * kTreeVecs + lane;         // this lane's vector
-    const bool has_vec = v < V;
-    const int64_t g = blockIdx.x;
-    const int m = int(min64(32, n_in - g * 32));          // inputs in this group
-    if (from_blocks && !header_ok(ws)) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) set_status(ws.hdr, kStHeader);
-        return;                                          // uniform across the CTA
-    }
-    float pair[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) pair[c] = 0.f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int i = 2 * w + h;
-        if (i >= m) break;                               // uniform per warp
-        const int64_t b = (from_blocks ? block_base : 0) + g * 32 + i;
-        float val[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) val[c] = 0.f;
-        const uint32_t state = from_blocks ? reinterpret_cast<const uint32_t *>(ws.block_state)[b] : kStateWhole;
-        if (!from_blocks) {
-            if (has_vec) load8(in + b * int64_t(H) + int64_t(v) * 8, val);
-        } else if (state == 0x01010101u) {
-            if (has_vec) {
-                float q0[8], q1[8], q2[8], q3[8];
-                const float *src = ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8;
-                load8(src, q0);
-                load8(src + H, q1);
-                load8(src + 2 * int64_t(H), q2);
-                load8(src + 3 * int64_t(H), q3);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) val[c] = __fadd_rn(__fadd_rn(q0[c], q1[c]), __fadd_rn(q2[c], q3[c]));
-            }
-        } else if (state == kStateWhole) {
-            if (has_vec) load8(ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8, val);
-        } else if (state == 0) {
-            // cut block: the warp rebuilds it vector by vector; lane l adds rows 2l, 2l+1
-            const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
-            const int64_t r0 = b * kBlockRows + 2 * lane;
-            const bool have0 = 2 * lane < rows, have1 = 2 * lane + 1 < rows;
-            const bool missing = (have0 && ws.leaf_flag[r0] == 0) || (have1 && ws.leaf_flag[r0 + 1] == 0);
-            if (__any_sync(kFull, missing) && lane == 0 && blockIdx.y == 0) set_status(ws.hdr, kStMissing);
-#pragma unroll 1
-            for (int vv = 0; vv < kTreeVecs; ++vv) {
-                const int vg = blockIdx.y * kTreeVecs + vv;
-                if (vg >= V) break;                      // uniform
-                float a[8], c2[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) a[c] = c2[c] = 0.f;
-                if (have0) load8(ws.spill + r0 * int64_t(H) + int64_t(vg) * 8, a);
-                if (have1) load8(ws.spill + (r0 + 1) * int64_t(H) + int64_t(vg) * 8, c2);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) a[c] = __fadd_rn(a[c], c2[c]);        // level 1
-#pragma unroll
-                for (int k = 1; k < 32; k <<= 1)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) a[c] = __fadd_rn(a[c], __shfl_xor_sync(kFull, a[c], k));
-                if (lane == vv) {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) val[c] = a[c];
-                }
-            }
-        } else {
-            if (lane == 0 && blockIdx.y == 0) set_status(ws.hdr, kStMissing);   // partly contributed block
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) pair[c] = h == 0 ? val[c] : __fadd_rn(pair[c], val[c]);
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) part[w][c][lane] = pair[c];
-    __syncthreads();
-    if (w == 0 && has_vec) {
-        const int np = (m + 1) / 2;                      // pair results present
-        TreeStack<8> st;
-        for (int i = 0; i < np; ++i) {
-            float x[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) x[c] = part[i][c][lane];
-            st.push(x, i, 0);
-        }
-        float res[8];
-        st.fold(np, res);
-        if (scale != 1.f) {                              // only on the root of a scaled finalize
-#pragma unroll
-            for (int c = 0; c < 8; ++c) res[c] = __fmul_rn(res[c], scale);
-        }
-        float *dst = out + g * int64_t(H) + int64_t(v) * 8;
-        st_global_f32x4(dst, res[0], res[1], res[2], res[3]);
-        st_global_f32x4(dst + 4, res[4], res[5], res[6], res[7]);
-    }
-}
-
-// Carry tree over n partials [n][H] (n <= 2^11), one lane per 8-column
-// vector, folded with the binary-counter stack: the top of the dweight tree
-// above aligned subtrees whose roots were gathered from several ranks.
-__global__ void __launch_bounds__(128) combine_kernel(const float *roots, int64_t n, int H, float scale,
-                                                      float *out) {
-    const int v = blockIdx.x * blockDim.x + threadIdx.x;
-    if (v >= (H >> 3)) return;
-    float s[11][8];
-    for (int64_t i = 0; i < n; ++i) {
-        float x[8];
-        load8(roots + i * int64_t(H) + int64_t(v) * 8, x);
-        // binary counter: combine with pending partials while the bit of i is set
-        int l = 0;
-        while ((i >> l) & 1) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) x[c] = __fadd_rn(s[l][c], x[c]);
-            ++l;
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) s[l][c] = x[c];
-    }
-    float res[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) res[c] = 0.f;
-    bool have = false;
-    for (int l = 0; l < 11; ++l) {
-        if (!((n >> l) & 1)) continue;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) res[c] = have ? __fadd_rn(s[l][c], res[c]) : s[l][c];
-        have = true;
-    }
-    if (scale != 1.f) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) res[c] = __fmul_rn(res[c], scale);
-    }
-    st_global_f32x4(out + int64_t(v) * 8, res[0], res[1], res[2], res[3]);
-    st_global_f32x4(out + int64_t(v) * 8 + 4, res[4], res[5], res[6], res[7]);
-}
-
-__global__ void zero_f32_kernel(float *p, int64_t n) {
-    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
-        p[i] = 0.f;
-}
-
 }  // namespace rbi
