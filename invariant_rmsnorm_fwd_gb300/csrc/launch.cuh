@@ -88,7 +88,7 @@ template <int MODE, int P2>
 int launch_small(const KParams &p, const DeviceInfo &d, cudaStream_t stream) {
     // warp steps loaded together (fewer when three tensors or the leaf tree hold registers)
     using T = ModeTraits<MODE>;
-    constexpr int U = (T::kLeaves && T::kTensors >= 3) ? 2 : (T::kLeaves || T::kTensors >= 3) ? 4 : 8;
+    constexpr int U = (T::kLeaves && T::kTensors >= 3) ? 2 : T::kNeedDy ? 4 : 8;
     constexpr int threads = kSmallWarps * 32;
     auto kern = small_row_kernel<MODE, P2, U>;
     int per_sm = 0;

@@ -442,6 +442,23 @@ __device__ __forceinline__ void f2_unpack8(const uint4 &v, f2_t (&f)[4]) {
     f[2] = f2_from_bf16x2(v.z);
     f[3] = f2_from_bf16x2(v.w);
 }
+// The same unpacking as a volatile sequence: the compiler may not merge it
+// with an earlier unpacking of the same registers, so the unpacked values
+// need not stay live in between (used where packed data is kept across phases).
+__device__ __forceinline__ f2_t f2_from_bf16x2_v(uint32_t w) {
+    f2_t d;
+    asm volatile("{\n\t.reg .b32 lo, hi;\n\tshl.b32 lo, %1, 16;\n\tand.b32 hi, %1, 0xffff0000;\n\t"
+                 "mov.b64 %0, {lo, hi};\n\t}"
+                 : "=l"(d)
+                 : "r"(w));
+    return d;
+}
+__device__ __forceinline__ void f2_unpack8_v(const uint4 &v, f2_t (&f)[4]) {
+    f[0] = f2_from_bf16x2_v(v.x);
+    f[1] = f2_from_bf16x2_v(v.y);
+    f[2] = f2_from_bf16x2_v(v.z);
+    f[3] = f2_from_bf16x2_v(v.w);
+}
 __device__ __forceinline__ uint4 f2_pack8(const f2_t (&f)[4]) {
     return make_uint4(f2_to_bf16x2(f[0]), f2_to_bf16x2(f[1]), f2_to_bf16x2(f[2]), f2_to_bf16x2(f[3]));
 }
@@ -518,14 +535,25 @@ __device__ __forceinline__ float lane_tree(float v, int width) {
     return v;
 }
 
+// v / H, correctly rounded.  For a power-of-two H it is the product with the
+// exact reciprocal 2^-k: both operations round the same real number, so the
+// result is the same bit pattern and the division's longer sequence is
+// skipped.  inv_h is 1/H for a power-of-two H and 0 otherwise (row_inv_h).
+__device__ __forceinline__ float div_h(float v, float Hf, float inv_h) {
+    return inv_h != 0.f ? __fmul_rn(v, inv_h) : __fdiv_rn(v, Hf);
+}
+__device__ __forceinline__ float row_inv_h(int H) {
+    return (H & (H - 1)) == 0 ? __frcp_rn(float(H)) : 0.f;
+}
+
 // rstd = 1 / sqrt(ss / H + eps), each step correctly rounded.
-__device__ __forceinline__ float row_rstd(float ss, float Hf, float eps) {
-    return __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, Hf), eps)));
+__device__ __forceinline__ float row_rstd(float ss, float Hf, float inv_h, float eps) {
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(div_h(ss, Hf, inv_h), eps)));
 }
 
 // m = mean(g * xhat) = (rstd * sum(g * x)) / H.
-__device__ __forceinline__ float row_mean_gxhat(float gx, float rstd, float Hf) {
-    return __fdiv_rn(__fmul_rn(gx, rstd), Hf);
+__device__ __forceinline__ float row_mean_gxhat(float gx, float rstd, float Hf, float inv_h) {
+    return div_h(__fmul_rn(gx, rstd), Hf, inv_h);
 }
 
 // ----------------------------------------------------------------- 64-leaf tree

@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     const uint32_t rank = (K > 1) ? cluster_rank() : 0u;
     const int64_t col0 = int64_t(rank) * HS;
     const float Hf = float(H);
+    const float inv_h = row_inv_h(H);
     const bool item_units = p.use_plan && T::kLeaves;
     const int64_t per_unit = item_units ? kUnitBatches : 1;
     const int64_t cluster_id = blockIdx.x / K;
@@ -433,10 +434,10 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                         ss = vals[r];
                         gx = vals[R + r];
                     }
-                const float rstd = row_rstd(ss, Hf, p.eps);
+                const float rstd = row_rstd(ss, Hf, inv_h, p.eps);
                 SplitStats st;
                 st.rstd = rstd;
-                st.mg = T::kNeedGx ? row_mean_gxhat(gx, rstd, Hf) : 0.f;
+                st.mg = T::kNeedGx ? row_mean_gxhat(gx, rstd, Hf, inv_h) : 0.f;
                 stats[s * R + lane] = st;
                 if (T::kFwdLike && rank == 0 && p.rstd_out != nullptr && m[lane].off >= 0)
                     p.rstd_out[m[lane].prow] = rstd;
@@ -584,12 +585,15 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
     constexpr int kLogTPW = (TPW == 1) ? 0 : (TPW == 2) ? 1 : (TPW == 4) ? 2 : (TPW == 8) ? 3 : (TPW == 16) ? 4 : 5;
     constexpr int kU = U < kSteps ? U : kSteps;
     static_assert(kSteps % kU == 0, "steps per unit must be a multiple of the prefetch depth");
+    constexpr int kLogU = (kU == 1) ? 0 : (kU == 2) ? 1 : (kU == 4) ? 2 : (kU == 8) ? 3 : (kU == 16) ? 4 : 5;
+    constexpr int kGroupLevel = kLogTPW + kLogU;          // tree level of one group of kU steps
 
     const int lane = threadIdx.x & 31;
     const int team = lane / P2, tl = lane % P2;
     const int H = p.hidden, V = H >> 3;
     const bool has_vec = tl < V;
     const float Hf = float(H);
+    const float inv_h = row_inv_h(H);
     const int64_t gwarp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
 
@@ -615,7 +619,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
             if (r0 < p.n_rows && p.tok_id[r0 / p.rpt] >= 0) pr2.x = int32_t(r0);
             if (r0 + 1 < p.n_rows && p.tok_id[(r0 + 1) / p.rpt] >= 0) pr2.y = int32_t(r0 + 1);
         }
-        TreeStackF2<4, kBlockLevels> tree;
+        TreeStackF2<4, kBlockLevels> tree;                // levels kGroupLevel.. of the 64-leaf tree
 #pragma unroll 1
         for (int st0 = 0; st0 < kSteps; st0 += kU) {
             int64_t off[kU];
@@ -648,55 +652,89 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                     if (kRv > 1) rv[q % kRv] = ld_global_stream_v4(p.res + off[q]);
                 }
             }
+            // phase 1: row sums of the group's steps (two FMA chains, then the team butterfly)
+            float ssv[kU], gxv[kU];
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
-                const bool act = off[q] >= 0;
                 f2_t xf[4], df[4];
                 f2_unpack8(xv[q], xf);
                 f2_unpack8(dv[q], df);
-                uint4 hb = make_uint4(0, 0, 0, 0);
                 if (MODE == kAddFwd) {                              // the row is h = bf16(x + r)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) xf[i] = f2_add(xf[i], df[i]);
-                    hb = f2_pack8(xf);
-                    f2_unpack8(hb, xf);
+                    xv[q] = f2_pack8(xf);                            // h replaces x from here on
+                    f2_unpack8(xv[q], xf);
                 }
-                // row sums: two FMA chains (even / odd columns), then the team butterfly
                 f2_t a2 = 0ull, b2 = 0ull;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) a2 = f2_fma(xf[i], xf[i], a2);
-                float ss = __fadd_rn(f2_lo(a2), f2_hi(a2));
-                float gx = 0.f;
+                ssv[q] = lane_tree(__fadd_rn(f2_lo(a2), f2_hi(a2)), P2);
+                gxv[q] = 0.f;
                 if (T::kNeedGx) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) b2 = f2_fma(f2_mul(df[i], wv[i]), xf[i], b2);
-                    gx = __fadd_rn(f2_lo(b2), f2_hi(b2));
+                    gxv[q] = lane_tree(__fadd_rn(f2_lo(b2), f2_hi(b2)), P2);
                 }
-                ss = lane_tree(ss, P2);
-                if (T::kNeedGx) gx = lane_tree(gx, P2);
-                const float rstd = row_rstd(ss, Hf, p.eps);
+            }
+            // phase 2: rstd and mean(g*xhat) of the group's rows.  Every lane of a
+            // team holds the team's sums; lane tl of the team evaluates step tl % kU
+            // and the results are fetched back by shuffles, so the scalar sequence
+            // runs once per group instead of once per step.
+            float rsv[kU], mgv[kU];
+            if (P2 >= kU) {
+                const int qs = tl % kU;
+                float ss = ssv[0], gx = gxv[0];
+#pragma unroll
+                for (int q = 1; q < kU; ++q) {
+                    ss = (qs == q) ? ssv[q] : ss;
+                    gx = (qs == q) ? gxv[q] : gx;
+                }
+                const float r = row_rstd(ss, Hf, inv_h, p.eps);
+                const float m = T::kNeedGx ? row_mean_gxhat(gx, r, Hf, inv_h) : 0.f;
+#pragma unroll
+                for (int q = 0; q < kU; ++q) {
+                    rsv[q] = __shfl_sync(kFull, r, team * P2 + q);
+                    mgv[q] = T::kNeedGx ? __shfl_sync(kFull, m, team * P2 + q) : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < kU; ++q) {
+                    rsv[q] = row_rstd(ssv[q], Hf, inv_h, p.eps);
+                    mgv[q] = T::kNeedGx ? row_mean_gxhat(gxv[q], rsv[q], Hf, inv_h) : 0.f;
+                }
+            }
+            // phase 3: outputs and leaves; the group's steps form a subtree of the
+            // 64-leaf tree with static positions, pushed once per group
+            TreeStackF2<4, (kLogU > 0 ? kLogU : 1)> mini;
+            f2_t node[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const bool act = off[q] >= 0;
+                const float rstd = rsv[q];
                 f2_t leaf[4] = {0ull, 0ull, 0ull, 0ull};
                 if (act && has_vec) {
                     const f2_t r2 = f2_make(rstd, rstd);
-                    f2_t xh[4], o[4];
+                    f2_t xf[4], xh[4], o[4];
+                    f2_unpack8_v(xv[q], xf);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) xh[i] = f2_mul(xf[i], r2);
                     if (T::kFwdLike) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) o[i] = f2_mul(xh[i], wv[i]);
                         st_global_v4(p.out + off[q], f2_pack8(o));
-                        if (MODE == kAddFwd) st_global_v4(p.out2 + off[q], hb);
+                        if (MODE == kAddFwd) st_global_v4(p.out2 + off[q], xv[q]);
                     } else {
+                        f2_t df[4];
+                        f2_unpack8_v(dv[q], df);
                         if (T::kNeedGx && p.out != nullptr) {
-                            const float mg = row_mean_gxhat(gx, rstd, Hf);
-                            const f2_t nm2 = f2_make(-mg, -mg);
+                            const f2_t nm2 = f2_make(-mgv[q], -mgv[q]);
                             const float rs = __fmul_rn(rstd, p.grad_scale);    // == rstd when unscaled
                             const f2_t rs2 = f2_make(rs, rs);
 #pragma unroll
                             for (int i = 0; i < 4; ++i) o[i] = f2_mul(rs2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
                             if (kRv > 1) {
                                 f2_t rf[4];
-                                f2_unpack8(rv[q % kRv], rf);
+                                f2_unpack8_v(rv[q % kRv], rf);
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) o[i] = f2_add(o[i], rf[i]);
                             }
@@ -716,16 +754,22 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                         for (int kk = P2; kk < 32; kk <<= 1)
 #pragma unroll
                             for (int i = 0; i < 4; ++i) leaf[i] = f2_add(leaf[i], shfl_xor_f2(leaf[i], kk));
-                        tree.template push_dyn<kLogTPW>(leaf, st0 + q);
-                        if (st0 + q == kSteps - 1) {
-                            if (team == 0 && has_vec)
-                                st_global_f2x4(p.ws.block_partial + int64_t(block) * 4 * H + tl * 8, leaf);
-                            if (lane == 0) mark_whole_block(p.ws, block);
+                        if (kLogU > 0) mini.template push_static<0>(leaf, q);
+                        if (q == kU - 1) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) node[i] = leaf[i];   // the group's subtree
                         }
                     } else if (kind == 1 && act) {
                         if (has_vec) st_global_f2x4(p.ws.spill + int64_t(lrow[q]) * H + tl * 8, leaf);
                         if (tl == 0) mark_spilled_row(p.ws, lrow[q]);
                     }
+                }
+            }
+            if (T::kLeaves && kind == 0) {
+                if (kGroupLevel < kBlockLevels) tree.template push_dyn<kGroupLevel>(node, st0 / kU);
+                if (st0 + kU == kSteps) {                    // node is the block partial
+                    if (team == 0 && has_vec) st_global_f2x4(p.ws.block_partial + int64_t(block) * 4 * H + tl * 8, node);
+                    if (lane == 0) mark_whole_block(p.ws, block);
                 }
             }
         }
