@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
+    ap.add_argument("--e2e-chunk", type=int, default=4096, help="token slots per sub-call of the e2e leg")
+    ap.add_argument("--e2e-lanes", type=int, default=1, help="copy streams per direction in the e2e leg")
     ap.add_argument("--chain", action="store_true",
                     help="residual add + norm forward and its backward with the residual gradient and the "
                          "loss seed's 1/D (D = active tokens of the multiset); no e2e or CPU legs")
@@ -355,55 +357,98 @@ def time_bwd_kernel(step_objs, stream, reps, flush):
     return [a.elapsed_time(b) for a, b in per]
 
 
-def e2e_steps(wl, lay, x_log_host, dy_log_host, w, rpt, steps, warmup, device):
-    """Public API with host buffers: per step, build plans, copy inputs in from pinned
-    memory, run, copy y/dx/dweight back.  Returns (ms per step, h2d bytes, d2h bytes)."""
+def e2e_steps(wl, lay, x_log_host, dy_log_host, w, rpt, steps, warmup, device, chunk_tokens=4096, copy_lanes=1):
+    """Public API with host buffers.  Per step: build the plans on the host, copy token
+    ids, plans and inputs in from pinned memory, run forward, backward and finalize,
+    copy y, dx and dweight back.  Every call of the layout is cut into sub-calls of at
+    most `chunk_tokens` token slots (the outputs do not depend on the physical layout),
+    and the sub-calls are pipelined: copy-in streams, the compute stream, copy-out
+    streams (`copy_lanes` of each, so that several copy engines work at once).
+    Returns (ms per step, h2d bytes, d2h bytes, description)."""
     import torch
     import invariant_rmsnorm_fwd_gb300 as rb
     H = wl.hidden
-    stream = torch.cuda.current_stream()
-    # pinned physical host buffers per call (the caller's own data, laid out physically)
-    host = []
+    comp = torch.cuda.current_stream()
+    s_ins = [torch.cuda.Stream(device=device) for _ in range(copy_lanes)]
+    s_outs = [torch.cuda.Stream(device=device) for _ in range(copy_lanes)]
+    subs = []
     for tok in lay.calls:
+        for i in range(0, max(tok.size, 1), chunk_tokens):
+            t = tok[i:i + chunk_tokens]
+            if t.size and (t >= 0).any():
+                subs.append(np.ascontiguousarray(t, dtype=np.int32))
+    # the caller's pinned host data, laid out physically per sub-call
+    host = []
+    for tok in subs:
         act = tok >= 0
         xh = torch.zeros((tok.size, rpt, H), dtype=torch.bfloat16).pin_memory()
         dh = torch.zeros_like(xh).pin_memory()
         idx = torch.as_tensor(tok[act]).long()
         xh[torch.as_tensor(act)] = x_log_host[idx]
         dh[torch.as_tensor(act)] = dy_log_host[idx]
-        host.append((tok, xh, dh, torch.empty_like(xh).pin_memory(), torch.empty_like(xh).pin_memory()))
-    dev = [(torch.empty(xh.shape, dtype=torch.bfloat16, device=device),
-            torch.empty(xh.shape, dtype=torch.bfloat16, device=device),
-            torch.empty(xh.shape, dtype=torch.bfloat16, device=device),
-            torch.empty(xh.shape, dtype=torch.bfloat16, device=device)) for _, xh, _, _, _ in host]
+        host.append((xh, dh, torch.empty_like(xh).pin_memory(), torch.empty_like(xh).pin_memory()))
+    dev = [tuple(torch.empty(xh.shape, dtype=torch.bfloat16, device=device) for _ in range(4))
+           for xh, _, _, _ in host]
+    # token ids and plans: pinned staging and device copies, sized for the largest sub-call
+    cap = [max(int(np.ceil(t.size * rpt / 64)) * 2 + 2, 1) * rb.PLAN_ITEM_BYTES for t in subs]
+    meta_h = [(torch.empty(t.size, dtype=torch.int32).pin_memory(), torch.empty(c, dtype=torch.uint8).pin_memory())
+              for t, c in zip(subs, cap)]
+    meta_d = [(torch.empty(t.size, dtype=torch.int32, device=device), torch.empty(c, dtype=torch.uint8, device=device))
+              for t, c in zip(subs, cap)]
     ws = rb.DweightWorkspace(wl.n_tokens * rpt, H, device=device)
     dw_d = torch.empty(H, dtype=torch.float32, device=device)
     dw_h = torch.empty(H, dtype=torch.float32).pin_memory()
-    h2d = d2h = 0
+    counts = {}
 
     def one():
-        nonlocal h2d, d2h
         h2d = d2h = 0
         cls = []
-        for (tok, xh, dh, yh, dxh), (xd, dd, yd, dxd) in zip(host, dev):
-            cl = rb.call_layout(tok, rpt, lay.n_logical_tokens, device=device)
-            h2d += tok.nbytes + (cl.plan.numel() if cl.plan is not None else 0)
-            xd.copy_(xh, non_blocking=True)
-            dd.copy_(dh, non_blocking=True)
-            h2d += xh.numel() * 2 * 2
-            rb.rmsnorm_fwd(xd, w, cl, wl.eps, y=yd, stream=stream)
-            cls.append(cl)
-        ws.begin(stream)
-        for cl, (tok, xh, dh, yh, dxh), (xd, dd, yd, dxd) in zip(cls, host, dev):
-            rb.rmsnorm_bwd_dx(xd, w, dd, cl, wl.eps, dx=dxd, workspace=ws, stream=stream)
-        ws.finalize(dw_d, stream)
-        for (tok, xh, dh, yh, dxh), (xd, dd, yd, dxd) in zip(host, dev):
-            yh.copy_(yd, non_blocking=True)
-            dxh.copy_(dxd, non_blocking=True)
-            d2h += yd.numel() * 2 * 2
-        dw_h.copy_(dw_d, non_blocking=True)
-        d2h += H * 4
+        for tok, (th, ph), (td, pd) in zip(subs, meta_h, meta_d):
+            pbytes, items, whole, spill = rb.plan_build(tok, rpt, lay.n_logical_tokens)
+            th.numpy()[:] = tok
+            ph.numpy()[:pbytes.size] = pbytes
+            cls.append(rb.CallLayout(td, pd, items, tok.size, rpt, lay.n_logical_tokens, whole, spill))
+            h2d += tok.nbytes + pbytes.size
+        ready = []
+        for i, ((th, ph), (td, pd), (xh, dh, _, _), (xd, dd, _, _)) in enumerate(zip(meta_h, meta_d, host, dev)):
+            s_in = s_ins[i % copy_lanes]
+            with torch.cuda.stream(s_in):
+                td.copy_(th, non_blocking=True)
+                pd.copy_(ph, non_blocking=True)
+                xd.copy_(xh, non_blocking=True)
+                dd.copy_(dh, non_blocking=True)
+                h2d += xh.numel() * 2 * 2
+                e = torch.cuda.Event()
+                e.record(s_in)
+                ready.append(e)
+        ws.begin(comp)
+        done = []
+        for cl, e, (xd, dd, yd, dxd) in zip(cls, ready, dev):
+            comp.wait_event(e)
+            rb.rmsnorm_fwd(xd, w, cl, wl.eps, y=yd, stream=comp)
+            e1 = torch.cuda.Event()
+            e1.record(comp)                        # y can leave while the backward runs
+            rb.rmsnorm_bwd_dx(xd, w, dd, cl, wl.eps, dx=dxd, workspace=ws, stream=comp)
+            e2 = torch.cuda.Event()
+            e2.record(comp)
+            done.append((e1, e2))
+        ws.finalize(dw_d, comp)
+        fin = torch.cuda.Event()
+        fin.record(comp)
+        for i, ((e1, e2), (_, _, yh, dxh), (_, _, yd, dxd)) in enumerate(zip(done, host, dev)):
+            s_out = s_outs[i % copy_lanes]
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(e1)
+                yh.copy_(yd, non_blocking=True)
+                s_out.wait_event(e2)
+                dxh.copy_(dxd, non_blocking=True)
+                d2h += yd.numel() * 2 * 2
+        with torch.cuda.stream(s_outs[0]):
+            s_outs[0].wait_event(fin)
+            dw_h.copy_(dw_d, non_blocking=True)
+            d2h += H * 4
         torch.cuda.synchronize()
+        counts["h2d"], counts["d2h"] = h2d, d2h
 
     for _ in range(warmup):
         one()
@@ -412,7 +457,9 @@ def e2e_steps(wl, lay, x_log_host, dy_log_host, w, rpt, steps, warmup, device):
         t0 = time.perf_counter()
         one()
         ts.append((time.perf_counter() - t0) * 1e3)
-    return statistics.median(ts), h2d, d2h
+    desc = (f"{len(subs)} sub-calls of <= {chunk_tokens} token slots, pipelined over {copy_lanes} copy-in "
+            f"streams, the compute stream and {copy_lanes} copy-out streams; plans built on the host every step")
+    return statistics.median(ts), counts["h2d"], counts["d2h"], desc
 
 
 def cpu_baseline(wl, x_log, dy_log, w, rpt, seconds):
@@ -612,14 +659,17 @@ def main():
         x_h = [d[1].cpu() for d in steps_data]
         dy_h = [d[2].cpu() for d in steps_data]
         tot_ms, tot_in, tot_out = 0.0, 0, 0
+        desc = ""
         for (rpt, x, dy, w), xh, dh in zip(steps_data, x_h, dy_h):
-            e_ms, bi, bo = e2e_steps(wl, lay, xh, dh, w, rpt, max(3, args.steps // 4), 2, device)
+            e_ms, bi, bo, desc = e2e_steps(wl, lay, xh, dh, w, rpt, max(3, args.steps // 4), 2, device,
+                                           args.e2e_chunk, args.e2e_lanes)
             tot_ms += e_ms
             tot_in += bi
             tot_out += bo
         line["e2e"] = {"value": round(n_act / (tot_ms * 1e-3) * world, 1), "unit": "tokens/s",
                        "h2d_bytes_per_step": int(tot_in), "d2h_bytes_per_step": int(tot_out),
-                       "ms_per_step": round(tot_ms, 3)}
+                       "ms_per_step": round(tot_ms, 3), "pipeline": desc,
+                       "link_gbs": round((tot_in + tot_out) / (tot_ms * 1e-3) / 1e9, 1)}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.chain:
         rpt, x, dy, w = steps_data[0][:4]
