@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
+    ap.add_argument("--max-tokens", type=int, default=0,
+                    help="cut the workload to its first N logical tokens (profiling runs only)")
     ap.add_argument("--e2e-chunk", type=int, default=4096, help="token slots per sub-call of the e2e leg")
     ap.add_argument("--e2e-lanes", type=int, default=1, help="copy streams per direction in the e2e leg")
     ap.add_argument("--chain", action="store_true",
@@ -510,6 +512,8 @@ def main():
         dist = tdist
 
     wl = synth.config(args.config)
+    if args.max_tokens:
+        wl = synth.truncated(wl, args.max_tokens)
     lay_name = args.layout or wl.headline
     rpt_list = list(wl.heads)
     hbm_peak, peak_kind = measured_peaks()

@@ -15,6 +15,7 @@ normals come from the Box-Muller transform in float64.
 from __future__ import annotations
 
 import math
+import dataclasses
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -161,6 +162,19 @@ class Workload:
     @property
     def n_tokens(self) -> int:
         return int(np.sum(self.lengths))
+
+
+def truncated(wl: Workload, max_tokens: int) -> Workload:
+    """The same workload cut to its first max_tokens logical tokens (samples in
+    sample_id order, the last one shortened); values are unchanged because they
+    are keyed by logical id.  Used for profiling runs of a smaller size."""
+    out, left = [], int(max_tokens)
+    for n in wl.lengths:
+        if left <= 0:
+            break
+        out.append(min(int(n), left))
+        left -= out[-1]
+    return dataclasses.replace(wl, name=f"{wl.name}[:{int(max_tokens)}]", lengths=np.asarray(out, dtype=np.int64))
 
 
 def config(name: str, seed: int = 0) -> Workload:
