@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
+    ap.add_argument("--streams", type=int, default=8, help="streams the calls of a multi-call layout fork over")
     ap.add_argument("--max-tokens", type=int, default=0,
                     help="cut the workload to its first N logical tokens (profiling runs only)")
     ap.add_argument("--e2e-chunk", type=int, default=4096, help="token slots per sub-call of the e2e leg")
@@ -195,7 +196,7 @@ class Step:
     With `chain`, the step is the residual add + norm forward and the backward
     with the residual gradient, scaled by the loss seed's 1/D."""
 
-    def __init__(self, wl, lay, x_log, dy_log, w, rpt, device, r_log=None, dres_log=None):
+    def __init__(self, wl, lay, x_log, dy_log, w, rpt, device, r_log=None, dres_log=None, n_streams=8):
         import torch
         import invariant_rmsnorm_fwd_gb300 as rb
         self.rb = rb
@@ -223,6 +224,7 @@ class Step:
         self.ws = rb.DweightWorkspace(wl.n_tokens * rpt, H, device=device)
         self.dw = torch.empty(H, dtype=torch.float32, device=device)
         self.n_active = wl.n_tokens
+        self.n_streams = n_streams
         self.bwd_events = []
 
     def fwd_call(self, c, st):
@@ -243,7 +245,7 @@ class Step:
 
     def run(self, stream):
         """Calls of a multi-call layout are independent (they touch disjoint rows and
-        blocks of the workspace), so they are spread over up to four streams that
+        blocks of the workspace), so they are spread over n_streams streams (8 by default) that
         fork from and join back into `stream`; one-call layouts stay on `stream`."""
         import torch
         rb = self.rb
@@ -276,7 +278,7 @@ class Step:
         if len(self.calls) == 1:
             return [stream]
         if getattr(self, "_side", None) is None:
-            self._side = [torch.cuda.Stream(device=self.dw.device) for _ in range(4)]
+            self._side = [torch.cuda.Stream(device=self.dw.device) for _ in range(self.n_streams)]
         return self._side
 
     def time_fwd_only(self, stream):
@@ -534,7 +536,8 @@ def main():
         steps_data.append((rpt, x, dy, w) + extra)
 
     def make_steps(layout_):
-        return [Step(wl, layout_, d[1], d[2], d[3], d[0], device, *d[4:]) for d in steps_data]
+        return [Step(wl, layout_, d[1], d[2], d[3], d[0], device, *d[4:], n_streams=args.streams)
+                for d in steps_data]
 
     lays = L.workload_layouts(wl, kinds=[lay_name])
     lay = lays[lay_name]

@@ -100,17 +100,22 @@ template <int MODE, int P2>
 int launch_small(const KParams &p, const DeviceInfo &d, cudaStream_t stream) {
     // warp steps loaded together (fewer when three tensors or the leaf tree hold registers)
     using T = ModeTraits<MODE>;
-    constexpr int U = (T::kLeaves && T::kTensors >= 3) ? 2 : T::kNeedDy ? 4 : 8;
+    constexpr int U = (T::kLeaves && T::kTensors >= 3) ? 2 : T::kTensors >= 2 ? 4 : 8;
+    constexpr int kSteps = kBlockRows / (32 / P2);
+    constexpr int kU = U < kSteps ? U : kSteps;
+    constexpr int smem = kSmallWarps * small_warp_bytes(kU, T::kTensors, kSteps / kU);
     constexpr int threads = kSmallWarps * 32;
     auto kern = small_row_kernel<MODE, P2, U>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
         return RMSNORM_ERR_CUDA;
     int64_t blocks = int64_t(per_sm) * d.sms;
     const int64_t need = (p.n_units + kSmallWarps - 1) / kSmallWarps;   // one unit per warp at least
     if (blocks > need) blocks = need;
     if (blocks < 1) return RMSNORM_OK;
-    kern<<<unsigned(blocks), threads, 0, stream>>>(p);
+    kern<<<unsigned(blocks), threads, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
     count_launch();
     return RMSNORM_OK;

@@ -571,12 +571,28 @@ __device__ __forceinline__ f2_t shfl_xor_f2(f2_t v, int k) {
 }
 
 constexpr int kSmallWarps = 8;                          // warps per CTA
+constexpr int kSmallTable = 64 * 16 + 16;               // one unit's slot table (off, lrow, prow), then its header
 
-// Small hidden sizes: each warp works through its units in groups of U warp
-// steps; the 16-byte loads of a group are issued together into registers, then
-// the U steps are computed as independent chains (so they overlap).  The slot
-// metadata of a unit is fetched once by the whole warp (lane l holds slots
-// 2l, 2l+1) and handed out by shuffles.
+// Shared memory of one warp of small_row_kernel: two unit tables, then a
+// ring of (D + 1) group buffers of kU warp steps x kT tensors x 512 bytes;
+// three buffers when they fit in 12 KB (two CTAs of eight warps per SM).
+__host__ __device__ constexpr int small_ring_depth(int groups, int group_bytes) {
+    return (groups > 2 && 3 * group_bytes <= 12288) ? 3 : (groups < 2 ? groups : 2);
+}
+__host__ __device__ constexpr int small_warp_bytes(int kU, int kT, int groups) {
+    return 2 * kSmallTable + small_ring_depth(groups, kU * kT * 512) * kU * kT * 512;
+}
+
+// Small hidden sizes: each warp works through its units (64 row slots) in
+// groups of kU warp steps.  The rows of a group are copied into a per-warp
+// shared-memory ring with 16-byte cp.async, D = depth - 1 groups ahead of the
+// group being computed, so the bytes in flight are not bounded by registers.
+// Each lane copies and later reads only its own 16-byte pieces, so the ring
+// needs no barrier; the slot table of a unit (row offset, logical and
+// physical row of each slot) is written once per unit by the warp and read
+// by broadcast.  Per group: (1) row sums of the kU steps, (2) rstd and
+// mean(g*xhat) once per row, (3) outputs and leaves, the group's steps
+// folded into a subtree with static positions.
 template <int MODE, int P2, int U>
 __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KParams p) {
     using T = ModeTraits<MODE>;
@@ -587,8 +603,16 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
     static_assert(kSteps % kU == 0, "steps per unit must be a multiple of the prefetch depth");
     constexpr int kLogU = (kU == 1) ? 0 : (kU == 2) ? 1 : (kU == 4) ? 2 : (kU == 8) ? 3 : (kU == 16) ? 4 : 5;
     constexpr int kGroupLevel = kLogTPW + kLogU;          // tree level of one group of kU steps
+    constexpr int kT = T::kTensors;
+    constexpr int kGroups = kSteps / kU;
+    constexpr int kDepth = small_ring_depth(kGroups, kU * kT * 512);
+    constexpr int kAhead = kDepth - 1;                   // groups issued ahead of the one computed
+    constexpr int kGroupBytes = kU * kT * 512;
 
+    extern __shared__ __align__(16) uint8_t small_smem[];
     const int lane = threadIdx.x & 31;
+    uint8_t *wbase = small_smem + (threadIdx.x >> 5) * small_warp_bytes(kU, kT, kGroups);
+    uint8_t *ring = wbase + 2 * kSmallTable;
     const int team = lane / P2, tl = lane % P2;
     const int H = p.hidden, V = H >> 3;
     const bool has_vec = tl < V;
@@ -596,32 +620,117 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
     const float inv_h = row_inv_h(H);
     const int64_t gwarp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int64_t my_units = p.n_units > gwarp ? (p.n_units - gwarp + nwarps - 1) / nwarps : 0;
+    const int64_t total = my_units * kGroups;
 
     f2_t wv[4] = {0ull, 0ull, 0ull, 0ull};
     if (MODE != kDw && has_vec) f2_unpack8(*reinterpret_cast<const uint4 *>(p.w + tl * 8), wv);
 
-#pragma unroll 1
-    for (int64_t u = gwarp; u < p.n_units; u += nwarps) {
-        int2 pr2 = make_int2(-1, -1), lr2 = make_int2(-1, -1);
-        int32_t kind = 0, block = -1;
+    // unit tables: entry = (row offset + tl * 8 of the lane's columns is added
+    // by the reader; -1 = inactive), logical row, physical row; plus the item
+    // header (kind, block) after the 64 entries
+    struct SlotEntry {
+        int64_t off;
+        int32_t lrow, prow;
+    };
+    auto table = [&](int64_t ord) { return reinterpret_cast<SlotEntry *>(wbase + int(ord & 1) * kSmallTable); };
+    int2 hdr_next = make_int2(0, -1);
+    int2 pr_next = make_int2(-1, -1), lr_next = make_int2(-1, -1);
+    // slot metadata of unit `ord` (lane l: slots 2l, 2l+1) into registers
+    auto fetch_unit = [&](int64_t ord, int2 &pr2, int2 &lr2, int2 &hd) {
+        pr2 = make_int2(-1, -1);
+        lr2 = make_int2(-1, -1);
+        hd = make_int2(0, -1);
+        if (ord >= my_units) return;
+        const int64_t u = gwarp + ord * nwarps;
         if (p.use_plan) {
             const PlanItem *it = p.items + u;
             pr2 = reinterpret_cast<const int2 *>(it->prow)[lane];
             lr2 = reinterpret_cast<const int2 *>(it->lrow)[lane];
-            kind = it->kind;
-            block = it->block;
-            if (T::kLeaves && ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1))) {
-                if (lane == 0) set_status(p.ws.hdr, kStPlan);
-                kind = 2;                                  // malformed item: contributes nothing
-            }
+            hd = make_int2(it->kind, it->block);
         } else {
             const int64_t r0 = u * kBlockRows + 2 * lane;
             if (r0 < p.n_rows && p.tok_id[r0 / p.rpt] >= 0) pr2.x = int32_t(r0);
             if (r0 + 1 < p.n_rows && p.tok_id[(r0 + 1) / p.rpt] >= 0) pr2.y = int32_t(r0 + 1);
         }
-        TreeStackF2<4, kBlockLevels> tree;                // levels kGroupLevel.. of the 64-leaf tree
+    };
+    int64_t issue_ord = -1;
+    auto issue = [&](int64_t gi) {
+        if (gi < total) {
+            const int64_t ord = gi / kGroups;
+            const int gg = int(gi % kGroups);
+            if (ord != issue_ord) {                      // entering a unit: its table, the next one's metadata
+                int2 pr2, lr2, hd;
+                if (ord == issue_ord + 1 && issue_ord >= 0) {
+                    pr2 = pr_next;
+                    lr2 = lr_next;
+                    hd = hdr_next;
+                } else {
+                    fetch_unit(ord, pr2, lr2, hd);
+                }
+                __syncwarp();                            // readers of the table being replaced are done
+                SlotEntry *tb = table(ord);
+                int32_t prs[2] = {pr2.x, pr2.y}, lrs[2] = {lr2.x, lr2.y};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int32_t pr = prs[h], lr = lrs[h];
+                    bool act = pr >= 0;
+                    if (act && (pr >= p.n_rows || (T::kLeaves && (lr < 0 || lr >= p.ws.n_rows)))) {
+                        if (T::kLeaves) set_status(p.ws.hdr, kStPlan);
+                        act = false;
+                    }
+                    SlotEntry e;
+                    e.off = act ? row_offset(p, pr) : -1;
+                    e.lrow = lr;
+                    e.prow = pr;
+                    tb[2 * lane + h] = e;
+                }
+                if (lane == 0) *reinterpret_cast<int2 *>(reinterpret_cast<uint8_t *>(tb) + 64 * 16) = hd;
+                issue_ord = ord;
+                fetch_unit(ord + 1, pr_next, lr_next, hdr_next);
+                __syncwarp();
+            }
+            const SlotEntry *tb = table(ord);
+            uint8_t *buf = ring + int(gi % kDepth) * kGroupBytes;
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const int slot = (gg * kU + q) * TPW + team;
+                const int64_t off = tb[slot].off;
+                if (off >= 0 && has_vec) {
+                    cp_async_16(buf + (q * kT + 0) * 512 + lane * 16, p.x + off + tl * 8);
+                    if (T::kNeedDy) cp_async_16(buf + (q * kT + 1) * 512 + lane * 16, p.dy + off + tl * 8);
+                    if (T::kRes) cp_async_16(buf + (q * kT + T::kResSlot) * 512 + lane * 16, p.res + off + tl * 8);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
+    for (int a = 0; a < kAhead; ++a) issue(a);
+    TreeStackF2<4, kBlockLevels> tree;                // levels kGroupLevel.. of the 64-leaf tree
+    int32_t kind = 0, block = -1;
 #pragma unroll 1
-        for (int st0 = 0; st0 < kSteps; st0 += kU) {
+    for (int64_t gi = 0; gi < total; ++gi) {
+        __syncwarp();                                // every lane is done with the buffer reused next
+        issue(gi + kAhead);
+        cp_async_wait<kAhead>();                     // this lane's copies of group gi have landed
+        const int64_t ord = gi / kGroups;
+        const int st0 = int(gi % kGroups) * kU;
+        const SlotEntry *tb = table(ord);
+        const uint8_t *buf = ring + int(gi % kDepth) * kGroupBytes;
+        if (st0 == 0) {
+            // the header of the unit being computed: the issue side may have
+            // moved on to the next unit already (D < kGroups), so it is kept
+            // with the table
+            const int2 hd = *reinterpret_cast<const int2 *>(reinterpret_cast<const uint8_t *>(tb) + 64 * 16);
+            kind = hd.x;
+            block = hd.y;
+            if (T::kLeaves && ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1))) {
+                if (lane == 0) set_status(p.ws.hdr, kStPlan);
+                kind = 2;                                  // malformed item: contributes nothing
+            }
+        }
+        {
             int64_t off[kU];
             int32_t lrow[kU], prow[kU];
             uint4 xv[kU], dv[kU];
@@ -629,27 +738,17 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
             uint4 rv[kRv];
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
-                const int slot = (st0 + q) * TPW + team;
-                const int px = __shfl_sync(kFull, pr2.x, slot >> 1), py = __shfl_sync(kFull, pr2.y, slot >> 1);
-                const int lx = __shfl_sync(kFull, lr2.x, slot >> 1), ly = __shfl_sync(kFull, lr2.y, slot >> 1);
-                int32_t pr = (slot & 1) ? py : px;
-                const int32_t lr = (slot & 1) ? ly : lx;
-                bool act = pr >= 0;
-                if (act && (pr >= p.n_rows || (T::kLeaves && (lr < 0 || lr >= p.ws.n_rows)))) {
-                    if (T::kLeaves && tl == 0) set_status(p.ws.hdr, kStPlan);
-                    act = false;
-                }
-                off[q] = act ? row_offset(p, pr) + tl * 8 : -1;
-                lrow[q] = lr;
-                prow[q] = pr;
+                const SlotEntry e = tb[(st0 + q) * TPW + team];
+                off[q] = e.off >= 0 ? e.off + tl * 8 : -1;
+                lrow[q] = e.lrow;
+                prow[q] = e.prow;
                 xv[q] = make_uint4(0, 0, 0, 0);
                 dv[q] = make_uint4(0, 0, 0, 0);
                 if (kRv > 1) rv[q % kRv] = make_uint4(0, 0, 0, 0);
-                if (act && has_vec) {
-                    xv[q] = ld_global_stream_v4(p.x + off[q]);
-                    if (T::kNeedDy) dv[q] = ld_global_stream_v4(p.dy + off[q]);
-                    if (MODE == kAddFwd) dv[q] = ld_global_stream_v4(p.res + off[q]);   // r rides in dv
-                    if (kRv > 1) rv[q % kRv] = ld_global_stream_v4(p.res + off[q]);
+                if (e.off >= 0 && has_vec) {
+                    xv[q] = ld_shared_v4(buf + (q * kT + 0) * 512 + lane * 16);
+                    if (T::kNeedDy || MODE == kAddFwd) dv[q] = ld_shared_v4(buf + (q * kT + 1) * 512 + lane * 16);
+                    if (kRv > 1) rv[q % kRv] = ld_shared_v4(buf + (q * kT + T::kResSlot) * 512 + lane * 16);
                 }
             }
             // phase 1: row sums of the group's steps (two FMA chains, then the team butterfly)
@@ -774,6 +873,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
             }
         }
     }
+    cp_async_wait<0>();
 }
 
 }  // namespace rbi
