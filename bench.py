@@ -544,12 +544,28 @@ def main():
     step_objs = make_steps(lay)
 
     class Multi:
+        """The normed tensors of one step (Q and K of a per-head norm) are
+        independent ops with their own weights and workspaces: they fork onto
+        their own streams and join back, as a model issues them."""
+
         def __init__(self, steps):
             self.steps = steps
+            self.side = [torch.cuda.Stream(device=device) for _ in steps[1:]]
 
         def run(self, stream):
-            for s in self.steps:
-                s.run(stream)
+            if len(self.steps) == 1:
+                self.steps[0].run(stream)
+                return
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            for st, s in zip(self.side, self.steps[1:]):
+                st.wait_event(ev)
+                s.run(st)
+            self.steps[0].run(stream)
+            for st in self.side:
+                e = torch.cuda.Event()
+                e.record(st)
+                stream.wait_event(e)
 
     multi = Multi(step_objs)
     # kernels of one step (counted on an eager step)

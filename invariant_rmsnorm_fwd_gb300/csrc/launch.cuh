@@ -98,9 +98,11 @@ int launch_split(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStr
 
 template <int MODE, int P2>
 int launch_small(const KParams &p, const DeviceInfo &d, cudaStream_t stream) {
-    // warp steps loaded together (fewer when three tensors or the leaf tree hold registers)
+    // warp steps per group: the fused backward keeps the leaf trees in
+    // registers, and two steps per group avoid spills (measured faster than
+    // four at hidden 128); two-tensor modes take four, the forward eight
     using T = ModeTraits<MODE>;
-    constexpr int U = (T::kLeaves && T::kTensors >= 3) ? 2 : T::kTensors >= 2 ? 4 : 8;
+    constexpr int U = (T::kLeaves && (T::kTensors >= 3 || MODE == kDxDw)) ? 2 : T::kTensors >= 2 ? 4 : 8;
     constexpr int kSteps = kBlockRows / (32 / P2);
     constexpr int kU = U < kSteps ? U : kSteps;
     constexpr int smem = kSmallWarps * small_warp_bytes(kU, T::kTensors, kSteps / kU);

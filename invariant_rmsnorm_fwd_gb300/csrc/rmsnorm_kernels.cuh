@@ -751,8 +751,15 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                     if (kRv > 1) rv[q % kRv] = ld_shared_v4(buf + (q * kT + T::kResSlot) * 512 + lane * 16);
                 }
             }
-            // phase 1: row sums of the group's steps (two FMA chains, then the team butterfly)
-            float ssv[kU], gxv[kU];
+            // phase 1: the lane partials of every row sum of the group (two FMA
+            // chains per 8-column vector); values 0..kU-1 are the sums of squares
+            // of the kU steps, kU..2kU-1 the sums of g*x
+            constexpr int kNV = kU * (T::kNeedGx ? 2 : 1);
+            constexpr int kLogNV = (kNV == 1) ? 0 : (kNV == 2) ? 1 : (kNV == 4) ? 2 : (kNV == 8) ? 3 : (kNV == 16) ? 4 : 5;
+            constexpr int kLogP2 = 5 - kLogTPW;
+            constexpr int kHalvings = kLogNV < kLogP2 ? kLogNV : kLogP2;
+            constexpr int kCnt = kNV >> kHalvings;       // values a lane holds after the reduction
+            float vals[kNV];
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
                 f2_t xf[4], df[4];
@@ -767,39 +774,70 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                 f2_t a2 = 0ull, b2 = 0ull;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) a2 = f2_fma(xf[i], xf[i], a2);
-                ssv[q] = lane_tree(__fadd_rn(f2_lo(a2), f2_hi(a2)), P2);
-                gxv[q] = 0.f;
+                vals[q] = __fadd_rn(f2_lo(a2), f2_hi(a2));
                 if (T::kNeedGx) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) b2 = f2_fma(f2_mul(df[i], wv[i]), xf[i], b2);
-                    gxv[q] = lane_tree(__fadd_rn(f2_lo(b2), f2_hi(b2)), P2);
+                    vals[kU + q] = __fadd_rn(f2_lo(b2), f2_hi(b2));
                 }
             }
-            // phase 2: rstd and mean(g*xhat) of the group's rows.  Every lane of a
-            // team holds the team's sums; lane tl of the team evaluates step tl % kU
-            // and the results are fetched back by shuffles, so the scalar sequence
-            // runs once per group instead of once per step.
+            // the team tree over the P2 lanes (lanes 1 apart first, then 2, 4, ...)
+            // as a transposing reduction: at distance d a lane keeps half of its
+            // values and adds its partner's copy of them, so every value is still
+            // the sum over the same lane pairs (addition is commutative) but the
+            // kNV trees cost kNV - 1 exchanges instead of kNV * log2(P2)
+#pragma unroll
+            for (int lv = 0; lv < kLogP2; ++lv) {
+                const int d = 1 << lv;
+                if (lv < kHalvings) {
+                    constexpr int kMaxHalf = kNV / 2;
+                    const int half = kNV >> (lv + 1);
+                    const bool upper = (lane & d) != 0;
+#pragma unroll
+                    for (int jj = 0; jj < kMaxHalf; ++jj) {
+                        if (jj < half) {
+                            const float send = upper ? vals[jj] : vals[jj + half];
+                            const float keep = upper ? vals[jj + half] : vals[jj];
+                            vals[jj] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, d));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < kCnt; ++jj) vals[jj] = __fadd_rn(vals[jj], __shfl_xor_sync(kFull, vals[jj], d));
+                }
+            }
+            // value index held in vals[jj]: (lane bits of the halvings, highest
+            // weight at distance 1) + jj
+            auto holder = [&](int idx) {                   // team lane holding value idx
+                int l = 0;
+#pragma unroll
+                for (int lv = 0; lv < kHalvings; ++lv) l |= ((idx >> (kLogNV - 1 - lv)) & 1) << lv;
+                return team * P2 + l;
+            };
+            // phase 2: rstd and mean(g*xhat), once per row: each lane evaluates the
+            // values it holds; a lane holding g*x of step q takes rstd of step q
+            // from the lane (or register) holding its sum of squares
+            float rloc[kCnt], mloc[kCnt];
+#pragma unroll
+            for (int jj = 0; jj < kCnt; ++jj) rloc[jj] = row_rstd(vals[jj], Hf, inv_h, p.eps);
+            if (T::kNeedGx) {
+#pragma unroll
+                for (int jj = 0; jj < kCnt; ++jj) {
+                    float rs_q;
+                    if (kHalvings >= 1) rs_q = __shfl_xor_sync(kFull, rloc[jj], 1);   // distance 1 splits ss / gx
+                    else rs_q = rloc[jj % (kCnt / 2 > 0 ? kCnt / 2 : 1)];           // one lane holds all values
+                    mloc[jj] = row_mean_gxhat(vals[jj], rs_q, Hf, inv_h);
+                }
+            }
             float rsv[kU], mgv[kU];
-            if (P2 >= kU) {
-                const int qs = tl % kU;
-                float ss = ssv[0], gx = gxv[0];
 #pragma unroll
-                for (int q = 1; q < kU; ++q) {
-                    ss = (qs == q) ? ssv[q] : ss;
-                    gx = (qs == q) ? gxv[q] : gx;
-                }
-                const float r = row_rstd(ss, Hf, inv_h, p.eps);
-                const float m = T::kNeedGx ? row_mean_gxhat(gx, r, Hf, inv_h) : 0.f;
-#pragma unroll
-                for (int q = 0; q < kU; ++q) {
-                    rsv[q] = __shfl_sync(kFull, r, team * P2 + q);
-                    mgv[q] = T::kNeedGx ? __shfl_sync(kFull, m, team * P2 + q) : 0.f;
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < kU; ++q) {
-                    rsv[q] = row_rstd(ssv[q], Hf, inv_h, p.eps);
-                    mgv[q] = T::kNeedGx ? row_mean_gxhat(gxv[q], rsv[q], Hf, inv_h) : 0.f;
+            for (int q = 0; q < kU; ++q) {
+                const int jr = q & (kCnt - 1);
+                rsv[q] = __shfl_sync(kFull, rloc[jr], holder(q));
+                mgv[q] = 0.f;
+                if (T::kNeedGx) {
+                    const int jg = (kU + q) & (kCnt - 1);
+                    mgv[q] = __shfl_sync(kFull, mloc[jg], holder(kU + q));
                 }
             }
             // phase 3: outputs and leaves; the group's steps form a subtree of the
