@@ -230,11 +230,6 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (MODE != kDw && T::kNeedGx) {
-        for (int i = tid; i < HS; i += blockDim.x) wsm[i] = __uint_as_float(uint32_t(p.w[col0 + i]) << 16);
-    }
-    if (K > 1) cluster_barrier(); else __syncthreads();
-
     // batch k of this team -> (plan item, slot base) or physical batch index
     auto batch_slots = [&](int k, int64_t &item, int &slot0) {
         if (item_units) {
@@ -253,42 +248,51 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
         }
     };
 
+    // The producer's first slot metadata is fetched before the CTA (cluster)
+    // barrier, so its latency overlaps the weight fill and the barrier.
+    constexpr int kPrefetch = 3;
+    SlotBatch<R> ring[kPrefetch];
+    auto load = [&](int k, SlotBatch<R> &mb) {
+        if (k >= n_batches) return;
+        int64_t item;
+        int slot0;
+        batch_slots(k, item, slot0);
+        mb.kind = 0;
+        mb.block = -1;
+        if (item_units) {
+            mb.kind = p.items[item].kind;
+            mb.block = p.items[item].block;
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            int32_t pr = -1, lr = -1;
+            if (p.use_plan) {
+                const PlanItem *it = p.items + item;
+                pr = it->prow[slot0 + r];
+                lr = it->lrow[slot0 + r];
+            } else {
+                const int64_t row = item * R + r;
+                if (row < p.n_rows) pr = p.tok_id[row / p.rpt] >= 0 ? int32_t(row) : -1;
+            }
+            mb.prow[r] = pr;
+            mb.lrow[r] = lr;
+        }
+    };
+    if (warp == NC + NS && lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kPrefetch; ++i) load(i, ring[i]);
+    }
+    if (MODE != kDw && T::kNeedGx) {
+        for (int i = tid; i < HS; i += blockDim.x) wsm[i] = __uint_as_float(uint32_t(p.w[col0 + i]) << 16);
+    }
+    if (K > 1) cluster_barrier(); else __syncthreads();
+
     if (warp == NC + NS) {
         // ------------------------------------------------ producer
         // The slot metadata of batch k comes from global memory (plan or
         // tok_id); it is loaded kPrefetch batches ahead so that issuing the
         // copies never waits on it.
         if (lane == 0) {
-            constexpr int kPrefetch = 3;
-            SlotBatch<R> ring[kPrefetch];
-            auto load = [&](int k, SlotBatch<R> &mb) {
-                if (k >= n_batches) return;
-                int64_t item;
-                int slot0;
-                batch_slots(k, item, slot0);
-                mb.kind = 0;
-                mb.block = -1;
-                if (item_units) {
-                    mb.kind = p.items[item].kind;
-                    mb.block = p.items[item].block;
-                }
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    int32_t pr = -1, lr = -1;
-                    if (p.use_plan) {
-                        const PlanItem *it = p.items + item;
-                        pr = it->prow[slot0 + r];
-                        lr = it->lrow[slot0 + r];
-                    } else {
-                        const int64_t row = item * R + r;
-                        if (row < p.n_rows) pr = p.tok_id[row / p.rpt] >= 0 ? int32_t(row) : -1;
-                    }
-                    mb.prow[r] = pr;
-                    mb.lrow[r] = lr;
-                }
-            };
-#pragma unroll
-            for (int i = 0; i < kPrefetch; ++i) load(i, ring[i]);
             int s = 0;
             uint32_t ph = 0;                             // parity of the current use of stage s
             for (int k = 0; k < n_batches; ++k) {
