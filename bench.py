@@ -53,6 +53,8 @@ def parse():
                     help="cut the workload to its first N logical tokens (profiling runs only)")
     ap.add_argument("--e2e-chunk", type=int, default=4096, help="token slots per sub-call of the e2e leg")
     ap.add_argument("--e2e-lanes", type=int, default=1, help="copy streams per direction in the e2e leg")
+    ap.add_argument("--gemm", action="store_true",
+                    help="the linear layer's deterministic weight gradient (in = out = hidden) instead of the norm")
     ap.add_argument("--chain", action="store_true",
                     help="residual add + norm forward and its backward with the residual gradient and the "
                          "loss seed's 1/D (D = active tokens of the multiset); no e2e or CPU legs")
@@ -499,6 +501,8 @@ def main():
 
     if args.impl == "reference":
         return reference_arm(args, rank, world)
+    if args.gemm:
+        return gemm_bench(args, rank, world)
 
     import torch
     import synth
@@ -702,6 +706,93 @@ def main():
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def gemm_bench(args, rank, world):
+    """The deterministic weight gradient of a linear layer y = x W^T with in =
+    out = hidden, over the workload's tokens in its headline layout: per step
+    begin, one placement call per layout call, one finalize (the GEMM)."""
+    import torch
+    import synth
+    import invariant_rmsnorm_fwd_gb300 as rb
+    from invariant_rmsnorm_fwd_gb300 import layout as L
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    wl = synth.config(args.config)
+    if args.max_tokens:
+        wl = synth.truncated(wl, args.max_tokens)
+    lay_name = args.layout or wl.headline
+    lay = L.workload_layouts(wl, kinds=[lay_name])[lay_name]
+    H, n = wl.hidden, wl.n_tokens
+    x = synth.logical_tensor(wl, synth.TAG_X, n, wl.x_std, device=device)
+    dy = synth.logical_tensor(wl, synth.TAG_DY, n, wl.dy_std, device=device)
+    calls = []
+    for tok in lay.calls:
+        cl = rb.call_layout(tok, 1, lay.n_logical_tokens, device=device, with_plan=False)
+        tid = cl.tok_id.long()
+        act = tid >= 0
+        xp = torch.zeros((tok.size, H), dtype=torch.bfloat16, device=device)
+        dp = torch.zeros_like(xp)
+        xp[act] = x[tid[act]]
+        dp[act] = dy[tid[act]]
+        calls.append((cl, xp, dp))
+    ws = rb.GemmDwWorkspace(n, H, H, device=device)
+    dw = torch.empty(H, H, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+
+    class G:
+        def run(self, st):
+            ws.begin(st)
+            for cl, xp, dp in calls:
+                ws.contrib(xp, dp, cl, st)
+            ws.finalize(dw, stream=st)
+
+    g = G()
+    flush = L2Flush(device)
+    g.run(stream)
+    torch.cuda.synchronize()
+    l0 = rb.kernel_launches()
+    g.run(stream)
+    torch.cuda.synchronize()
+    launches = rb.kernel_launches() - l0
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms, graph = time_steps(g, stream, args.steps, args.warmup, flush, None, graph=not args.no_graph)
+    clk = clocks.stop()
+    # the finalize alone (flag check + GEMM), CUDA events on its stream
+    fin = []
+    for _ in range(max(3, args.steps // 2)):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ws.finalize(dw, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        fin.append(e0.elapsed_time(e1))
+    fin_ms = statistics.median(fin)
+    ms_step = statistics.mean(ms)
+    flops = 2.0 * n * H * H
+    peak_tf = 1900.0
+    line = {
+        "metric": "linear-layer weight gradient (det_gemm dW) tokens/s, bitwise across layouts",
+        "value": round(n / (ms_step * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 accumulate", "io_dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64/Box-Muller, keyed by logical token id)",
+        "config": {"workload": workload_desc(wl, lay_name, lay.n_physical) + f", linear {H} -> {H}",
+                   "calls": len(lay.calls), "l2": "flushed before every timed step",
+                   "launch": "one CUDA graph replay per step" if graph is not None else "eager launches"},
+        "roofline": {"bound": "tensor", "kernel": "finalize (flag check + GEMM, FP32 accumulate)",
+                     "achieved": round(flops / (fin_ms * 1e-3) / 1e12, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(flops / (fin_ms * 1e-3) / 1e12 / peak_tf, 4), "traffic": None,
+                     "peak_source": "fallback (bf16 dense burst)", "launch_ms": round(fin_ms, 5)},
+        "placement_gbs": round(4.0 * H * n * 2 / ((ms_step - fin_ms) * 1e-3) / 1e9, 1),
+        "gpu_launches": int(launches) * args.steps, "gpu_launches_per_step": int(launches),
+        "clocks": clk,
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -80,6 +80,11 @@ def _load():
         "rmsnorm_plan_build": ([P, I64, I32, I64, P, ctypes.c_size_t, ctypes.POINTER(I64),
                                 ctypes.POINTER(I64), ctypes.POINTER(I64)], ctypes.c_int),
         "rmsnorm_bwd_noalloc": ([P, P, P, I64, F, LP, P, P, P, P], ctypes.c_int),
+        "gemm_dw_workspace_bytes": ([I64, I64, I64], ctypes.c_size_t),
+        "gemm_dw_begin": ([P, ctypes.c_size_t, I64, I64, I64, P], ctypes.c_int),
+        "gemm_dw_contrib": ([P, I64, P, I64, I64, I64, LP, P, P], ctypes.c_int),
+        "gemm_dw_finalize": ([P, I64, I64, I64, F, P, P], ctypes.c_int),
+        "gemm_dw_status": ([P, P, ctypes.POINTER(I32)], ctypes.c_int),
         "rmsnorm_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "rmsnorm_kernel_launches": ([], I64),
     }
@@ -311,6 +316,46 @@ def dweight_combine(roots, dweight=None, stream=None, grad_scale: float = 1.0):
     _check(_load().dweight_combine(_ptr(roots), n, H, float(grad_scale), _ptr(dweight), _stream(stream)),
            "dweight_combine")
     return dweight
+
+
+class GemmDwWorkspace:
+    """Workspace of one deterministic linear-layer weight gradient (det_gemm dW)
+    over n_logical_tokens tokens: logical-order copies of x and dy and a flag
+    per token (see gemm_dw_* in the C header)."""
+
+    def __init__(self, n_logical_tokens: int, in_features: int, out_features: int, device="cuda"):
+        import torch
+        self.n, self.i, self.o = int(n_logical_tokens), int(in_features), int(out_features)
+        self.bytes = int(_load().gemm_dw_workspace_bytes(self.n, self.i, self.o))
+        if self.bytes == 0:
+            raise RmsNormError(-2, "gemm_dw_workspace_bytes")
+        self.buf = torch.empty(self.bytes, dtype=torch.uint8, device=device)
+        assert self.buf.data_ptr() % 256 == 0
+
+    def begin(self, stream=None):
+        _check(_load().gemm_dw_begin(_ptr(self.buf), self.bytes, self.n, self.i, self.o, _stream(stream)),
+               "gemm_dw_begin")
+
+    def contrib(self, x, dy, lay: CallLayout, stream=None):
+        """Places one call's tokens: x [T, I] and dy [T, O] (row strides taken from the tensors)."""
+        assert x.dim() == 2 and dy.dim() == 2 and x.shape[1] == self.i and dy.shape[1] == self.o
+        assert x.stride(1) == 1 and dy.stride(1) == 1 and x.shape[0] == dy.shape[0] == lay.n_tokens
+        L = lay.struct(x.stride(0))
+        _check(_load().gemm_dw_contrib(_ptr(x), x.stride(0), _ptr(dy), dy.stride(0), self.i, self.o,
+                                       ctypes.byref(L), _ptr(self.buf), _stream(stream)), "gemm_dw_contrib")
+
+    def finalize(self, dw=None, grad_scale: float = 1.0, stream=None):
+        import torch
+        if dw is None:
+            dw = torch.empty(self.o, self.i, dtype=torch.float32, device=self.buf.device)
+        _check(_load().gemm_dw_finalize(_ptr(self.buf), self.n, self.i, self.o, float(grad_scale), _ptr(dw),
+                                        _stream(stream)), "gemm_dw_finalize")
+        return dw
+
+    def status(self, stream=None) -> int:
+        out = ctypes.c_int32(0)
+        _check(_load().gemm_dw_status(_ptr(self.buf), _stream(stream), ctypes.byref(out)), "gemm_dw_status")
+        return int(out.value)
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fno-strict-aliasing", f"-I{INCLUDE}"]
-SOURCES = ["rmsnorm_bi.cu", "rows_fwd.cu", "rows_dx.cu", "rows_dxdw.cu", "rows_adddxdw.cu", "plan.cpp"]
+SOURCES = ["rmsnorm_bi.cu", "rows_fwd.cu", "rows_dx.cu", "rows_dxdw.cu", "rows_adddxdw.cu", "gemm_dw.cu",
+           "plan.cpp"]
 
 
 def nvcc() -> str:
@@ -65,7 +66,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

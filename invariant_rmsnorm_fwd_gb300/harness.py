@@ -221,6 +221,30 @@ def run_layout_chain(lay: layout_mod.Layout, x_log, r_log, dy_log, dres_log, wei
                      whole, spill, untouched, h=outs["h"])
 
 
+def run_layout_gemm(lay: layout_mod.Layout, x_log, dy_log, device="cuda", stream=None) -> LayoutRun:
+    """The linear layer's deterministic weight gradient for one layout: every call
+    places its tokens, one finalize forms dW.  dW is returned as the run's
+    `dweight` (FP32 [O][I]); y and dx are empty."""
+    import torch
+    import invariant_rmsnorm_fwd_gb300 as rb
+    n_tok, I = x_log.shape
+    O = dy_log.shape[1]
+    ws = rb.GemmDwWorkspace(n_tok, I, O, device=device)
+    ws.begin(stream)
+    for tok in lay.calls:
+        cl = rb.call_layout(tok, 1, lay.n_logical_tokens, device=device, with_plan=False)
+        tid = cl.tok_id.long()
+        act = tid >= 0
+        xp = torch.full((tok.size, I), float("nan"), dtype=torch.bfloat16, device=device)
+        dp = torch.full((tok.size, O), float("nan"), dtype=torch.bfloat16, device=device)
+        xp[act] = x_log[tid[act]]
+        dp[act] = dy_log[tid[act]]
+        ws.contrib(xp, dp, cl, stream)
+    dw = ws.finalize(stream=stream)
+    empty = torch.empty(0, dtype=torch.bfloat16, device=device)
+    return LayoutRun(lay.name, empty, empty.clone(), dw, ws.status(stream), len(lay.calls), lay.rows_per_call)
+
+
 def assert_batch_invariant(runs: dict, layouts: dict, reference: str = "full") -> InvarianceReport:
     """Bitwise comparison of every layout's y, dx and dweight with the reference layout."""
     rep = InvarianceReport(reference)

@@ -82,6 +82,15 @@ def test_host_side_errors_need_no_gpu():
     assert lib.dweight_combine(good, 2048, 8, 1.0, good, None) == -5
     assert lib.dweight_finalize_range(good, 640, 8, 1, 2, good, None) == -5    # not aligned
     assert lib.dweight_finalize_range(good, 640, 8, 0, 3, good, None) == -5    # not a power of two
+    # linear-layer weight gradient
+    assert lib.gemm_dw_workspace_bytes(10, 12, 8) == 0                           # in_features % 8
+    assert lib.gemm_dw_workspace_bytes(10, 16, 8) >= 256 + 10 * 4 + 10 * 16 * 2 + 10 * 8 * 2
+    assert lib.gemm_dw_begin(good, 16, 10, 16, 8, None) == -6
+    assert lib.gemm_dw_begin(P(272), 1 << 20, 10, 16, 8, None) == -3
+    assert lib.gemm_dw_contrib(good, 16, good, 8, 16, 8, ctypes.byref(_layout(rpt=2)), good, None) == -5
+    assert lib.gemm_dw_contrib(good, 8, good, 8, 16, 8, ctypes.byref(L), good, None) == -4    # x stride < I
+    assert lib.gemm_dw_finalize(good, 10, 16, 8, nan, good, None) == -13
+    assert lib.gemm_dw_finalize(None, 10, 16, 8, 1.0, good, None) == -1
 
 
 def test_workspace_size_formula():
