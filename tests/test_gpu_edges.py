@@ -31,7 +31,7 @@ def _workload(lengths, hidden, seed=7, x_std=1.0, dy_std=1e-2):
 # ------------------------------------------------------------------ exact order
 
 @pytest.mark.parametrize("hidden", [8, 128, 4096, 5120])
-@pytest.mark.parametrize("n_rows", [1, 63, 64, 65, 259])
+@pytest.mark.parametrize("n_rows", [1, 63, 64, 65, 259, 4999])
 def test_dweight_follows_the_fixed_tree_bitwise(hidden, n_rows):
     """eps = 0 and rows of constant magnitude 2^k make xhat = +-1 exactly, so the
     leaves are +-dy exactly; dy is chosen so that every association order gives
