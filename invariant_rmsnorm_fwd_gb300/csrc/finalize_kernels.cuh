@@ -47,6 +47,25 @@ __device__ __forceinline__ void load8(const float *src, float (&v)[8]) {
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// Every quarter of the block arrived, each as one quarter partial (byte 1) or
+// as two eighth partials (byte 12).
+__device__ __forceinline__ bool quarter_state(uint32_t state) {
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t b = (state >> (8 * k)) & 0xffu;
+        ok &= b == kStateQuarter || b == (kStateEighth0 | kStateEighth1);
+    }
+    return ok;
+}
+__device__ __forceinline__ void add_second_eighth(uint32_t state, int q, const float *src, float (&v)[8]) {
+    if (((state >> (8 * q)) & 0xffu) != (kStateEighth0 | kStateEighth1)) return;
+    float e[8];
+    load8(src, e);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = __fadd_rn(v[c], e[c]);
+}
+
 constexpr int kTreeWarps = 16;                           // warps per CTA: 2 inputs each
 constexpr int kTreeVecs = 32;                            // vectors (8 columns) per CTA
 
@@ -78,14 +97,20 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, c
         const uint32_t state = from_blocks ? reinterpret_cast<const uint32_t *>(ws.block_state)[b] : kStateWhole;
         if (!from_blocks) {
             if (has_vec) load8(in + b * int64_t(H) + int64_t(v) * 8, val);
-        } else if (state == 0x01010101u) {
+        } else if (quarter_state(state)) {
             if (has_vec) {
                 float q0[8], q1[8], q2[8], q3[8];
                 const float *src = ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8;
+                const float *src2 = ws.eighth + b * 4 * int64_t(H) + int64_t(v) * 8;
                 load8(src, q0);
                 load8(src + H, q1);
                 load8(src + 2 * int64_t(H), q2);
                 load8(src + 3 * int64_t(H), q3);
+                // a quarter that arrived as two eighths: the halves make level 4
+                add_second_eighth(state, 0, src2, q0);
+                add_second_eighth(state, 1, src2 + H, q1);
+                add_second_eighth(state, 2, src2 + 2 * int64_t(H), q2);
+                add_second_eighth(state, 3, src2 + 3 * int64_t(H), q3);
 #pragma unroll
                 for (int c = 0; c < 8; ++c) val[c] = __fadd_rn(__fadd_rn(q0[c], q1[c]), __fadd_rn(q2[c], q3[c]));
             }

@@ -34,9 +34,12 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 struct WsView {                      // device addresses of the workspace regions
     WsHeader *hdr;
-    uint8_t *block_state;            // [nb][4] per quarter: 0 none, 1 quarter partial, 2 whole-block partial
+    uint8_t *block_state;            // [nb][4] per quarter: 0 none, 1 quarter partial, 2 whole-block partial,
+                                     //   4 / 8 / 12 first / second / both eighth partials
     uint8_t *leaf_flag;              // [N]    1 = row spilled
-    float *block_partial;            // [nb][4][H] quarter partials (slot 0 holds a whole-block partial)
+    float *block_partial;            // [nb][4][H] quarter partials (slot 0 holds a whole-block partial;
+                                     //   a quarter split in two eighths holds the first one)
+    float *eighth;                   // [nb][4][H] second eighth partials of split quarters
     float *scratch_a;                // [ceil(nb/32)][H]
     float *scratch_b;                // [ceil(nb/32)][H]
     float *spill;                    // [N][H]
@@ -47,14 +50,15 @@ __host__ __device__ inline int64_t align256(int64_t v) { return (v + 255) & ~int
 
 // Region offsets depend only on (N, H); host and device compute them alike.
 struct WsLayout {
-    int64_t off_state, off_flag, off_partial, off_sa, off_sb, off_spill, total;
+    int64_t off_state, off_flag, off_partial, off_eighth, off_sa, off_sb, off_spill, total;
     __host__ __device__ WsLayout(int64_t N, int64_t H) {
         int64_t nb = (N + kBlockRows - 1) / kBlockRows;
         int64_t ng = (nb + 31) / 32;                     // first-pass groups of 32 blocks
         off_state = 256;
         off_flag = align256(off_state + nb * 4);
         off_partial = align256(off_flag + N);
-        off_sa = align256(off_partial + nb * 4 * H * 4);
+        off_eighth = align256(off_partial + nb * 4 * H * 4);
+        off_sa = align256(off_eighth + nb * 4 * H * 4);
         off_sb = align256(off_sa + ng * H * 4);
         off_spill = align256(off_sb + ng * H * 4);
         total = align256(off_spill + N * H * 4);
@@ -69,6 +73,7 @@ inline WsView ws_view(void *base, int64_t N, int64_t H) {
     v.block_state = b + L.off_state;
     v.leaf_flag = b + L.off_flag;
     v.block_partial = reinterpret_cast<float *>(b + L.off_partial);
+    v.eighth = reinterpret_cast<float *>(b + L.off_eighth);
     v.scratch_a = reinterpret_cast<float *>(b + L.off_sa);
     v.scratch_b = reinterpret_cast<float *>(b + L.off_sb);
     v.spill = reinterpret_cast<float *>(b + L.off_spill);

@@ -79,6 +79,7 @@ struct ModeTraits {
 // spilled.  Any contribution that meets an earlier one is a double count.
 constexpr uint32_t kStateWhole = 0x02020202u;
 constexpr uint8_t kStateQuarter = 1;
+constexpr uint8_t kStateEighth0 = 4, kStateEighth1 = 8;   // the halves of a quarter split in two
 
 __device__ __forceinline__ bool leaf_flags_clear(const WsView &ws, int64_t r0, int64_t rows) {
     bool clear = true;
@@ -108,7 +109,23 @@ __device__ __forceinline__ void mark_quarter(const WsView &ws, int64_t b, int q)
     for (int i = 0; i < 4; ++i) dup |= st[i] == 2;
     if (rows > 0) dup |= !leaf_flags_clear(ws, r0, rows);
     if (dup) set_status(ws.hdr, kStDouble);
-    st[q] = kStateQuarter;
+    // a word-wide OR: the two halves of another quarter of this block may be
+    // marked by other CTAs at the same time
+    atomicOr(reinterpret_cast<unsigned int *>(st), unsigned(kStateQuarter) << (8 * q));
+}
+
+// Half `half` (rows 8*half .. 8*half+7) of quarter q of block b arrived as an
+// eighth partial.
+__device__ __forceinline__ void mark_eighth(const WsView &ws, int64_t b, int q, int half) {
+    uint8_t *st = ws.block_state + b * 4;
+    const int64_t r0 = b * kBlockRows + q * 16 + half * 8;
+    const int64_t rows = max64(0, min64(8, ws.n_rows - r0));
+    const uint8_t bit = half ? kStateEighth1 : kStateEighth0;
+    bool dup = (st[q] & (bit | kStateQuarter)) != 0;
+    for (int i = 0; i < 4; ++i) dup |= st[i] == 2;
+    if (rows > 0) dup |= !leaf_flags_clear(ws, r0, rows);
+    if (dup) set_status(ws.hdr, kStDouble);
+    atomicOr(reinterpret_cast<unsigned int *>(st), unsigned(bit) << (8 * q));
 }
 
 __device__ __forceinline__ void mark_spilled_row(const WsView &ws, int64_t lrow) {
@@ -217,8 +234,16 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     const int64_t per_unit = item_units ? kUnitBatches : 1;
     const int64_t cluster_id = blockIdx.x / K;
     const int64_t n_clusters = gridDim.x / K;
-    const int64_t my_units = p.n_units > cluster_id ? (p.n_units - cluster_id + n_clusters - 1) / n_clusters : 0;
-    const int n_batches = int(my_units * per_unit);      // < 2^31: units are bounded by rows / 2
+    // Leaf modes: quarter units round-robin over the teams.  When the last
+    // round would leave at least half the teams idle (0 < rem <= teams / 2),
+    // its quarters are split into two 8-row eighths instead, one per team, so
+    // that every team ends after (full + 1/2) quarters.
+    const int64_t q_full = p.n_units / n_clusters, q_rem = p.n_units % n_clusters;
+    const bool eighths = item_units && q_rem > 0 && 2 * q_rem <= n_clusters;
+    const int64_t my_units = eighths ? q_full
+                             : (p.n_units > cluster_id ? (p.n_units - cluster_id + n_clusters - 1) / n_clusters : 0);
+    const int64_t my_eighths = (eighths && cluster_id < 2 * q_rem) ? 1 : 0;
+    const int n_batches = int(my_units * per_unit + my_eighths * (kUnitBatches / 2));   // < 2^31
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -232,7 +257,12 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     }
     // batch k of this team -> (plan item, slot base) or physical batch index
     auto batch_slots = [&](int k, int64_t &item, int &slot0) {
-        if (item_units) {
+        if (item_units && k >= my_units * kUnitBatches) {  // this team's eighth (cluster_id-th)
+            const int64_t qg = q_full * n_clusters + (cluster_id >> 1);
+            item = qg >> 2;
+            slot0 = int(qg & 3) * kSplitUnitRows + int(cluster_id & 1) * (kSplitUnitRows / 2) +
+                    int(k - my_units * kUnitBatches) * R;
+        } else if (item_units) {
             const int64_t u = cluster_id + (k / kUnitBatches) * n_clusters;   // quarter unit
             item = u >> 2;
             slot0 = int(u & 3) * kSplitUnitRows + int(k % kUnitBatches) * R;
@@ -465,12 +495,15 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
         // Leaf modes walk their 16-row units; the inner loop over the unit's
         // batches (stages of R rows) is unrolled, so `sub`, the batch's place in
         // the unit, is a compile-time constant and the tree positions are static.
+        // A team's eighth (8 rows, kInner / 2 batches) comes after its quarters.
         constexpr int kInner = T::kLeaves ? kUnitBatches : 1;
-        const int64_t n_outer = n_batches / kInner;          // leaf modes: n_batches = units * kUnitBatches
+        const int64_t n_outer = T::kLeaves ? my_units + my_eighths : n_batches;
         bool stop = false;
         for (int64_t j = 0; j < n_outer && !stop; ++j, u += n_clusters) {
+          const bool half_unit = T::kLeaves && j >= my_units;
 #pragma unroll
           for (int sub = 0; sub < kInner; ++sub) {
+            if (half_unit && sub >= kInner / 2) break;
             if (*abort_flag) {
                 stop = true;
                 break;
@@ -483,7 +516,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
             }
             if (T::kLeaves && sub == 0) {                    // item header, staged by the producer
                 const int2 hd = item_hdr[s];
-                quarter = int(u & 3);
+                quarter = half_unit ? int((q_full * n_clusters + (cluster_id >> 1)) & 3) : int(u & 3);
                 kind = hd.x;
                 block = hd.y;
                 if ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1)) {
@@ -550,6 +583,11 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                                 if (has_vec)
                                     st_global_f2x4(p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + my_col, leaf);
                                 if (t == 0 && rank == 0) mark_quarter(p.ws, block, quarter);
+                            } else if (half_unit && sub == kUnitBatches / 2 - 1) {   // leaf[] is the eighth partial
+                                const int half = int(cluster_id & 1);
+                                float *dst = half ? p.ws.eighth : p.ws.block_partial;
+                                if (has_vec) st_global_f2x4(dst + (int64_t(block) * 4 + quarter) * H + my_col, leaf);
+                                if (t == 0 && rank == 0) mark_eighth(p.ws, block, quarter, half);
                             }
                         }
                     } else if (kind == 1 && act) {
