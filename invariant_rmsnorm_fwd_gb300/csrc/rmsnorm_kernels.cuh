@@ -9,9 +9,10 @@
 //    column warps write y or dx and reduce the dweight leaves.
 //
 //  * small_row_kernel (hidden <= 256): a team is P2 = next_pow2(hidden/8)
-//    lanes of one warp, so a warp works on 32/P2 rows at once with 16-byte
-//    vector loads straight into registers; the rows of a step are combined
-//    across teams by a butterfly before entering the 64-leaf tree.
+//    lanes of one warp, so a warp works on 32/P2 rows at once; rows reach
+//    each lane's 16-byte pieces through a per-warp shared-memory ring filled
+//    by cp.async ahead of use; the rows of a step are combined across teams
+//    by a butterfly before entering the 64-leaf tree.
 //
 // Work units are either plan items (64 row slots: a whole logical block in
 // logical order, or rows of blocks cut by a call boundary) or, without a
