@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
-    ap.add_argument("--streams", type=int, default=8, help="streams the calls of a multi-call layout fork over")
+    ap.add_argument("--streams", type=int, default=32, help="streams the calls of a multi-call layout fork over")
     ap.add_argument("--max-tokens", type=int, default=0,
                     help="cut the workload to its first N logical tokens (profiling runs only)")
     ap.add_argument("--e2e-chunk", type=int, default=4096, help="token slots per sub-call of the e2e leg")
@@ -198,7 +198,7 @@ class Step:
     With `chain`, the step is the residual add + norm forward and the backward
     with the residual gradient, scaled by the loss seed's 1/D."""
 
-    def __init__(self, wl, lay, x_log, dy_log, w, rpt, device, r_log=None, dres_log=None, n_streams=8):
+    def __init__(self, wl, lay, x_log, dy_log, w, rpt, device, r_log=None, dres_log=None, n_streams=32):
         import torch
         import invariant_rmsnorm_fwd_gb300 as rb
         self.rb = rb
@@ -247,7 +247,7 @@ class Step:
 
     def run(self, stream):
         """Calls of a multi-call layout are independent (they touch disjoint rows and
-        blocks of the workspace), so they are spread over n_streams streams (8 by default) that
+        blocks of the workspace), so they are spread over n_streams streams (32 by default) that
         fork from and join back into `stream`; one-call layouts stay on `stream`."""
         import torch
         rb = self.rb

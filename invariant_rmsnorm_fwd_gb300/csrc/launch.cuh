@@ -48,15 +48,15 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
     }
     // Every team pays the pipeline's ramp (barrier set-up, first metadata and
     // bulk-copy latency), so a small call gives each team at least 64 rows
-    // instead of spreading a few rows over every SM, but keeps at least a
-    // quarter of the resident teams; calls issued on other streams fill the
-    // rest (measured on the many-call layouts with eight streams: 14-19%
-    // faster steps than one team per SM).
+    // instead of spreading a few rows over every SM, but keeps at least an
+    // eighth of the resident teams; calls issued on other streams fill the
+    // rest (measured on the many-call layouts with 32 streams: c2 1.06 ->
+    // 0.99 ms, c4 2.79 -> 2.73 ms against a quarter with 8 streams).
     {
         const int64_t rows_per_unit = (p.use_plan && ModeTraits<MODE>::kLeaves) ? kSplitUnitRows : R;
         const int64_t min_units = (64 + rows_per_unit - 1) / rows_per_unit;
         int64_t want = (p.n_units + min_units - 1) / min_units;
-        if (want < teams / 4) want = teams / 4;
+        if (want < teams / 8) want = teams / 8;
         if (want < teams) teams = want;
     }
     if (teams > p.n_units) teams = p.n_units;
