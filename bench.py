@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
     ap.add_argument("--streams", type=int, default=32, help="streams the calls of a multi-call layout fork over")
+    ap.add_argument("--clock-log", default=None, help="keep the nvidia-smi clock samples in this CSV file")
     ap.add_argument("--max-tokens", type=int, default=0,
                     help="cut the workload to its first N logical tokens (profiling runs only)")
     ap.add_argument("--e2e-chunk", type=int, default=4096, help="token slots per sub-call of the e2e leg")
@@ -113,15 +114,21 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path=None):
+        """Samples go to `path` (the --clock-log option) or to a temporary file."""
+        import tempfile
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        if path:
+            self.path = path
+        else:
+            fd, self.path = tempfile.mkstemp(prefix=f"clocks_gpu{gpu_index}_", suffix=".csv")
+            os.close(fd)
 
     def start(self):
         """Start sampling every 100 ms; returns once the first sample is on disk (or after 5 s)."""
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
@@ -579,7 +586,7 @@ def main():
     multi.run(stream)
     torch.cuda.synchronize()
     launches = rb.kernel_launches() - l0
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clock_log)
     clocks.start()
     ms, graph = time_steps(multi, stream, args.steps, args.warmup, flush, dist, graph=not args.no_graph)
     # keep the same step running (untimed) so the clock samples cover the load
@@ -758,7 +765,7 @@ def gemm_bench(args, rank, world):
     g.run(stream)
     torch.cuda.synchronize()
     launches = rb.kernel_launches() - l0
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clock_log)
     clocks.start()
     ms, graph = time_steps(g, stream, args.steps, args.warmup, flush, None, graph=not args.no_graph)
     clk = clocks.stop()
