@@ -119,6 +119,7 @@ class ClockSampler:
         import tempfile
         self.proc = None
         self.gpu = gpu_index
+        self.tmp = not path
         if path:
             self.path = path
         else:
@@ -145,6 +146,8 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
+            if self.tmp and os.path.exists(self.path):
+                os.unlink(self.path)
             return None
         self.proc.terminate()
         try:
@@ -166,6 +169,8 @@ class ClockSampler:
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+        if self.tmp:
+            os.unlink(self.path)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
