@@ -275,8 +275,11 @@ int rmsnorm_dweight_status(const void *workspace, rmsnorm_stream_t stream, int32
  * execute: one item per logical block wholly inside the call (its 64 rows in
  * logical order) and items of up to 64 rows from blocks cut by a call
  * boundary.  rmsnorm_plan_bytes gives a capacity that always suffices.
- * Errors: RMSNORM_ERR_ID, RMSNORM_ERR_DUPLICATE, RMSNORM_ERR_CAPACITY.
- * The plan depends only on tok_id, rows_per_token and n_logical_tokens.
+ * Errors: RMSNORM_ERR_ID, RMSNORM_ERR_DUPLICATE, RMSNORM_ERR_CAPACITY
+ * (host_plan's contents are then unspecified).  The plan depends only on
+ * tok_id, rows_per_token and n_logical_tokens.  Cost: linear in the call's
+ * rows when its ids ascend, plus a sort otherwise; per-thread working arrays
+ * are kept between calls.  Thread-safe.
  */
 int rmsnorm_plan_bytes(int64_t n_tokens, int32_t rows_per_token, size_t *bytes);
 int rmsnorm_plan_build(const int32_t *host_tok_id, int64_t n_tokens, int32_t rows_per_token,
@@ -284,7 +287,7 @@ int rmsnorm_plan_build(const int32_t *host_tok_id, int64_t n_tokens, int32_t row
                        int64_t *plan_items, int64_t *whole_blocks, int64_t *spill_rows);
 
 /*
- * Allocation-free backward (no counterpart in the paper; it exists for
+ * Allocation-free backward (the pages describe no such call; it exists for
  * callers that cannot allocate device memory).  Some callers cannot call
  * cudaMalloc or an allocating library routine at the point where they run
  * the backward: code recorded into a CUDA graph without a memory pool,

@@ -118,14 +118,20 @@ def kernel_launches() -> int:
 
 # ------------------------------------------------------------------ planning
 
-def plan_build(tok_id: np.ndarray, rows_per_token: int, n_logical_tokens: int):
+def plan_build(tok_id: np.ndarray, rows_per_token: int, n_logical_tokens: int, out: np.ndarray = None):
     """Host planner (C++ in the library).  Returns (plan bytes as np.uint8, items,
-    whole blocks, spilled rows)."""
+    whole blocks, spilled rows).  `out` (contiguous np.uint8, e.g. a view of pinned
+    memory) receives the plan in place; the returned bytes are then a view of it."""
     lib = _load()
     tok_id = np.ascontiguousarray(tok_id, dtype=np.int32)
     cap = ctypes.c_size_t(0)
     _check(lib.rmsnorm_plan_bytes(tok_id.size, rows_per_token, ctypes.byref(cap)), "rmsnorm_plan_bytes")
-    buf = np.empty(max(int(cap.value), PLAN_ITEM_BYTES), dtype=np.uint8)
+    if out is None:
+        buf = np.empty(max(int(cap.value), PLAN_ITEM_BYTES), dtype=np.uint8)
+    else:
+        if out.dtype != np.uint8 or out.ndim != 1 or not out.flags["C_CONTIGUOUS"]:
+            raise ValueError("plan_build: out must be a contiguous 1-D np.uint8 array")
+        buf = out
     items, whole, spill = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
     _check(lib.rmsnorm_plan_build(tok_id.ctypes.data_as(ctypes.c_void_p), tok_id.size, rows_per_token,
                                   n_logical_tokens, buf.ctypes.data_as(ctypes.c_void_p), buf.size,

@@ -28,9 +28,32 @@ struct Item {                       // must match rbi::PlanItem (528 bytes)
 };
 static_assert(sizeof(Item) == 528, "plan item layout");
 
-void clear_item(Item &it) {
-    std::memset(&it, 0, sizeof it);
-    for (int i = 0; i < kBlockRows; ++i) it.prow[i] = it.lrow[i] = -1;
+void fill_item(Item &it, int32_t kind, int32_t block, const int32_t *prow, const int32_t *lrow, size_t n) {
+    it.kind = kind;
+    it.block = block;
+    it.count = int32_t(n);
+    it.reserved = 0;
+    std::memcpy(it.prow, prow, n * sizeof(int32_t));
+    std::memcpy(it.lrow, lrow, n * sizeof(int32_t));
+    for (size_t q = n; q < size_t(kBlockRows); ++q) it.prow[q] = it.lrow[q] = -1;
+}
+
+// Per-thread working arrays, kept between calls so that planning a call every
+// step does not map and fault in fresh pages each time.
+struct Scratch {
+    std::vector<std::pair<int32_t, int32_t>> tok;
+    std::vector<int32_t> lrows, prows, sp_lrow, sp_prow;
+
+    template <class T>
+    T *reserve(std::vector<T> &v, size_t n) {                 // grows only; contents are scratch
+        if (v.size() < n) v.resize(n);
+        return v.data();
+    }
+};
+
+Scratch &scratch() {
+    thread_local Scratch s;
+    return s;
 }
 
 }  // namespace
@@ -52,72 +75,70 @@ extern "C" int rmsnorm_plan_build(const int32_t *tok_id, int64_t n_tokens, int32
     const int64_t R = rows_per_token;
     const int64_t N = n_logical_tokens * R;                    // logical rows
     if (n_tokens * R >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return RMSNORM_ERR_LAYOUT;
+    Scratch &sc = scratch();
+    using Tok = std::pair<int32_t, int32_t>;                   // (id, slot)
+    const size_t n_act_max = size_t(n_tokens) * size_t(R);
+    Tok *tok = sc.reserve(sc.tok, size_t(n_tokens));
+    int32_t *lrows = sc.reserve(sc.lrows, n_act_max), *prows = sc.reserve(sc.prows, n_act_max);
+    int32_t *sp_lrow = sc.reserve(sc.sp_lrow, n_act_max), *sp_prow = sc.reserve(sc.sp_prow, n_act_max);
 
-    // active tokens sorted by logical id
-    std::vector<std::pair<int32_t, int32_t>> tok;             // (id, slot)
-    tok.reserve(size_t(n_tokens));
+    // active tokens sorted by logical id (ids of a call usually arrive ascending:
+    // the sort is skipped then)
+    size_t n_tok = 0;
+    bool ascending = true;
     for (int64_t t = 0; t < n_tokens; ++t) {
         const int32_t id = tok_id[t];
         if (id < -1 || id >= n_logical_tokens) return RMSNORM_ERR_ID;
-        if (id >= 0) tok.emplace_back(id, int32_t(t));
+        if (id >= 0) {
+            if (n_tok && id <= tok[n_tok - 1].first) ascending = false;
+            tok[n_tok++] = Tok(id, int32_t(t));
+        }
     }
-    std::sort(tok.begin(), tok.end());
-    for (size_t i = 1; i < tok.size(); ++i)
-        if (tok[i].first == tok[i - 1].first) return RMSNORM_ERR_DUPLICATE;
+    if (!ascending) {
+        std::sort(tok, tok + n_tok);
+        for (size_t i = 1; i < n_tok; ++i)
+            if (tok[i].first == tok[i - 1].first) return RMSNORM_ERR_DUPLICATE;
+    }
 
     // rows in logical order: token id*R + h sits at physical row slot*R + h
-    const size_t n_act = tok.size() * size_t(R);
-    std::vector<Item> whole, spill;
-    std::vector<int32_t> sp_prow, sp_lrow;
+    const size_t n_act = n_tok * size_t(R);
+    for (size_t t = 0, k = 0; t < n_tok; ++t) {
+        const int32_t l0 = int32_t(int64_t(tok[t].first) * R), p0 = int32_t(int64_t(tok[t].second) * R);
+        for (int32_t h = 0; h < int32_t(R); ++h, ++k) {
+            lrows[k] = l0 + h;
+            prows[k] = p0 + h;
+        }
+    }
+
+    // whole blocks go straight to the output, cut rows are gathered for the spill items
+    const size_t max_items = capacity / sizeof(Item);
+    Item *out = static_cast<Item *>(plan);
+    size_t n_items = 0, n_sp = 0;
     size_t i = 0;
     while (i < n_act) {
-        const int64_t lrow0 = int64_t(tok[i / R].first) * R + int64_t(i % R);
-        const int64_t b = lrow0 / kBlockRows;
-        const int64_t b_rows = std::min<int64_t>(kBlockRows, N - b * kBlockRows);
+        const int32_t b = lrows[i] / kBlockRows;
+        const int64_t b_rows = std::min<int64_t>(kBlockRows, N - int64_t(b) * kBlockRows);
         size_t j = i;                                          // rows of block b in this call: [i, j)
-        while (j < n_act && (int64_t(tok[j / R].first) * R + int64_t(j % R)) / kBlockRows == b) ++j;
-        if (int64_t(j - i) == b_rows) {
-            Item it;
-            clear_item(it);
-            it.kind = 0;
-            it.block = int32_t(b);
-            it.count = int32_t(b_rows);
-            for (size_t k = i; k < j; ++k) {
-                const int64_t lrow = int64_t(tok[k / R].first) * R + int64_t(k % R);
-                const int s = int(lrow - b * kBlockRows);
-                it.prow[s] = int32_t(int64_t(tok[k / R].second) * R + int64_t(k % R));
-                it.lrow[s] = int32_t(lrow);
-            }
-            whole.push_back(it);
+        while (j < n_act && lrows[j] / kBlockRows == b) ++j;
+        if (int64_t(j - i) == b_rows) {                        // rows [64b, 64b + b_rows) in order
+            if (n_items == max_items) return RMSNORM_ERR_CAPACITY;
+            if (!out) return RMSNORM_ERR_NULL;
+            fill_item(out[n_items++], 0, b, prows + i, lrows + i, size_t(b_rows));
         } else {
-            for (size_t k = i; k < j; ++k) {
-                sp_lrow.push_back(int32_t(int64_t(tok[k / R].first) * R + int64_t(k % R)));
-                sp_prow.push_back(int32_t(int64_t(tok[k / R].second) * R + int64_t(k % R)));
-            }
+            std::memcpy(sp_lrow + n_sp, lrows + i, (j - i) * sizeof(int32_t));
+            std::memcpy(sp_prow + n_sp, prows + i, (j - i) * sizeof(int32_t));
+            n_sp += j - i;
         }
         i = j;
     }
-    for (size_t k = 0; k < sp_prow.size(); k += kBlockRows) {
-        Item it;
-        clear_item(it);
-        it.kind = 1;
-        it.block = -1;
-        const size_t n = std::min<size_t>(kBlockRows, sp_prow.size() - k);
-        it.count = int32_t(n);
-        for (size_t q = 0; q < n; ++q) {
-            it.prow[q] = sp_prow[k + q];
-            it.lrow[q] = sp_lrow[k + q];
-        }
-        spill.push_back(it);
+    const size_t n_whole = n_items;
+    for (size_t k = 0; k < n_sp; k += kBlockRows) {
+        if (n_items == max_items) return RMSNORM_ERR_CAPACITY;
+        if (!out) return RMSNORM_ERR_NULL;
+        fill_item(out[n_items++], 1, -1, sp_prow + k, sp_lrow + k, std::min<size_t>(kBlockRows, n_sp - k));
     }
-    const int64_t items = int64_t(whole.size() + spill.size());
-    if (size_t(items) * sizeof(Item) > capacity) return RMSNORM_ERR_CAPACITY;
-    if (items > 0 && !plan) return RMSNORM_ERR_NULL;
-    Item *out = static_cast<Item *>(plan);
-    if (!whole.empty()) std::memcpy(out, whole.data(), whole.size() * sizeof(Item));
-    if (!spill.empty()) std::memcpy(out + whole.size(), spill.data(), spill.size() * sizeof(Item));
-    *plan_items = items;
-    if (whole_blocks) *whole_blocks = int64_t(whole.size());
-    if (spill_rows) *spill_rows = int64_t(sp_prow.size());
+    *plan_items = int64_t(n_items);
+    if (whole_blocks) *whole_blocks = int64_t(n_whole);
+    if (spill_rows) *spill_rows = int64_t(n_sp);
     return RMSNORM_OK;
 }

@@ -125,3 +125,60 @@ def test_plan_is_a_function_of_the_ids_only():
     a = _plan(tok, 1, 300)[0]
     b = _plan(tok.copy(), 1, 300)[0]
     assert np.array_equal(a, b)
+
+
+def _plan_ref(tok, rpt, ntok):
+    """The plan spelled out in numpy: active rows in logical order, one item per
+    logical block held whole (its rows in order, -1 beyond the block's last row),
+    the rows of cut blocks in logical order cut into items of 64."""
+    act = np.nonzero(tok >= 0)[0]
+    order = act[np.argsort(tok[act], kind="stable")]
+    lrows = (tok[order].astype(np.int64)[:, None] * rpt + np.arange(rpt)).ravel()
+    prows = (order.astype(np.int64)[:, None] * rpt + np.arange(rpt)).ravel()
+    n_rows = ntok * rpt
+    whole, sp_l, sp_p = [], [], []
+    for b in np.unique(lrows // 64):
+        sel = lrows // 64 == b
+        if sel.sum() == min(64, n_rows - 64 * b):
+            whole.append((0, b, prows[sel], lrows[sel]))
+        else:
+            sp_l.append(lrows[sel])
+            sp_p.append(prows[sel])
+    sp_l = np.concatenate(sp_l) if sp_l else np.zeros(0, np.int64)
+    sp_p = np.concatenate(sp_p) if sp_p else np.zeros(0, np.int64)
+    items = whole + [(1, -1, sp_p[k:k + 64], sp_l[k:k + 64]) for k in range(0, sp_l.size, 64)]
+    out = np.full((len(items), 132), -1, dtype=np.int32)
+    for i, (kind, b, p, l) in enumerate(items):
+        out[i, :4] = (kind, b, p.size, 0)
+        out[i, 4:4 + p.size] = p
+        out[i, 68:68 + l.size] = l
+    return out, len(whole), int(sp_l.size)
+
+
+@pytest.mark.parametrize("cfg,kind,rpt", [("c0", "permuted", 1), ("c0p", "padded_right", 3), ("c1", "chunked", 1),
+                                          ("c1", "permuted", 1), ("c3", "singleton", 8),
+                                          ("c4", "permuted_slots_left_chunked", 1)])
+def test_plan_bytes_match_the_spelled_out_plan(cfg, kind, rpt):
+    wl = synth.config(cfg)
+    lay = L.workload_layouts(wl, kinds=[kind])[kind]
+    calls = lay.calls[:12] + [np.ascontiguousarray(lay.calls[0][::-1])]      # a descending call too
+    for tok in calls:
+        buf, n, whole, spill = _plan(tok, rpt, wl.n_tokens)
+        ref, ref_whole, ref_spill = _plan_ref(tok, rpt, wl.n_tokens)
+        assert (n, whole, spill) == (ref.shape[0], ref_whole, ref_spill)
+        assert np.array_equal(np.frombuffer(buf.tobytes(), dtype=np.int32).reshape(n, 132), ref)
+
+
+def test_plan_into_caller_buffer_and_capacity():
+    import invariant_rmsnorm_fwd_gb300 as rb
+    tok = np.arange(0, 200, dtype=np.int32)               # N=200: three whole blocks and the short last one
+    out = np.zeros(4 * rb.PLAN_ITEM_BYTES, dtype=np.uint8)
+    buf, n, whole, spill = rb.plan_build(tok, 1, 200, out=out)
+    assert (n, whole, spill) == (4, 4, 0) and np.shares_memory(buf, out)
+    ref = _plan_ref(tok, 1, 200)[0]
+    assert np.array_equal(np.frombuffer(out.tobytes(), dtype=np.int32).reshape(4, 132), ref)
+    with pytest.raises(rb.RmsNormError) as e:
+        rb.plan_build(tok, 1, 200, out=np.zeros(3 * rb.PLAN_ITEM_BYTES, dtype=np.uint8))
+    assert e.value.code == -10
+    with pytest.raises(ValueError):
+        rb.plan_build(tok, 1, 200, out=np.zeros(4 * rb.PLAN_ITEM_BYTES, dtype=np.int32))
