@@ -54,6 +54,8 @@ def parse():
                     help="cut the workload to its first N logical tokens (profiling runs only)")
     ap.add_argument("--e2e-chunk", type=int, default=4096, help="token slots per sub-call of the e2e leg")
     ap.add_argument("--e2e-lanes", type=int, default=1, help="copy streams per direction in the e2e leg")
+    ap.add_argument("--e2e-first", type=int, default=1024,
+                    help="token slots of the first e2e sub-call (doubling up to --e2e-chunk)")
     ap.add_argument("--gemm", action="store_true",
                     help="the linear layer's deterministic weight gradient (in = out = hidden) instead of the norm")
     ap.add_argument("--chain", action="store_true",
@@ -375,29 +377,53 @@ def time_bwd_kernel(step_objs, stream, reps, flush):
     return [a.elapsed_time(b) for a, b in per]
 
 
-def e2e_steps(wl, lay, x_log_host, dy_log_host, w, rpt, steps, warmup, device, chunk_tokens=4096, copy_lanes=1):
-    """Public API with host buffers.  Per step: build the plans on the host, copy token
-    ids, plans and inputs in from pinned memory, run forward, backward and finalize,
-    copy y, dx and dweight back.  Every call of the layout is cut into sub-calls of at
-    most `chunk_tokens` token slots (the outputs do not depend on the physical layout),
-    and the sub-calls are pipelined: copy-in streams, the compute stream, copy-out
-    streams (`copy_lanes` of each, so that several copy engines work at once).
-    Returns (ms per step, h2d bytes, d2h bytes, description)."""
+def e2e_subcalls(lay, chunk_tokens, first_tokens):
+    """Token slots of the sub-calls the end-to-end leg issues, in order.  Every call
+    of the layout is cut into pieces of at most `chunk_tokens` slots, the first
+    pieces growing from `first_tokens` (doubling) so that compute starts after a
+    short first copy; padding slots at either end of a piece are dropped (their
+    rows are neither read nor written by the kernels) and all-padding pieces are
+    skipped.  The outputs do not depend on this cut."""
+    subs = []
+    size = min(first_tokens or chunk_tokens, chunk_tokens)
+    for tok in lay.calls:
+        i = 0
+        while i < tok.size:
+            t = tok[i:i + size]
+            i += size
+            size = min(size * 2, chunk_tokens)
+            act = np.nonzero(t >= 0)[0]
+            if act.size:
+                subs.append(np.ascontiguousarray(t[act[0]:act[-1] + 1], dtype=np.int32))
+    return subs
+
+
+def e2e_steps(wl, lay, norms, steps, warmup, device, chunk_tokens=4096, copy_lanes=1, first_tokens=1024):
+    """Public API with host buffers.  `norms` lists the normed tensors of one step as
+    (rows_per_token, x, dy, weight) with x and dy in logical order on the host (Q
+    and K of a per-head norm are two).  Per step, for every sub-call (see
+    e2e_subcalls) of every tensor, in one pipeline: copy x and dy in from pinned
+    memory, build the plan on the host while they copy, copy token ids and plan
+    in, run forward and fused backward, copy y and dx back; then finalize each
+    dweight and copy it back.  Copy-in streams, the compute stream and copy-out
+    streams (`copy_lanes` of each) overlap.  Returns (ms per step, h2d bytes, d2h
+    bytes, description, per tensor (y, dx, dweight) of the last step gathered to
+    logical order on the host)."""
     import torch
     import invariant_rmsnorm_fwd_gb300 as rb
     H = wl.hidden
     comp = torch.cuda.current_stream()
     s_ins = [torch.cuda.Stream(device=device) for _ in range(copy_lanes)]
     s_outs = [torch.cuda.Stream(device=device) for _ in range(copy_lanes)]
-    subs = []
-    for tok in lay.calls:
-        for i in range(0, max(tok.size, 1), chunk_tokens):
-            t = tok[i:i + chunk_tokens]
-            if t.size and (t >= 0).any():
-                subs.append(np.ascontiguousarray(t, dtype=np.int32))
+    cuts = e2e_subcalls(lay, chunk_tokens, first_tokens)
+    subs = []                                   # (tensor index, token slots), tensors interleaved
+    for tok in cuts:
+        for n in range(len(norms)):
+            subs.append((n, tok))
     # the caller's pinned host data, laid out physically per sub-call
-    host = []
-    for tok in subs:
+    host, dev, meta_h, meta_d = [], [], [], []
+    for n, tok in subs:
+        rpt, x_log_host, dy_log_host, _ = norms[n]
         act = tok >= 0
         xh = torch.zeros((tok.size, rpt, H), dtype=torch.bfloat16).pin_memory()
         dh = torch.zeros_like(xh).pin_memory()
@@ -405,64 +431,57 @@ def e2e_steps(wl, lay, x_log_host, dy_log_host, w, rpt, steps, warmup, device, c
         xh[torch.as_tensor(act)] = x_log_host[idx]
         dh[torch.as_tensor(act)] = dy_log_host[idx]
         host.append((xh, dh, torch.empty_like(xh).pin_memory(), torch.empty_like(xh).pin_memory()))
-    dev = [tuple(torch.empty(xh.shape, dtype=torch.bfloat16, device=device) for _ in range(4))
-           for xh, _, _, _ in host]
-    # token ids and plans: pinned staging and device copies, sized for the largest sub-call
-    cap = [max(int(np.ceil(t.size * rpt / 64)) * 2 + 2, 1) * rb.PLAN_ITEM_BYTES for t in subs]
-    meta_h = [(torch.empty(t.size, dtype=torch.int32).pin_memory(), torch.empty(c, dtype=torch.uint8).pin_memory())
-              for t, c in zip(subs, cap)]
-    meta_d = [(torch.empty(t.size, dtype=torch.int32, device=device), torch.empty(c, dtype=torch.uint8, device=device))
-              for t, c in zip(subs, cap)]
-    ws = rb.DweightWorkspace(wl.n_tokens * rpt, H, device=device)
-    dw_d = torch.empty(H, dtype=torch.float32, device=device)
-    dw_h = torch.empty(H, dtype=torch.float32).pin_memory()
+        dev.append(tuple(torch.empty(xh.shape, dtype=torch.bfloat16, device=device) for _ in range(4)))
+        cap = max(int(np.ceil(tok.size * rpt / 64)) * 2 + 2, 1) * rb.PLAN_ITEM_BYTES
+        meta_h.append((torch.empty(tok.size, dtype=torch.int32).pin_memory(),
+                       torch.empty(cap, dtype=torch.uint8).pin_memory()))
+        meta_d.append((torch.empty(tok.size, dtype=torch.int32, device=device),
+                       torch.empty(cap, dtype=torch.uint8, device=device)))
+    wss = [rb.DweightWorkspace(wl.n_tokens * rpt, H, device=device) for rpt, _, _, _ in norms]
+    dw_d = [torch.empty(H, dtype=torch.float32, device=device) for _ in norms]
+    dw_h = [torch.empty(H, dtype=torch.float32).pin_memory() for _ in norms]
     counts = {}
 
     def one():
         h2d = d2h = 0
-        cls, ready = [], []
-        for i, (tok, (th, ph), (td, pd), (xh, dh, _, _), (xd, dd, _, _)) in enumerate(
+        for ws in wss:
+            ws.begin(comp)
+        for i, ((n, tok), (th, ph), (td, pd), (xh, dh, yh, dxh), (xd, dd, yd, dxd)) in enumerate(
                 zip(subs, meta_h, meta_d, host, dev)):
-            s_in = s_ins[i % copy_lanes]
+            rpt, _, _, w = norms[n]
+            s_in, s_out = s_ins[i % copy_lanes], s_outs[i % copy_lanes]
             with torch.cuda.stream(s_in):
                 # the bulk copies go first: the host builds this sub-call's plan while they run
                 xd.copy_(xh, non_blocking=True)
                 dd.copy_(dh, non_blocking=True)
-                h2d += xh.numel() * 2 * 2
                 pbytes, items, whole, spill = rb.plan_build(tok, rpt, lay.n_logical_tokens, out=ph.numpy())
                 th.numpy()[:] = tok
-                cls.append(rb.CallLayout(td, pd, items, tok.size, rpt, lay.n_logical_tokens, whole, spill))
-                h2d += tok.nbytes + pbytes.size
                 td.copy_(th, non_blocking=True)
                 pd[:pbytes.size].copy_(ph[:pbytes.size], non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(s_in)
-                ready.append(e)
-        ws.begin(comp)
-        done = []
-        for cl, e, (xd, dd, yd, dxd) in zip(cls, ready, dev):
-            comp.wait_event(e)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            h2d += xh.numel() * 2 * 2 + tok.nbytes + pbytes.size
+            cl = rb.CallLayout(td, pd, items, tok.size, rpt, lay.n_logical_tokens, whole, spill)
+            comp.wait_event(ready)
             rb.rmsnorm_fwd(xd, w, cl, wl.eps, y=yd, stream=comp)
             e1 = torch.cuda.Event()
             e1.record(comp)                        # y can leave while the backward runs
-            rb.rmsnorm_bwd_dx(xd, w, dd, cl, wl.eps, dx=dxd, workspace=ws, stream=comp)
+            rb.rmsnorm_bwd_dx(xd, w, dd, cl, wl.eps, dx=dxd, workspace=wss[n], stream=comp)
             e2 = torch.cuda.Event()
             e2.record(comp)
-            done.append((e1, e2))
-        ws.finalize(dw_d, comp)
-        fin = torch.cuda.Event()
-        fin.record(comp)
-        for i, ((e1, e2), (_, _, yh, dxh), (_, _, yd, dxd)) in enumerate(zip(done, host, dev)):
-            s_out = s_outs[i % copy_lanes]
             with torch.cuda.stream(s_out):
                 s_out.wait_event(e1)
                 yh.copy_(yd, non_blocking=True)
                 s_out.wait_event(e2)
                 dxh.copy_(dxd, non_blocking=True)
-                d2h += yd.numel() * 2 * 2
-        with torch.cuda.stream(s_outs[0]):
-            s_outs[0].wait_event(fin)
-            dw_h.copy_(dw_d, non_blocking=True)
+            d2h += yd.numel() * 2 * 2
+        for ws, dd_, dh_ in zip(wss, dw_d, dw_h):
+            ws.finalize(dd_, comp)
+            fin = torch.cuda.Event()
+            fin.record(comp)
+            with torch.cuda.stream(s_outs[0]):
+                s_outs[0].wait_event(fin)
+                dh_.copy_(dd_, non_blocking=True)
             d2h += H * 4
         torch.cuda.synchronize()
         counts["h2d"], counts["d2h"] = h2d, d2h
@@ -474,10 +493,23 @@ def e2e_steps(wl, lay, x_log_host, dy_log_host, w, rpt, steps, warmup, device, c
         t0 = time.perf_counter()
         one()
         ts.append((time.perf_counter() - t0) * 1e3)
-    desc = (f"{len(subs)} sub-calls of <= {chunk_tokens} token slots, pipelined over {copy_lanes} copy-in "
-            f"streams, the compute stream and {copy_lanes} copy-out streams; plans built on the host every step, "
-            f"each while its sub-call's inputs are copied")
-    return statistics.median(ts), counts["h2d"], counts["d2h"], desc
+    outs = []
+    for n, (rpt, _, _, _) in enumerate(norms):
+        y = torch.zeros((wl.n_tokens, rpt, H), dtype=torch.bfloat16)
+        dx = torch.zeros_like(y)
+        for (m, tok), (_, _, yh, dxh) in zip(subs, host):
+            if m == n:
+                act = torch.as_tensor(tok >= 0)
+                idx = torch.as_tensor(tok[tok >= 0]).long()
+                y[idx] = yh[act]
+                dx[idx] = dxh[act]
+        outs.append((y, dx, dw_h[n].clone()))
+    sizes = sorted({int(t.size) for t in cuts})
+    desc = (f"{len(subs)} sub-calls ({len(cuts)} per normed tensor, token slots from {sizes[0]} to {sizes[-1]}: "
+            f"the first ones ramp up from {first_tokens}, at most {chunk_tokens}, padding at their ends not "
+            f"copied), pipelined over {copy_lanes} copy-in streams, the compute stream and {copy_lanes} "
+            f"copy-out streams; every plan built on the host each step while its sub-call's inputs copy")
+    return statistics.median(ts), counts["h2d"], counts["d2h"], desc, outs
 
 
 def cpu_baseline(wl, x_log, dy_log, w, rpt, seconds):
@@ -695,19 +727,17 @@ def main():
         line["config"]["chain"] = ("h = bf16(x + r), y = RMSNorm(h); dh = bf16(dx/D + dres), dweight/D; "
                                    "D = active tokens of the multiset")
     if rank == 0 and not args.no_e2e and not args.chain:
-        x_h = [d[1].cpu() for d in steps_data]
-        dy_h = [d[2].cpu() for d in steps_data]
-        tot_ms, tot_in, tot_out = 0.0, 0, 0
-        desc = ""
-        for (rpt, x, dy, w), xh, dh in zip(steps_data, x_h, dy_h):
-            e_ms, bi, bo, desc = e2e_steps(wl, lay, xh, dh, w, rpt, max(3, args.steps // 4), 2, device,
-                                           args.e2e_chunk, args.e2e_lanes)
-            tot_ms += e_ms
-            tot_in += bi
-            tot_out += bo
+        norms = [(d[0], d[1].cpu(), d[2].cpu(), d[3]) for d in steps_data]
+        tot_ms, tot_in, tot_out, desc, e2e_out = e2e_steps(wl, lay, norms, max(3, args.steps // 4), 2, device,
+                                                           args.e2e_chunk, args.e2e_lanes, args.e2e_first)
+        # the host-buffer path must give the device path's outputs bit for bit
+        e2e_bitwise = True
+        for s_obj, got in zip(step_objs, e2e_out):
+            for a, b in zip(s_obj.gather(wl.n_tokens), got):
+                e2e_bitwise &= harness.bitwise_diff("t", a.cpu(), b, "e2e", "device").equal
         line["e2e"] = {"value": round(n_act / (tot_ms * 1e-3) * world, 1), "unit": "tokens/s",
                        "h2d_bytes_per_step": int(tot_in), "d2h_bytes_per_step": int(tot_out),
-                       "ms_per_step": round(tot_ms, 3), "pipeline": desc,
+                       "ms_per_step": round(tot_ms, 3), "pipeline": desc, "bitwise_vs_device_path": bool(e2e_bitwise),
                        "link_gbs": round((tot_in + tot_out) / (tot_ms * 1e-3) / 1e9, 1)}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.chain:

@@ -52,3 +52,22 @@ def test_parse_defaults_run_one_gpu_briefly():
         sys.argv = old
     assert args.gpus == 1 and args.steps >= 1 and args.warmup >= 3 and args.impl == "ours"
     assert args.config == "c1" and not args.chain and not args.gemm
+
+
+def test_e2e_subcalls_cover_every_token_once_and_ramp():
+    from invariant_rmsnorm_fwd_gb300 import layout as L
+    b = _bench()
+    for cfg, kind in (("c1", "full"), ("c2", "padded_right_chunked"), ("c4", "permuted_slots_left_chunked"),
+                      ("c0", "padded_left")):
+        wl = synth.config(cfg)
+        lay = L.workload_layouts(wl, kinds=[kind])[kind]
+        subs = b.e2e_subcalls(lay, 4096, 1024)
+        ids = np.concatenate([t[t >= 0] for t in subs])
+        assert np.array_equal(np.sort(ids), np.arange(wl.n_tokens))
+        assert all(t.size <= 4096 and t[0] >= 0 and t[-1] >= 0 for t in subs)
+        # padding dropped at the ends only: the slots kept are contiguous pieces of the calls
+        n_pad = sum(int((t < 0).sum()) for t in subs)
+        assert n_pad <= sum(int((c < 0).sum()) for c in lay.calls)
+    wl = synth.config("c1")
+    sizes = [t.size for t in b.e2e_subcalls(L.workload_layouts(wl, kinds=["full"])["full"], 4096, 1024)]
+    assert sizes[:3] == [1024, 2048, 4096] and sum(sizes) == wl.n_tokens
