@@ -54,7 +54,7 @@ def parse():
                     help="cut the workload to its first N logical tokens (profiling runs only)")
     ap.add_argument("--e2e-chunk", type=int, default=4096, help="token slots per sub-call of the e2e leg")
     ap.add_argument("--e2e-lanes", type=int, default=1, help="copy streams per direction in the e2e leg")
-    ap.add_argument("--e2e-first", type=int, default=1024,
+    ap.add_argument("--e2e-first", type=int, default=2048,
                     help="token slots of the first e2e sub-call (doubling up to --e2e-chunk)")
     ap.add_argument("--gemm", action="store_true",
                     help="the linear layer's deterministic weight gradient (in = out = hidden) instead of the norm")
@@ -398,7 +398,7 @@ def e2e_subcalls(lay, chunk_tokens, first_tokens):
     return subs
 
 
-def e2e_steps(wl, lay, norms, steps, warmup, device, chunk_tokens=4096, copy_lanes=1, first_tokens=1024):
+def e2e_steps(wl, lay, norms, steps, warmup, device, chunk_tokens=4096, copy_lanes=1, first_tokens=2048):
     """Public API with host buffers.  `norms` lists the normed tensors of one step as
     (rows_per_token, x, dy, weight) with x and dy in logical order on the host (Q
     and K of a per-head norm are two).  Per step, for every sub-call (see
@@ -728,7 +728,7 @@ def main():
                                    "D = active tokens of the multiset")
     if rank == 0 and not args.no_e2e and not args.chain:
         norms = [(d[0], d[1].cpu(), d[2].cpu(), d[3]) for d in steps_data]
-        tot_ms, tot_in, tot_out, desc, e2e_out = e2e_steps(wl, lay, norms, max(3, args.steps // 4), 2, device,
+        tot_ms, tot_in, tot_out, desc, e2e_out = e2e_steps(wl, lay, norms, max(10, args.steps), 3, device,
                                                            args.e2e_chunk, args.e2e_lanes, args.e2e_first)
         # the host-buffer path must give the device path's outputs bit for bit
         e2e_bitwise = True
