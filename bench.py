@@ -512,7 +512,7 @@ def e2e_steps(wl, lay, norms, steps, warmup, device, chunk_tokens=4096, copy_lan
     return statistics.median(ts), counts["h2d"], counts["d2h"], desc, outs
 
 
-def cpu_baseline(wl, x_log, dy_log, w, rpt, seconds):
+def cpu_baseline(wl, x_log, dy_log, w, seconds):
     """The FP64 oracle as it stands (single-threaded C) on a bounded sample of rows."""
     import oracle
     H = wl.hidden
@@ -531,10 +531,12 @@ def cpu_baseline(wl, x_log, dy_log, w, rpt, seconds):
         done += r1 - r0
         r0 = 0 if r1 >= n else r1
     dt = time.perf_counter() - t0
-    tokens = done / rpt
+    rows_per_token = sum(wl.heads)              # every normed tensor of a token (Q and K heads)
+    tokens = done / rows_per_token
     return {"value": tokens / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{done} logical rows of hidden {H} (fwd + bwd incl. dweight, FP64 C, "
-                      f"single thread) in {dt:.1f} s, cycled over the first rows of the workload"}
+                      f"single thread) in {dt:.1f} s, cycled over the first rows of the workload; "
+                      f"a token is {rows_per_token} such rows"}
 
 
 def main():
@@ -741,10 +743,9 @@ def main():
                        "link_gbs": round((tot_in + tot_out) / (tot_ms * 1e-3) / 1e9, 1)}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.chain:
-        rpt, x, dy, w = steps_data[0][:4]
+        _, x, dy, w = steps_data[0][:4]
         n_cpu = min(x.shape[0], 4096)
-        line["cpu_baseline"] = cpu_baseline(wl, x[:n_cpu].cpu(), dy[:n_cpu].cpu(), w.cpu(), rpt,
-                                            args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(wl, x[:n_cpu].cpu(), dy[:n_cpu].cpu(), w.cpu(), args.cpu_seconds)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -845,8 +846,10 @@ def reference_arm(args, rank, world):
         return
     import torch
     import synth
+    from invariant_rmsnorm_fwd_gb300 import layout as L
     wl = synth.config(args.config)
     lay_name = args.layout or wl.headline
+    lay = L.workload_layouts(wl, kinds=[lay_name])[lay_name]
     rpt = wl.heads[0]
     n_rows = min(wl.n_tokens * rpt, max(64, (1 << 21) // wl.hidden))
     x = synth.logical_tensor(wl, synth.TAG_X, n_rows, wl.x_std, 0)
@@ -866,16 +869,20 @@ def reference_arm(args, rank, world):
             done += n_rows
         times.append(time.perf_counter() - t0)
         rows_done.append(done)
-    tok_s = (sum(rows_done) / rpt) / sum(times)
+    rows_per_token = sum(wl.heads)              # every normed tensor of a token (Q and K heads)
+    tok_s = (sum(rows_done) / rows_per_token) / sum(times)
     sample = (f"{n_rows} logical rows of {wl.name} (hidden {wl.hidden}) repeated for ~{per_step:.1f} s per step; "
-              f"FP64 C oracle, single thread")
+              f"a token is {rows_per_token} such rows; FP64 C oracle, single thread")
     ms = statistics.mean(times) * 1e3
     line = {"metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{wl.name}: hidden={wl.hidden}, layout={lay_name} (oracle works in logical order)",
-                       "hidden": wl.hidden, "tokens": wl.n_tokens},
+            "config": {"workload": workload_desc(wl, lay_name, lay.n_physical), "hidden": wl.hidden,
+                       "heads": list(wl.heads), "tokens": wl.n_tokens, "layout": lay_name, "calls": len(lay.calls),
+                       "l2": "not applicable: the oracle runs on the host, in logical order",
+                       "launch": "oracle calls on the host (FP64 C, one thread)",
+                       "parallelism": "single host thread"},
             "cpu_baseline": {"value": round(tok_s, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(tok_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
