@@ -38,9 +38,9 @@ __global__ void ws_begin_kernel(WsView ws) {
 // In the first pass (from_blocks) an input is a block partial: the four
 // quarter partials as (q0 + q1) + (q2 + q3) (levels 5 and 6 of the 64-leaf
 // tree), a whole-block partial as is, or, for a block cut by a call boundary,
-// the 64-leaf tree over its spilled rows, rebuilt by the whole warp (lane l
-// adds rows 2l and 2l+1, then butterflies xor 1..16): the same tree as the
-// in-kernel path.
+// the 64-leaf tree over its spilled rows, rebuilt by each lane for its own
+// 8-column vector (pairs (0,1), (2,3), ... at every level): the same tree as
+// the in-kernel path.
 __device__ __forceinline__ void load8(const float *src, float (&v)[8]) {
     const float4 a = ld_global_f32x4(src), b = ld_global_f32x4(src + 4);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
@@ -117,30 +117,40 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, c
         } else if (state == kStateWhole) {
             if (has_vec) load8(ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8, val);
         } else if (state == 0) {
-            // cut block: the warp rebuilds it vector by vector; lane l adds rows 2l, 2l+1
+            // cut block: each lane rebuilds its own vector from the spilled rows,
+            // eight rows per step with all their loads in flight (levels 1-3 of the
+            // tree over those eight, then the carry stack from level 3 up)
             const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
             const int64_t r0 = b * kBlockRows + 2 * lane;
             const bool have0 = 2 * lane < rows, have1 = 2 * lane + 1 < rows;
             const bool missing = (have0 && ws.leaf_flag[r0] == 0) || (have1 && ws.leaf_flag[r0 + 1] == 0);
             if (__any_sync(kFull, missing) && lane == 0 && blockIdx.y == 0) set_status(ws.hdr, kStMissing);
+            if (has_vec) {
+                const float *src = ws.spill + b * kBlockRows * int64_t(H) + int64_t(v) * 8;
+                TreeStack<8> st;
 #pragma unroll 1
-            for (int vv = 0; vv < kTreeVecs; ++vv) {
-                const int vg = blockIdx.y * kTreeVecs + vv;
-                if (vg >= V) break;                      // uniform
-                float a[8], c2[8];
+                for (int r = 0; r < kBlockRows; r += 8) {
+                    float x[8][8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) a[c] = c2[c] = 0.f;
-                if (have0) load8(ws.spill + r0 * int64_t(H) + int64_t(vg) * 8, a);
-                if (have1) load8(ws.spill + (r0 + 1) * int64_t(H) + int64_t(vg) * 8, c2);
+                    for (int k = 0; k < 8; ++k) {
+                        if (r + k < rows) {
+                            load8(src + int64_t(r + k) * H, x[k]);
+                        } else {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) a[c] = __fadd_rn(a[c], c2[c]);        // level 1
+                            for (int c = 0; c < 8; ++c) x[k][c] = 0.f;     // leaves past the multiset
+                        }
+                    }
 #pragma unroll
-                for (int k = 1; k < 32; k <<= 1)
+                    for (int c = 0; c < 8; ++c) {
+                        const float a01 = __fadd_rn(x[0][c], x[1][c]), a23 = __fadd_rn(x[2][c], x[3][c]);
+                        const float a45 = __fadd_rn(x[4][c], x[5][c]), a67 = __fadd_rn(x[6][c], x[7][c]);
+                        x[0][c] = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
+                    }
+                    st.push(x[0], r >> 3, 3);
+                    if (r == kBlockRows - 8) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) a[c] = __fadd_rn(a[c], __shfl_xor_sync(kFull, a[c], k));
-                if (lane == vv) {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) val[c] = a[c];
+                        for (int c = 0; c < 8; ++c) val[c] = x[0][c];           // the whole block
+                    }
                 }
             }
         } else {
