@@ -153,6 +153,16 @@ class CallLayout:
     spill_rows: int = 0
 
     def struct(self, token_stride: int) -> _Layout:
+        torch = _torch()
+        if self.n_tokens:
+            _cuda_tensor(self.tok_id, "layout.tok_id", torch.int32)
+            if self.tok_id.numel() != self.n_tokens or not self.tok_id.is_contiguous():
+                raise ValueError(f"layout.tok_id: expected {self.n_tokens} contiguous ids")
+        if self.plan is not None and self.plan_items:
+            _cuda_tensor(self.plan, "layout.plan", torch.uint8, self.tok_id.device)
+            if self.plan.numel() < self.plan_items * PLAN_ITEM_BYTES or not self.plan.is_contiguous():
+                raise ValueError(f"layout.plan: {self.plan_items} items need {self.plan_items * PLAN_ITEM_BYTES} "
+                                 f"contiguous bytes")
         return _Layout(self.n_tokens, self.rows_per_token, 0, token_stride,
                        self.tok_id.data_ptr() if self.n_tokens else None,
                        self.n_logical_tokens,
@@ -176,22 +186,88 @@ def call_layout(tok_id: np.ndarray, rows_per_token: int, n_logical_tokens: int, 
 
 # ------------------------------------------------------------------ ops
 
-def _rows_view(t, rpt: int, hidden: int):
-    """Token stride in elements of a [n_tokens, rpt*hidden] or [n_tokens, rpt, hidden] tensor."""
+def _torch():
+    import torch
+    return torch
+
+
+def _cuda_tensor(t, name: str, dtype, device=None):
+    """Raise unless t is a CUDA tensor of `dtype` (on `device` when given): the
+    library takes raw device pointers and cannot tell a host buffer or another
+    element type from the right one."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, the call's layout is on {device}")
+
+
+def _rows_view(t, name: str, lay: "CallLayout", hidden: int) -> int:
+    """Token stride (elements) of a bf16 [T, rows_per_token, hidden] or
+    [T, rows_per_token * hidden] tensor whose first n_tokens token slots are the
+    call's (T >= n_tokens; the library touches no slot past n_tokens)."""
+    torch = _torch()
+    _cuda_tensor(t, name, torch.bfloat16, lay.tok_id.device if lay.n_tokens else None)
+    rpt = lay.rows_per_token
     if t.dim() == 3:
-        assert t.shape[1] == rpt and t.shape[2] == hidden and t.stride(2) == 1 and t.stride(1) == hidden
+        ok = t.shape[1] == rpt and t.shape[2] == hidden and t.stride(2) == 1 and t.stride(1) == hidden
+    elif t.dim() == 2:
+        ok = t.shape[1] == rpt * hidden and t.stride(1) == 1
     else:
-        assert t.dim() == 2 and t.shape[1] == rpt * hidden and t.stride(1) == 1
+        ok = False
+    if not ok:
+        raise ValueError(f"{name}: expected [n_tokens, {rpt}, {hidden}] or [n_tokens, {rpt * hidden}] with "
+                         f"unit column stride, got shape {tuple(t.shape)} strides {t.stride()}")
+    if t.shape[0] < lay.n_tokens:
+        raise ValueError(f"{name}: {t.shape[0]} token slots, the call's layout has {lay.n_tokens}")
     return t.stride(0)
+
+
+def _same_stride(stride: int, *named):
+    for name, t in named:
+        if t is not None and t.stride(0) != stride:
+            raise ValueError(f"{name}: token stride {t.stride(0)} differs from x's {stride} (one stride per call)")
+
+
+def _weight(weight, lay: "CallLayout") -> int:
+    torch = _torch()
+    _cuda_tensor(weight, "weight", torch.bfloat16, lay.tok_id.device if lay.n_tokens else None)
+    if weight.dim() != 1 or not weight.is_contiguous():
+        raise ValueError(f"weight: expected a contiguous [hidden] tensor, got shape {tuple(weight.shape)}")
+    return int(weight.shape[0])
+
+
+def _f32_out(t, name: str, numel: int, device):
+    torch = _torch()
+    _cuda_tensor(t, name, torch.float32, device)
+    if not t.is_contiguous() or t.numel() < numel:
+        raise ValueError(f"{name}: expected a contiguous float32 tensor of at least {numel} elements")
+
+
+def _workspace(ws, cls, device):
+    if ws is None:
+        return None
+    if not isinstance(ws, cls):
+        raise TypeError(f"workspace: expected {cls.__name__}, got {type(ws).__name__}")
+    if device is not None and ws.buf.device != device:
+        raise ValueError(f"workspace: on {ws.buf.device}, the call's layout is on {device}")
+    return _ptr(ws.buf)
 
 
 def rmsnorm_fwd(x, weight, lay: CallLayout, eps: float, y=None, rstd=None, stream=None):
     import torch
-    H = weight.shape[0]
+    H = _weight(weight, lay)
+    stride = _rows_view(x, "x", lay, H)
     if y is None:
         y = torch.empty_like(x)
-    stride = _rows_view(x, lay.rows_per_token, H)
-    assert _rows_view(y, lay.rows_per_token, H) == stride
+    _rows_view(y, "y", lay, H)
+    _same_stride(stride, ("y", y))
+    if rstd is not None:
+        _f32_out(rstd, "rstd", lay.n_tokens * lay.rows_per_token, x.device)
     L = lay.struct(stride)
     _check(_load().rmsnorm_fwd(_ptr(x), _ptr(weight), H, eps, ctypes.byref(L), _ptr(y), _ptr(rstd),
                                _stream(stream)), "rmsnorm_fwd")
@@ -201,31 +277,35 @@ def rmsnorm_fwd(x, weight, lay: CallLayout, eps: float, y=None, rstd=None, strea
 def rmsnorm_bwd_dx(x, weight, dy, lay: CallLayout, eps: float, dx=None, workspace=None, stream=None,
                    write_dx: bool = True):
     import torch
-    H = weight.shape[0]
+    H = _weight(weight, lay)
+    stride = _rows_view(x, "x", lay, H)
+    _rows_view(dy, "dy", lay, H)
     if dx is None and write_dx:
         dx = torch.empty_like(dy)
-    stride = _rows_view(x, lay.rows_per_token, H)
-    assert _rows_view(dy, lay.rows_per_token, H) == stride
     if dx is not None:
-        assert _rows_view(dx, lay.rows_per_token, H) == stride
+        _rows_view(dx, "dx", lay, H)
+    _same_stride(stride, ("dy", dy), ("dx", dx))
+    ws = _workspace(workspace, DweightWorkspace, x.device)
     L = lay.struct(stride)
     _check(_load().rmsnorm_bwd_dx(_ptr(x), _ptr(weight), _ptr(dy), H, eps, ctypes.byref(L), _ptr(dx),
-                                  None if workspace is None else _ptr(workspace.buf), _stream(stream)),
-           "rmsnorm_bwd_dx")
+                                  ws, _stream(stream)), "rmsnorm_bwd_dx")
     return dx
 
 
 def rmsnorm_add_fwd(x, residual, weight, lay: CallLayout, eps: float, h=None, y=None, rstd=None, stream=None):
     """Residual add fused with the norm: h = bf16(x + residual), y = RMSNorm(h) * w."""
     import torch
-    H = weight.shape[0]
+    H = _weight(weight, lay)
+    stride = _rows_view(x, "x", lay, H)
     if h is None:
         h = torch.empty_like(x)
     if y is None:
         y = torch.empty_like(x)
-    stride = _rows_view(x, lay.rows_per_token, H)
-    for t in (residual, h, y):
-        assert _rows_view(t, lay.rows_per_token, H) == stride
+    for name, t in (("residual", residual), ("h", h), ("y", y)):
+        _rows_view(t, name, lay, H)
+    _same_stride(stride, ("residual", residual), ("h", h), ("y", y))
+    if rstd is not None:
+        _f32_out(rstd, "rstd", lay.n_tokens * lay.rows_per_token, x.device)
     L = lay.struct(stride)
     _check(_load().rmsnorm_add_fwd(_ptr(x), _ptr(residual), _ptr(weight), H, eps, ctypes.byref(L), _ptr(h),
                                    _ptr(y), _ptr(rstd), _stream(stream)), "rmsnorm_add_fwd")
@@ -237,26 +317,32 @@ def rmsnorm_add_bwd(x, weight, dy, lay: CallLayout, eps: float, dres=None, grad_
     """dx = bf16(grad_scale * (norm backward) + dres); x is the saved h.  The
     dweight contribution to `workspace` stays unscaled (scale it at finalize)."""
     import torch
-    H = weight.shape[0]
+    H = _weight(weight, lay)
+    stride = _rows_view(x, "x", lay, H)
+    _rows_view(dy, "dy", lay, H)
     if dx is None:
         dx = torch.empty_like(dy)
-    stride = _rows_view(x, lay.rows_per_token, H)
-    for t in (dy, dx) + (() if dres is None else (dres,)):
-        assert _rows_view(t, lay.rows_per_token, H) == stride
+    _rows_view(dx, "dx", lay, H)
+    if dres is not None:
+        _rows_view(dres, "dres", lay, H)
+    _same_stride(stride, ("dy", dy), ("dx", dx), ("dres", dres))
+    ws = _workspace(workspace, DweightWorkspace, x.device)
     L = lay.struct(stride)
     _check(_load().rmsnorm_add_bwd(_ptr(x), _ptr(weight), _ptr(dy), _ptr(dres), H, eps, float(grad_scale),
-                                   ctypes.byref(L), _ptr(dx),
-                                   None if workspace is None else _ptr(workspace.buf), _stream(stream)),
-           "rmsnorm_add_bwd")
+                                   ctypes.byref(L), _ptr(dx), ws, _stream(stream)), "rmsnorm_add_bwd")
     return dx
 
 
 def rmsnorm_bwd_dweight_contrib(x, dy, hidden: int, lay: CallLayout, eps: float, workspace, stream=None):
-    stride = _rows_view(x, lay.rows_per_token, hidden)
+    stride = _rows_view(x, "x", lay, hidden)
+    _rows_view(dy, "dy", lay, hidden)
+    _same_stride(stride, ("dy", dy))
+    if workspace is None:
+        raise ValueError("workspace: required")
+    ws = _workspace(workspace, DweightWorkspace, x.device)
     L = lay.struct(stride)
-    _check(_load().rmsnorm_bwd_dweight_contrib(_ptr(x), _ptr(dy), hidden, eps, ctypes.byref(L),
-                                               _ptr(workspace.buf), _stream(stream)),
-           "rmsnorm_bwd_dweight_contrib")
+    _check(_load().rmsnorm_bwd_dweight_contrib(_ptr(x), _ptr(dy), hidden, eps, ctypes.byref(L), ws,
+                                               _stream(stream)), "rmsnorm_bwd_dweight_contrib")
 
 
 class DweightWorkspace:
@@ -270,7 +356,8 @@ class DweightWorkspace:
         if self.bytes == 0:
             raise RmsNormError(-5, "rmsnorm_dweight_workspace_bytes")
         self.buf = torch.empty(self.bytes, dtype=torch.uint8, device=device)
-        assert self.buf.data_ptr() % 256 == 0
+        if self.buf.data_ptr() % 256:
+            raise RuntimeError("workspace allocation is not 256-byte aligned")
 
     def begin(self, stream=None):
         _check(_load().rmsnorm_dweight_begin(_ptr(self.buf), self.bytes, self.n_rows, self.hidden,
@@ -281,6 +368,7 @@ class DweightWorkspace:
         import torch
         if dweight is None:
             dweight = torch.empty(self.hidden, dtype=torch.float32, device=self.buf.device)
+        _f32_out(dweight, "dweight", self.hidden, self.buf.device)
         if grad_scale is None:
             _check(_load().dweight_finalize(_ptr(self.buf), self.n_rows, self.hidden, _ptr(dweight),
                                             _stream(stream)), "dweight_finalize")
@@ -295,6 +383,7 @@ class DweightWorkspace:
         import torch
         if root is None:
             root = torch.empty(self.hidden, dtype=torch.float32, device=self.buf.device)
+        _f32_out(root, "root", self.hidden, self.buf.device)
         _check(_load().dweight_finalize_range(_ptr(self.buf), self.n_rows, self.hidden, int(block_lo),
                                               int(block_count), _ptr(root), _stream(stream)),
                "dweight_finalize_range")
@@ -315,10 +404,13 @@ def dweight_combine(roots, dweight=None, stream=None, grad_scale: float = 1.0):
     """Carry tree over FP32 roots [n, H] (device), the top of the dweight tree,
     the result multiplied once by grad_scale."""
     import torch
+    _cuda_tensor(roots, "roots", torch.float32)
+    if roots.dim() != 2 or not roots.is_contiguous():
+        raise ValueError(f"roots: expected a contiguous [n, hidden] tensor, got shape {tuple(roots.shape)}")
     n, H = roots.shape
-    assert roots.is_contiguous() and roots.dtype == torch.float32
     if dweight is None:
         dweight = torch.empty(H, dtype=torch.float32, device=roots.device)
+    _f32_out(dweight, "dweight", H, roots.device)
     _check(_load().dweight_combine(_ptr(roots), n, H, float(grad_scale), _ptr(dweight), _stream(stream)),
            "dweight_combine")
     return dweight
@@ -336,7 +428,8 @@ class GemmDwWorkspace:
         if self.bytes == 0:
             raise RmsNormError(-2, "gemm_dw_workspace_bytes")
         self.buf = torch.empty(self.bytes, dtype=torch.uint8, device=device)
-        assert self.buf.data_ptr() % 256 == 0
+        if self.buf.data_ptr() % 256:
+            raise RuntimeError("workspace allocation is not 256-byte aligned")
 
     def begin(self, stream=None):
         _check(_load().gemm_dw_begin(_ptr(self.buf), self.bytes, self.n, self.i, self.o, _stream(stream)),
@@ -344,8 +437,18 @@ class GemmDwWorkspace:
 
     def contrib(self, x, dy, lay: CallLayout, stream=None):
         """Places one call's tokens: x [T, I] and dy [T, O] (row strides taken from the tensors)."""
-        assert x.dim() == 2 and dy.dim() == 2 and x.shape[1] == self.i and dy.shape[1] == self.o
-        assert x.stride(1) == 1 and dy.stride(1) == 1 and x.shape[0] == dy.shape[0] == lay.n_tokens
+        torch = _torch()
+        dev = self.buf.device
+        _cuda_tensor(x, "x", torch.bfloat16, dev)
+        _cuda_tensor(dy, "dy", torch.bfloat16, dev)
+        if not (x.dim() == 2 and dy.dim() == 2 and x.shape[1] == self.i and dy.shape[1] == self.o
+                and x.stride(1) == 1 and dy.stride(1) == 1):
+            raise ValueError(f"x [T, {self.i}] and dy [T, {self.o}] with unit column stride expected, got "
+                             f"{tuple(x.shape)} / {tuple(dy.shape)}")
+        if min(x.shape[0], dy.shape[0]) < lay.n_tokens:
+            raise ValueError(f"x and dy hold {x.shape[0]} / {dy.shape[0]} token slots, the layout {lay.n_tokens}")
+        if lay.n_tokens and lay.tok_id.device != dev:
+            raise ValueError(f"layout on {lay.tok_id.device}, workspace on {dev}")
         L = lay.struct(x.stride(0))
         _check(_load().gemm_dw_contrib(_ptr(x), x.stride(0), _ptr(dy), dy.stride(0), self.i, self.o,
                                        ctypes.byref(L), _ptr(self.buf), _stream(stream)), "gemm_dw_contrib")
@@ -354,6 +457,7 @@ class GemmDwWorkspace:
         import torch
         if dw is None:
             dw = torch.empty(self.o, self.i, dtype=torch.float32, device=self.buf.device)
+        _f32_out(dw, "dw", self.o * self.i, self.buf.device)
         _check(_load().gemm_dw_finalize(_ptr(self.buf), self.n, self.i, self.o, float(grad_scale), _ptr(dw),
                                         _stream(stream)), "gemm_dw_finalize")
         return dw
@@ -372,10 +476,17 @@ def rmsnorm_bwd_noalloc(x, weight, dy, lay: CallLayout, eps: float, dx=None, dwe
     """Backward with dweight for one call, using the library's built-in scratch
     instead of a workspace (see rmsnorm_bwd_noalloc in the C header)."""
     import torch
-    H = weight.shape[0]
+    H = _weight(weight, lay)
+    stride = _rows_view(x, "x", lay, H)
+    _rows_view(dy, "dy", lay, H)
+    if dx is not None:
+        _rows_view(dx, "dx", lay, H)
+    _same_stride(stride, ("dy", dy), ("dx", dx))
     if dweight is None:
         dweight = torch.empty(H, dtype=torch.float32, device=x.device)
-    stride = _rows_view(x, lay.rows_per_token, H)
+    _f32_out(dweight, "dweight", H, x.device)
+    if status is not None:
+        _cuda_tensor(status, "status", torch.int32, x.device)
     L = lay.struct(stride)
     _check(_load().rmsnorm_bwd_noalloc(_ptr(x), _ptr(weight), _ptr(dy), H, eps, ctypes.byref(L), _ptr(dx),
                                        _ptr(dweight), _ptr(status), _stream(stream)), "rmsnorm_bwd_noalloc")
