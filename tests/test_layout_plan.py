@@ -182,3 +182,22 @@ def test_plan_into_caller_buffer_and_capacity():
     assert e.value.code == -10
     with pytest.raises(ValueError):
         rb.plan_build(tok, 1, 200, out=np.zeros(4 * rb.PLAN_ITEM_BYTES, dtype=np.int32))
+
+
+def test_plan_build_from_several_threads():
+    """The planner keeps per-thread working arrays: concurrent calls (ctypes
+    releases the GIL) must each get their own call's plan."""
+    import concurrent.futures as cf
+    wl = synth.config("c4")
+    lay = L.workload_layouts(wl, kinds=["permuted_slots_left_chunked"])["permuted_slots_left_chunked"]
+    calls = [c for c in lay.calls if (c >= 0).any()][:24]
+    want = [_plan_ref(c, 1, wl.n_tokens)[0] for c in calls]
+
+    def one(i):
+        buf, n, _, _ = _plan(calls[i], 1, wl.n_tokens)
+        return np.frombuffer(buf.tobytes(), dtype=np.int32).reshape(n, 132)
+
+    with cf.ThreadPoolExecutor(8) as ex:
+        for _ in range(3):
+            got = list(ex.map(one, range(len(calls))))
+            assert all(np.array_equal(g, w) for g, w in zip(got, want))
