@@ -7,13 +7,19 @@ layout: rmsnorm_fwd on every call, rmsnorm_dweight_begin, rmsnorm_bwd_dx
 Inputs are resident in HBM when the timed region starts; L2 is flushed
 before every timed step (a 256 MB write, then a 256 MB read so that no dirty
 lines are left to be written back inside the timed region); each step is
-timed with CUDA events on the launching stream.  `value` is active tokens per second; the roofline
-object reports the dominant kernel (the fused backward) against the measured
-HBM copy bandwidth.  `e2e` is the same metric through the public API with
-host buffers: plans built on the host, inputs copied in from pinned memory
-and y, dx, dweight copied back, all inside the timed region.
+timed with CUDA events on the launching stream.  `value` is active tokens per
+second.  The default workload is c4 in its headline layout (hidden 5120,
+262,144 tokens in 2^20 left-padded slots, 256 calls of 4096 slots), the
+largest one that fits one GPU; the headline layouts of c1, c2 and c3 are
+timed in the same run and reported under `other_workloads`.  The roofline
+object reports the dominant kernel (the fused backward: its launches of one
+step, timed as they run inside the step) against the measured HBM copy
+bandwidth.  `e2e` is the same metric through the public API with host
+buffers: plans built on the host, inputs copied in from pinned memory and y,
+dx, dweight copied back, all inside the timed region.  `cpu_baseline` is the
+FP64 oracle on every host core (one process per core) and on one core.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1] [--layout full]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4] [--layout L] [--also c1,c2,c3]
   python bench.py --impl reference ...   # the FP64 oracle on host cores (reported baseline)
 """
 from __future__ import annotations
@@ -41,7 +47,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="c1")
+    ap.add_argument("--config", default="c4")
+    ap.add_argument("--also", default="c1,c2,c3",
+                    help="other workloads whose headline layouts are timed in the same run (comma list, '' = none)")
     ap.add_argument("--layout", default=None, help="headline layout (default: the workload's)")
     ap.add_argument("--all-layouts", action="store_true", help="also time every layout cell")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -91,16 +99,19 @@ def source_sha256():
 
 
 def recorded_traffic(config: str, layout: str):
-    """DRAM bytes per launch of the fused backward from profiles/traffic.json, or None
-    if it was taken on another workload or the kernels changed since."""
+    """DRAM bytes of the backward phase (the sum over its launches) from
+    profiles/traffic.json, or None if no record is for this workload and layout
+    or the kernels changed since the record was taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(p))
     except Exception:
         return None
-    if d.get("workload") != config or d.get("layout") != layout or d.get("source_sha256") != source_sha256():
-        return None
-    return int(d["dram_bytes_read"]) + int(d["dram_bytes_write"])
+    sha = source_sha256()
+    for rec in d.get("records", [d]):
+        if rec.get("workload") == config and rec.get("layout") == layout and rec.get("source_sha256") == sha:
+            return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+    return None
 
 
 def workload_desc(wl, lay_name, n_phys):
@@ -259,35 +270,37 @@ class Step:
     def finalize(self, st):
         self.ws.finalize(self.dw, st, grad_scale=self.scale)
 
-    def run(self, stream):
+    def _fan(self, fn, stream):
         """Calls of a multi-call layout are independent (they touch disjoint rows and
         blocks of the workspace), so they are spread over n_streams streams (32 by default) that
         fork from and join back into `stream`; one-call layouts stay on `stream`."""
         import torch
-        rb = self.rb
         lanes = self._lanes(stream)
+        if len(lanes) == 1:
+            for c in self.calls:
+                fn(c, stream)
+            return
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        for i, c in enumerate(self.calls):
+            st = lanes[i % len(lanes)]
+            if i < len(lanes):
+                st.wait_event(ev)
+            fn(c, st)
+        for st in lanes[:min(len(lanes), len(self.calls))]:
+            e = torch.cuda.Event()
+            e.record(st)
+            stream.wait_event(e)
 
-        def fan(fn):
-            if len(lanes) == 1:
-                for c in self.calls:
-                    fn(c, stream)
-                return
-            ev = torch.cuda.Event()
-            ev.record(stream)
-            for i, c in enumerate(self.calls):
-                st = lanes[i % len(lanes)]
-                if i < len(lanes):
-                    st.wait_event(ev)
-                fn(c, st)
-            for st in lanes[:min(len(lanes), len(self.calls))]:
-                e = torch.cuda.Event()
-                e.record(st)
-                stream.wait_event(e)
-
-        fan(self.fwd_call)
+    def run(self, stream):
+        self._fan(self.fwd_call, stream)
         self.ws.begin(stream)
-        fan(self.bwd_call)
+        self._fan(self.bwd_call, stream)
         self.finalize(stream)
+
+    def bwd_phase(self, stream):
+        """The backward launches of one step alone (the workspace begun beforehand)."""
+        self._fan(self.bwd_call, stream)
 
     def _lanes(self, stream):
         import torch
@@ -375,6 +388,40 @@ def time_bwd_kernel(step_objs, stream, reps, flush):
             so.finalize(stream)
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in per]
+
+
+def time_bwd_phase(multi, stream, reps, flush):
+    """Duration of the backward phase of one step as it runs inside the step: every
+    fused-backward launch of every normed tensor (all calls of a many-call layout,
+    forked over the step's streams), captured as one CUDA graph and replayed
+    between two CUDA events on the launching stream.  Each workspace is begun
+    (eagerly, outside the events) and L2 is flushed before each replay."""
+    import torch
+    for s in multi.steps:
+        s.ws.begin(stream)
+    multi.bwd_phase(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.graph(g, stream=cap):
+        multi.bwd_phase(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(reps):
+        for s in multi.steps:
+            s.ws.begin(stream)
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    for s in multi.steps:
+        s.finalize(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
 
 
 def e2e_subcalls(lay, chunk_tokens, first_tokens):
@@ -512,31 +559,171 @@ def e2e_steps(wl, lay, norms, steps, warmup, device, chunk_tokens=4096, copy_lan
     return statistics.median(ts), counts["h2d"], counts["d2h"], desc, outs
 
 
-def cpu_baseline(wl, x_log, dy_log, w, seconds):
-    """The FP64 oracle as it stands (single-threaded C) on a bounded sample of rows."""
+def _oracle_rows(x, dy, w, eps, seconds):
+    """Runs the oracle's forward and backward over the rows x, dy (uint16 bf16
+    patterns [n, H]) again and again for about `seconds`; returns (rows done, s)."""
     import oracle
-    H = wl.hidden
-    xr = x_log.reshape(-1, H)
-    dr = dy_log.reshape(-1, H)
-    n = xr.shape[0]
-    chunk = max(1, min(n, (1 << 22) // H))
+    n = x.shape[0]
     done = 0
     t0 = time.perf_counter()
-    r0 = 0
     while time.perf_counter() - t0 < seconds:
-        r1 = min(n, r0 + chunk)
-        xs, ds = xr[r0:r1], dr[r0:r1]
-        oracle.forward(xs, w, wl.eps)
-        oracle.backward(xs, w, ds, wl.eps)
-        done += r1 - r0
-        r0 = 0 if r1 >= n else r1
-    dt = time.perf_counter() - t0
+        oracle.forward(x, w, eps)
+        oracle.backward(x, w, dy, eps)
+        done += n
+    return done, time.perf_counter() - t0
+
+
+def _oracle_worker(job):
+    x, dy, w, eps, seconds = job
+    return _oracle_rows(x, dy, w, eps, seconds)
+
+
+def cpu_baseline(wl, x_log, dy_log, w, seconds):
+    """The FP64 oracle as it stands (plain single-threaded C) on a bounded sample of
+    rows: once on one core, then as one process per host core (spawned, each with
+    its own slice of the sample rows, all running at once).  Returns the all-core
+    figure with the one-core figure beside it."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    import torch
+    H = wl.hidden
+    to_u16 = lambda t: t.reshape(-1, H).contiguous().view(torch.int16).numpy().view(np.uint16)
+    xr, dr = to_u16(x_log), to_u16(dy_log)
+    wu = w.contiguous().view(torch.int16).numpy().view(np.uint16)
+    n = xr.shape[0]
     rows_per_token = sum(wl.heads)              # every normed tensor of a token (Q and K heads)
-    tokens = done / rows_per_token
-    return {"value": tokens / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} logical rows of hidden {H} (fwd + bwd incl. dweight, FP64 C, "
-                      f"single thread) in {dt:.1f} s, cycled over the first rows of the workload; "
-                      f"a token is {rows_per_token} such rows"}
+    chunk = max(1, min(n, (1 << 22) // H))
+    done1, dt1 = _oracle_rows(xr[:chunk], dr[:chunk], wu, wl.eps, seconds)
+    one = done1 / rows_per_token / dt1
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    per = max(1, n // cores)
+    jobs = [(xr[i * per:(i + 1) * per], dr[i * per:(i + 1) * per], wu, wl.eps, seconds) for i in range(cores)]
+    with cf.ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")) as ex:
+        res = list(ex.map(_oracle_worker, jobs))
+    done_all = sum(r[0] for r in res)
+    dt_all = max(r[1] for r in res)
+    allc = done_all / rows_per_token / dt_all
+    return {"value": allc, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "one_core": {"value": one, "unit": "tokens/s", "cores": 1,
+                         "sample": f"{done1} logical rows (the first {chunk}, cycled) in {dt1:.1f} s"},
+            "sample": f"{n} logical rows of hidden {H} (the workload's first rows), fwd + bwd incl. dweight "
+                      f"in the FP64 C oracle (single-threaded code, unchanged): one spawned process per "
+                      f"host core ({cores}), each cycling its own slice of {per} rows for ~{seconds:.0f} s, "
+                      f"{done_all} rows in all; rate = rows / slowest process's time; a token is "
+                      f"{rows_per_token} such rows"}
+
+
+class Multi:
+    """The normed tensors of one step (Q and K of a per-head norm) are
+    independent ops with their own weights and workspaces: they fork onto
+    their own streams and join back, as a model issues them."""
+
+    def __init__(self, steps, device):
+        import torch
+        self.steps = steps
+        self.side = [torch.cuda.Stream(device=device) for _ in steps[1:]]
+
+    def _fork(self, stream, fn):
+        import torch
+        if len(self.steps) == 1:
+            fn(self.steps[0], stream)
+            return
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        for st, s in zip(self.side, self.steps[1:]):
+            st.wait_event(ev)
+            fn(s, st)
+        fn(self.steps[0], stream)
+        for st in self.side:
+            e = torch.cuda.Event()
+            e.record(st)
+            stream.wait_event(e)
+
+    def run(self, stream):
+        self._fork(stream, lambda s, st: s.run(st))
+
+    def bwd_phase(self, stream):
+        self._fork(stream, lambda s, st: s.bwd_phase(st))
+
+
+def workload_data(wl, device, chain=False):
+    """Logical inputs of every normed tensor of a workload: (rows per token, x, dy, w[, r, dres])."""
+    import synth
+    out = []
+    for hs, rpt in enumerate(wl.heads):
+        n_rows = wl.n_tokens * rpt
+        shape = (wl.n_tokens, rpt, wl.hidden)
+        x = synth.logical_tensor(wl, synth.TAG_X, n_rows, wl.x_std, hs, device=device).reshape(shape)
+        dy = synth.logical_tensor(wl, synth.TAG_DY, n_rows, wl.dy_std, hs, device=device).reshape(shape)
+        w = synth.weight(wl, hs, device=device)
+        extra = ()
+        if chain:
+            r = synth.logical_tensor(wl, synth.TAG_RES, n_rows, wl.x_std, hs, device=device)
+            dres = synth.logical_tensor(wl, synth.TAG_DRES, n_rows, wl.dy_std, hs, device=device)
+            extra = (r.reshape(shape), dres.reshape(shape))
+        out.append((rpt, x, dy, w) + extra)
+    return out
+
+
+def measure(wl, lay, data, args, device, flush, stream, hbm_peak, dist=None, sample_clocks=None):
+    """Times one workload in one layout: whole steps (CUDA-graph replays), the
+    backward phase inside the step, each backward launch alone and the forward
+    alone.  Returns (dict of figures, the Multi of steps)."""
+    import torch
+    import invariant_rmsnorm_fwd_gb300 as rb
+    steps = [Step(wl, lay, d[1], d[2], d[3], d[0], device, *d[4:], n_streams=args.streams) for d in data]
+    multi = Multi(steps, device)
+    multi.run(stream)                           # kernels of one step, counted on an eager step
+    torch.cuda.synchronize()
+    l0 = rb.kernel_launches()
+    multi.run(stream)
+    torch.cuda.synchronize()
+    launches = rb.kernel_launches() - l0
+    if sample_clocks is not None:
+        sample_clocks.start()
+    ms, graph = time_steps(multi, stream, args.steps, args.warmup, flush, dist, graph=not args.no_graph)
+    clk = None
+    if sample_clocks is not None:
+        # keep the same step running (untimed) so the clock samples cover the load
+        t_end = time.time() + 0.6
+        while time.time() < t_end:
+            for _ in range(20):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    multi.run(stream)
+            torch.cuda.synchronize()
+        clk = sample_clocks.stop()
+    ms_step = statistics.mean(ms)
+    if dist is not None:
+        t = torch.tensor([ms_step], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    reps = max(3, args.steps // 2)
+    phase_ms = statistics.mean(time_bwd_phase(multi, stream, reps, flush))
+    bwd_ms = time_bwd_kernel(steps, stream, 1 if len(lay.calls) > 16 else reps, flush)
+    fwd_ms = []
+    for _ in range(reps):
+        flush()
+        evs = [s.time_fwd_only(stream) for s in steps]
+        torch.cuda.synchronize()
+        fwd_ms.append(sum(a.elapsed_time(b) for a, b in evs))
+    heff = wl.hidden * sum(wl.heads)
+    n_act = wl.n_tokens
+    fwd_b, bwd_b = (8.0, 8.0) if args.chain else (4.0, 6.0)
+    alg_step = (fwd_b + bwd_b) * heff * n_act
+    alg_bwd = bwd_b * heff * n_act
+    bwd_launches = len(lay.calls) * len(wl.heads)
+    iso_ms = statistics.mean(bwd_ms)
+    r = {"ms_step": ms_step, "launches": int(launches), "clocks": clk, "graph": graph is not None,
+         "tokens_per_s": n_act / (ms_step * 1e-3),
+         "hbm_gbs_step": alg_step / (ms_step * 1e-3) / 1e9,
+         "frac_step": alg_step / (ms_step * 1e-3) / 1e9 / hbm_peak,
+         "bwd_phase_ms": phase_ms, "bwd_alg_bytes": alg_bwd, "bwd_launches": bwd_launches,
+         "bwd_gbs": alg_bwd / (phase_ms * 1e-3) / 1e9,
+         "bwd_iso_launch_ms": iso_ms, "bwd_iso_gbs": alg_bwd / bwd_launches / (iso_ms * 1e-3) / 1e9,
+         "fwd_gbs": fwd_b * heff * n_act / (statistics.mean(fwd_ms) * 1e-3) / 1e9}
+    return r, multi
 
 
 def main():
@@ -552,7 +739,6 @@ def main():
 
     import torch
     import synth
-    import invariant_rmsnorm_fwd_gb300 as rb
     from invariant_rmsnorm_fwd_gb300 import layout as L, harness
 
     torch.cuda.set_device(local)
@@ -572,104 +758,22 @@ def main():
     flush = L2Flush(device)
     stream = torch.cuda.current_stream()
 
-    steps_data = []
-    for hs, rpt in enumerate(rpt_list):
-        n_rows = wl.n_tokens * rpt
-        x = synth.logical_tensor(wl, synth.TAG_X, n_rows, wl.x_std, hs, device=device).reshape(wl.n_tokens, rpt, wl.hidden)
-        dy = synth.logical_tensor(wl, synth.TAG_DY, n_rows, wl.dy_std, hs, device=device).reshape(wl.n_tokens, rpt, wl.hidden)
-        w = synth.weight(wl, hs, device=device)
-        extra = ()
-        if args.chain:
-            r = synth.logical_tensor(wl, synth.TAG_RES, n_rows, wl.x_std, hs, device=device)
-            dres = synth.logical_tensor(wl, synth.TAG_DRES, n_rows, wl.dy_std, hs, device=device)
-            extra = (r.reshape(wl.n_tokens, rpt, wl.hidden), dres.reshape(wl.n_tokens, rpt, wl.hidden))
-        steps_data.append((rpt, x, dy, w) + extra)
-
-    def make_steps(layout_):
-        return [Step(wl, layout_, d[1], d[2], d[3], d[0], device, *d[4:], n_streams=args.streams)
-                for d in steps_data]
-
-    lays = L.workload_layouts(wl, kinds=[lay_name])
-    lay = lays[lay_name]
-    step_objs = make_steps(lay)
-
-    class Multi:
-        """The normed tensors of one step (Q and K of a per-head norm) are
-        independent ops with their own weights and workspaces: they fork onto
-        their own streams and join back, as a model issues them."""
-
-        def __init__(self, steps):
-            self.steps = steps
-            self.side = [torch.cuda.Stream(device=device) for _ in steps[1:]]
-
-        def run(self, stream):
-            if len(self.steps) == 1:
-                self.steps[0].run(stream)
-                return
-            ev = torch.cuda.Event()
-            ev.record(stream)
-            for st, s in zip(self.side, self.steps[1:]):
-                st.wait_event(ev)
-                s.run(st)
-            self.steps[0].run(stream)
-            for st in self.side:
-                e = torch.cuda.Event()
-                e.record(st)
-                stream.wait_event(e)
-
-    multi = Multi(step_objs)
-    # kernels of one step (counted on an eager step)
-    multi.run(stream)
-    torch.cuda.synchronize()
-    l0 = rb.kernel_launches()
-    multi.run(stream)
-    torch.cuda.synchronize()
-    launches = rb.kernel_launches() - l0
-    clocks = ClockSampler(local, args.clock_log)
-    clocks.start()
-    ms, graph = time_steps(multi, stream, args.steps, args.warmup, flush, dist, graph=not args.no_graph)
-    # keep the same step running (untimed) so the clock samples cover the load
-    t_end = time.time() + 0.6
-    while time.time() < t_end:
-        for _ in range(20):
-            if graph is not None:
-                graph.replay()
-            else:
-                multi.run(stream)
-        torch.cuda.synchronize()
-    clk = clocks.stop()
-    ms_step = statistics.mean(ms)
-    if dist is not None:
-        t = torch.tensor([ms_step], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    bwd_ms = time_bwd_kernel(step_objs, stream, max(3, args.steps // 2), flush)
-
+    steps_data = workload_data(wl, device, args.chain)
+    lay = L.workload_layouts(wl, kinds=[lay_name])[lay_name]
+    m, multi = measure(wl, lay, steps_data, args, device, flush, stream, hbm_peak, dist,
+                       ClockSampler(local, args.clock_log))
+    step_objs = multi.steps
+    ms_step = m["ms_step"]
     H = wl.hidden
-    heff = H * sum(rpt_list)
     n_act = wl.n_tokens
-    # algorithmic bytes per token and width: fwd x+y, bwd x+dy+dx (bf16); the chain adds
-    # r and h to the forward and dres to the backward
-    fwd_b, bwd_b = (8.0, 8.0) if args.chain else (4.0, 6.0)
-    alg_step = (fwd_b + bwd_b) * heff * n_act
-    bwd_calls = len(lay.calls) * len(rpt_list)
-    bwd_per_launch_ms = statistics.mean(bwd_ms) if bwd_ms else float("nan")
-    alg_bwd_launch = bwd_b * heff * n_act / bwd_calls
-    achieved_bwd = alg_bwd_launch / (bwd_per_launch_ms * 1e-3) / 1e9
-    tokens_per_s = n_act / (ms_step * 1e-3) * world
-
-    # forward alone, for the record
-    fwd_ms = []
-    for _ in range(max(3, args.steps // 2)):
-        flush()
-        evs = [s.time_fwd_only(stream) for s in step_objs]
-        torch.cuda.synchronize()
-        fwd_ms.append(sum(a.elapsed_time(b) for a, b in evs))
-    fwd_gbs = fwd_b * heff * n_act / (statistics.mean(fwd_ms) * 1e-3) / 1e9
+    bwd_calls = m["bwd_launches"]
+    traffic = recorded_traffic(args.config, lay_name) if not args.chain and not args.max_tokens else None
+    kernel = ("residual-add backward (dh + dweight leaves), rmsnorm_add_bwd" if args.chain
+              else "fused backward (dx + dweight leaves), rmsnorm_bwd_dx")
 
     line = {
         "metric": METRIC,
-        "value": round(tokens_per_s, 1),
+        "value": round(n_act / (ms_step * 1e-3) * world, 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -684,24 +788,29 @@ def main():
         "config": {"workload": workload_desc(wl, lay_name, lay.n_physical), "hidden": H,
                    "heads": list(wl.heads), "tokens": n_act, "layout": lay_name, "calls": len(lay.calls),
                    "l2": "flushed before every timed step (256 MB write, then a 256 MB read so no dirty lines remain); inputs already in HBM",
-                   "launch": "one CUDA graph replay per step" if graph is not None else "eager launches",
+                   "launch": "one CUDA graph replay per step" if m["graph"] else "eager launches",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "hbm_gbs_step": round(alg_step / (ms_step * 1e-3) / 1e9, 1),
-        "frac_step": round(alg_step / (ms_step * 1e-3) / 1e9 / hbm_peak, 4),
-        "fwd_gbs": round(fwd_gbs, 1),
-        "roofline": {"bound": "hbm",
-                     "kernel": ("residual-add backward (dh + dweight leaves), rmsnorm_add_bwd" if args.chain
-                                else "fused backward (dx + dweight leaves), rmsnorm_bwd_dx"),
-                     "achieved": round(achieved_bwd, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved_bwd / hbm_peak, 4),
-                     "traffic": (recorded_traffic(args.config, lay_name) if bwd_calls == 1 and not args.chain
-                                 else None),
+        "hbm_gbs_step": round(m["hbm_gbs_step"], 1),
+        "frac_step": round(m["frac_step"], 4),
+        "fwd_gbs": round(m["fwd_gbs"], 1),
+        "roofline": {"bound": "hbm", "kernel": kernel,
+                     "achieved": round(m["bwd_gbs"], 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(m["bwd_gbs"] / hbm_peak, 4),
+                     "traffic": traffic,
                      "peak_source": peak_kind,
-                     "algorithmic_bytes_per_launch": alg_bwd_launch,
-                     "launch_ms": round(bwd_per_launch_ms, 5)},
-        "gpu_launches": int(launches) * args.steps,
-        "gpu_launches_per_step": int(launches),
-        "clocks": clk,
+                     "algorithmic_bytes": m["bwd_alg_bytes"],
+                     "launches": bwd_calls,
+                     "launch_ms": round(m["bwd_phase_ms"], 5),
+                     "timing": ("the backward phase of the step: all its launches (forked over the step's "
+                                "streams when a layout has several calls), one CUDA-graph replay between "
+                                "CUDA events on the launching stream, L2 flushed before; achieved = "
+                                "algorithmic_bytes / launch_ms"),
+                     "isolated_launch": {"ms": round(m["bwd_iso_launch_ms"], 5),
+                                         "gbs": round(m["bwd_iso_gbs"], 1),
+                                         "how": "each launch alone after an L2 flush, mean over launches"}},
+        "gpu_launches": m["launches"] * args.steps,
+        "gpu_launches_per_step": m["launches"],
+        "clocks": m["clocks"],
     }
 
     if rank == 0 and args.all_layouts:
@@ -709,9 +818,10 @@ def main():
         ref_out = None
         bitwise = True
         for k, v in L.workload_layouts(wl).items():
-            so = make_steps(v)
-            m = Multi(so)
-            t, _ = time_steps(m, stream, max(3, args.steps // 2), 2, flush, graph=not args.no_graph)
+            so = [Step(wl, v, d[1], d[2], d[3], d[0], device, *d[4:], n_streams=args.streams)
+                  for d in steps_data]
+            mm = Multi(so, device)
+            t, _ = time_steps(mm, stream, max(3, args.steps // 2), 2, flush, graph=not args.no_graph)
             per[k] = {"ms": round(statistics.mean(t), 4), "calls": len(v.calls),
                       "tokens_per_s": round(n_act / (statistics.mean(t) * 1e-3), 1)}
             outs = [s.gather(wl.n_tokens) for s in so]
@@ -721,7 +831,7 @@ def main():
                 for a, b in zip(outs, ref_out):
                     for ta, tb in zip(a, b):
                         bitwise &= harness.bitwise_diff("t", ta, tb, k, "ref").equal
-            del so, m
+            del so, mm
         line["layouts"] = per
         line["bitwise_across_layouts"] = bool(bitwise)
 
@@ -741,11 +851,33 @@ def main():
                        "h2d_bytes_per_step": int(tot_in), "d2h_bytes_per_step": int(tot_out),
                        "ms_per_step": round(tot_ms, 3), "pipeline": desc, "bitwise_vs_device_path": bool(e2e_bitwise),
                        "link_gbs": round((tot_in + tot_out) / (tot_ms * 1e-3) / 1e9, 1)}
+        del norms, e2e_out
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.chain:
         _, x, dy, w = steps_data[0][:4]
         n_cpu = min(x.shape[0], 4096)
         line["cpu_baseline"] = cpu_baseline(wl, x[:n_cpu].cpu(), dy[:n_cpu].cpu(), w.cpu(), args.cpu_seconds)
+
+    # the other workloads' headline layouts, measured in the same run (step and backward phase)
+    others = [c for c in (args.also.split(",") if args.also else []) if c and c != args.config]
+    if others and not args.max_tokens:
+        del multi, step_objs, steps_data
+        torch.cuda.empty_cache()
+        per_cfg = {}
+        for c in others:
+            wlc = synth.config(c)
+            layc = L.workload_layouts(wlc, kinds=[wlc.headline])[wlc.headline]
+            data = workload_data(wlc, device, args.chain)
+            mc, mm = measure(wlc, layc, data, args, device, flush, stream, hbm_peak, dist)
+            per_cfg[c] = {"workload": workload_desc(wlc, wlc.headline, layc.n_physical),
+                          "ms_per_step": round(mc["ms_step"], 4), "tokens_per_s": round(mc["tokens_per_s"], 1),
+                          "hbm_gbs_step": round(mc["hbm_gbs_step"], 1), "frac_step": round(mc["frac_step"], 4),
+                          "bwd_phase_ms": round(mc["bwd_phase_ms"], 5), "bwd_gbs": round(mc["bwd_gbs"], 1),
+                          "bwd_frac": round(mc["bwd_gbs"] / hbm_peak, 4), "bwd_launches": mc["bwd_launches"],
+                          "fwd_gbs": round(mc["fwd_gbs"], 1), "gpu_launches_per_step": mc["launches"]}
+            del mm, data
+            torch.cuda.empty_cache()
+        line["other_workloads"] = per_cfg
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -841,9 +973,13 @@ def gemm_bench(args, rank, world):
 
 
 def reference_arm(args, rank, world):
-    """The oracle (FP64 C, as it stands) on the host cores, bounded per step."""
+    """The oracle (FP64 C, as it stands) on every host core: one spawned process
+    per core, each running the oracle over its own slice of a bounded sample of
+    the workload's rows for a fixed time per step."""
     if rank != 0:
         return
+    import concurrent.futures as cf
+    import multiprocessing as mp
     import torch
     import synth
     from invariant_rmsnorm_fwd_gb300 import layout as L
@@ -851,39 +987,44 @@ def reference_arm(args, rank, world):
     lay_name = args.layout or wl.headline
     lay = L.workload_layouts(wl, kinds=[lay_name])[lay_name]
     rpt = wl.heads[0]
-    n_rows = min(wl.n_tokens * rpt, max(64, (1 << 21) // wl.hidden))
-    x = synth.logical_tensor(wl, synth.TAG_X, n_rows, wl.x_std, 0)
-    dy = synth.logical_tensor(wl, synth.TAG_DY, n_rows, wl.dy_std, 0)
-    w = synth.weight(wl, 0)
-    import oracle
+    H = wl.hidden
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    per_core = max(8, (1 << 21) // H)
+    n_rows = min(wl.n_tokens * rpt, per_core * cores)
+    to_u16 = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    x = to_u16(synth.logical_tensor(wl, synth.TAG_X, n_rows, wl.x_std, 0))
+    dy = to_u16(synth.logical_tensor(wl, synth.TAG_DY, n_rows, wl.dy_std, 0))
+    w = to_u16(synth.weight(wl, 0))
+    per = max(1, n_rows // cores)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        oracle.forward(x[:64], w, wl.eps)
-    times, rows_done = [], []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        done = 0
-        while time.perf_counter() - t0 < per_step:
-            oracle.forward(x, w, wl.eps)
-            oracle.backward(x, w, dy, wl.eps)
-            done += n_rows
-        times.append(time.perf_counter() - t0)
-        rows_done.append(done)
     rows_per_token = sum(wl.heads)              # every normed tensor of a token (Q and K heads)
+    times, rows_done = [], []
+    with cf.ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")) as ex:
+        def one(seconds):
+            jobs = [(x[i * per:(i + 1) * per], dy[i * per:(i + 1) * per], w, wl.eps, seconds) for i in range(cores)]
+            res = list(ex.map(_oracle_worker, jobs))
+            return sum(r[0] for r in res), max(r[1] for r in res)
+        for _ in range(args.warmup):
+            one(0.05)
+        for _ in range(args.steps):
+            done, dt = one(per_step)
+            times.append(dt)
+            rows_done.append(done)
     tok_s = (sum(rows_done) / rows_per_token) / sum(times)
-    sample = (f"{n_rows} logical rows of {wl.name} (hidden {wl.hidden}) repeated for ~{per_step:.1f} s per step; "
-              f"a token is {rows_per_token} such rows; FP64 C oracle, single thread")
+    sample = (f"{n_rows} logical rows of {wl.name} (hidden {H}); one spawned process per host core ({cores}), "
+              f"each cycling its own slice of {per} rows for ~{per_step:.1f} s per step; a token is "
+              f"{rows_per_token} such rows; FP64 C oracle (single-threaded code, unchanged)")
     ms = statistics.mean(times) * 1e3
     line = {"metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": workload_desc(wl, lay_name, lay.n_physical), "hidden": wl.hidden,
+            "config": {"workload": workload_desc(wl, lay_name, lay.n_physical), "hidden": H,
                        "heads": list(wl.heads), "tokens": wl.n_tokens, "layout": lay_name, "calls": len(lay.calls),
                        "l2": "not applicable: the oracle runs on the host, in logical order",
-                       "launch": "oracle calls on the host (FP64 C, one thread)",
-                       "parallelism": "single host thread"},
-            "cpu_baseline": {"value": round(tok_s, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                       "launch": f"oracle calls on the host (FP64 C), one process per core ({cores})",
+                       "parallelism": f"{cores} host processes"},
+            "cpu_baseline": {"value": round(tok_s, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(tok_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -19,14 +19,15 @@ def _bench():
 
 def test_recorded_traffic_is_used_only_for_its_workload_and_sources():
     b = _bench()
-    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-    got = b.recorded_traffic(rec["workload"], rec["layout"])
-    if rec["source_sha256"] == b.source_sha256():
-        assert got == rec["dram_bytes_read"] + rec["dram_bytes_write"]
-    else:
-        assert got is None                                # sources changed since the capture
-    assert b.recorded_traffic("c4", rec["layout"]) is None
-    assert b.recorded_traffic(rec["workload"], "chunked") is None
+    d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for rec in d.get("records", [d]):
+        got = b.recorded_traffic(rec["workload"], rec["layout"])
+        if rec["source_sha256"] == b.source_sha256():
+            assert got == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+        else:
+            assert got is None                            # sources changed since the capture
+        assert b.recorded_traffic(rec["workload"], "no-such-layout") is None
+    assert b.recorded_traffic("c9", "full") is None
 
 
 def test_truncated_workload_keeps_the_first_tokens_and_values():
@@ -51,7 +52,8 @@ def test_parse_defaults_run_one_gpu_briefly():
     finally:
         sys.argv = old
     assert args.gpus == 1 and args.steps >= 1 and args.warmup >= 3 and args.impl == "ours"
-    assert args.config == "c1" and not args.chain and not args.gemm
+    assert args.config == "c4" and not args.chain and not args.gemm
+    assert set(args.also.split(",")) == {"c1", "c2", "c3"}
 
 
 def test_e2e_subcalls_cover_every_token_once_and_ramp():

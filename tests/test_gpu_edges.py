@@ -55,6 +55,78 @@ def test_dweight_follows_the_fixed_tree_bitwise(hidden, n_rows):
         assert got.tobytes() == want.tobytes(), (kind, np.flatnonzero(got != want)[:5])
 
 
+def _exact_tree_inputs(n_tok, rpt, hidden, seed):
+    """Inputs whose dweight leaves are exact and whose FP32 sums depend on the
+    association order: eps = 0, every row of constant magnitude 2^k (so rstd =
+    2^-k and xhat = +-1 exactly) and dy drawn from values that straddle 2^24.
+    Returns bf16 x, dy [n_tok, rpt, hidden] and the tree replay of the leaves
+    in logical row order (token-major, head-minor: row g*rpt + head)."""
+    rng = np.random.default_rng(seed)
+    n_rows = n_tok * rpt
+    signs = rng.choice(np.array([-1.0, 1.0], dtype=np.float32), size=(n_rows, hidden))
+    mags = (2.0 ** rng.integers(-3, 4, size=(n_rows, 1))).astype(np.float32)
+    pool = np.array([16777216.0, 1.0, -1.0, 3.0, -16777216.0, 0.5, 2.0 ** -20, 65536.0, -0.0, 255.0],
+                    dtype=np.float32)
+    dy = pool[rng.integers(0, pool.size, size=(n_rows, hidden))]
+    want = tree_replay.dweight(dy * signs)
+    x = bf16(signs * mags).reshape(n_tok, rpt, hidden)
+    return x, bf16(dy).reshape(n_tok, rpt, hidden), want
+
+
+def _split_lengths(n, seed):
+    """n tokens as a few samples of uneven length (at least one token each)."""
+    rng = np.random.default_rng(seed)
+    k = int(min(n, 1 + rng.integers(1, 7)))
+    cuts = np.sort(rng.choice(np.arange(1, n), size=k - 1, replace=False)) if k > 1 else np.zeros(0, int)
+    return np.diff(np.concatenate([[0], cuts, [n]])).astype(np.int64)
+
+
+_TREE_KINDS = ("full", "chunked", "singleton", "padded_right", "padded_left", "permuted",
+               "padded_right_chunked", "permuted_chunked")
+
+
+def _assert_tree_layouts(lengths, rpt, hidden, seed, kinds=_TREE_KINDS, chunk=37):
+    n_tok = int(np.sum(lengths))
+    x, dy, want = _exact_tree_inputs(n_tok, rpt, hidden, seed)
+    perm = synth.seeded_permutation(seed, len(lengths))
+    ones = bf16(np.ones(hidden))
+    for kind in kinds:
+        lay = L.make_layout(kind, lengths, chunk=chunk, perm=perm)
+        run = harness.run_layout(lay, x, dy, ones, 0.0, rows_per_token=rpt)
+        assert run.status == 0, (kind, run.status)
+        got = run.dweight.cpu().numpy()
+        assert got.tobytes() == want.tobytes(), (kind, hidden, rpt, np.flatnonzero(got != want)[:5])
+
+
+@pytest.mark.parametrize("hidden", [8192, 16384])
+@pytest.mark.parametrize("n_tok", [1, 65, 259, 4999])
+def test_dweight_tree_bitwise_on_cluster_kernels(hidden, n_tok):
+    """Hidden sizes above 5120 run on 2- and 4-CTA clusters (row sums exchanged
+    through distributed shared memory, column slices split over the CTAs); the
+    tree must still be the fixed one, in every layout.  4999 rows: 316 quarter
+    units leave a partial last round, which the backward splits into eighths."""
+    _assert_tree_layouts(_split_lengths(n_tok, hidden + n_tok), 1, hidden, hidden * 7 + n_tok)
+
+
+@pytest.mark.parametrize("rpt", [8, 32])
+@pytest.mark.parametrize("n_tok", [1, 7, 9, 100, 700])
+def test_dweight_tree_bitwise_per_head_rows(rpt, n_tok):
+    """Per-head norms (head_dim 128): logical row g*heads + head, so a token's
+    heads are adjacent leaves and a 64-row block holds 64/heads tokens."""
+    _assert_tree_layouts(_split_lengths(n_tok, rpt + n_tok), rpt, 128, rpt * 1000 + n_tok)
+
+
+@pytest.mark.parametrize("hidden", [8, 128, 4096, 5120, 8192])
+@pytest.mark.parametrize("chunk", [37, 16, 61])
+def test_dweight_tree_bitwise_padded_and_permuted_layouts(hidden, chunk):
+    """Several samples, padded on either side, permuted, and chunked so that
+    call boundaries cut logical blocks at every offset (37 and 61 are prime to
+    64; chunks of 16 cut the padded stream on quarter boundaries that are not
+    logical ones)."""
+    lengths = np.array([70, 3, 130, 1, 64, 9, 500, 37, 129])
+    _assert_tree_layouts(lengths, 1, hidden, hidden + chunk, chunk=chunk)
+
+
 def test_constant_rows_map_to_w_times_sign_bitwise():
     H = 4096
     wl = _workload([5, 3], H)

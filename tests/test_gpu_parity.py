@@ -45,7 +45,7 @@ def test_invariance_and_accuracy(cfg):
 def test_c2_hidden8192_padded_chunked():
     wl = synth.config("c2")
     x, dy, w, lays, runs = G.run_all_layouts(wl, kinds=["full", "padded_right_chunked", "singleton",
-                                                          "padded_left", "permuted", "chunked"])
+                                                          "padded_right", "padded_left", "permuted", "chunked"])
     _assert_green(harness.assert_batch_invariant(runs, lays), runs)
     _assert_accurate(G.oracle_check(runs["padded_right_chunked"], x, dy, w, wl.eps))
 
@@ -60,8 +60,8 @@ def test_c3_per_head_norm(head_set, heads):
 
 def test_c4_hidden5120_slots_quarter_density():
     wl = synth.config("c4")
-    x, dy, w, lays, runs = G.run_all_layouts(wl, kinds=["full", "permuted_slots_left_chunked", "padded_left",
-                                                          "permuted", "chunked"])
+    x, dy, w, lays, runs = G.run_all_layouts(wl, kinds=["full", "permuted_slots_left_chunked", "singleton",
+                                                          "padded_right", "padded_left", "permuted", "chunked"])
     _assert_green(harness.assert_batch_invariant(runs, lays), runs)
     _assert_accurate(G.oracle_check(runs["permuted_slots_left_chunked"], x, dy, w, wl.eps))
 
