@@ -302,6 +302,10 @@ class Step:
         """The backward launches of one step alone (the workspace begun beforehand)."""
         self._fan(self.bwd_call, stream)
 
+    def fwd_phase(self, stream):
+        """The forward launches of one step alone."""
+        self._fan(self.fwd_call, stream)
+
     def _lanes(self, stream):
         import torch
         if len(self.calls) == 1:
@@ -309,15 +313,6 @@ class Step:
         if getattr(self, "_side", None) is None:
             self._side = [torch.cuda.Stream(device=self.dw.device) for _ in range(self.n_streams)]
         return self._side
-
-    def time_fwd_only(self, stream):
-        import torch
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for c in self.calls:
-            self.fwd_call(c, stream)
-        e1.record(stream)
-        return e0, e1
 
     def gather(self, n_tok):
         import torch
@@ -390,27 +385,32 @@ def time_bwd_kernel(step_objs, stream, reps, flush):
     return [a.elapsed_time(b) for a, b in per]
 
 
-def time_bwd_phase(multi, stream, reps, flush):
-    """Duration of the backward phase of one step as it runs inside the step: every
-    fused-backward launch of every normed tensor (all calls of a many-call layout,
-    forked over the step's streams), captured as one CUDA graph and replayed
-    between two CUDA events on the launching stream.  Each workspace is begun
-    (eagerly, outside the events) and L2 is flushed before each replay."""
+def time_phase(multi, stream, reps, flush, which="bwd"):
+    """Duration of one phase of a step as it runs inside the step: every forward
+    ("fwd") or fused-backward ("bwd") launch of every normed tensor (all calls
+    of a many-call layout, forked over the step's streams), captured as one
+    CUDA graph and replayed between two CUDA events on the launching stream.
+    For the backward each workspace is begun (eagerly, outside the events);
+    L2 is flushed before each replay."""
     import torch
-    for s in multi.steps:
-        s.ws.begin(stream)
-    multi.bwd_phase(stream)
+    phase = multi.bwd_phase if which == "bwd" else multi.fwd_phase
+
+    def prep():
+        if which == "bwd":
+            for s in multi.steps:
+                s.ws.begin(stream)
+    prep()
+    phase(stream)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
     cap.wait_stream(stream)
     with torch.cuda.graph(g, stream=cap):
-        multi.bwd_phase(torch.cuda.current_stream())
+        phase(torch.cuda.current_stream())
     torch.cuda.synchronize()
     evs = []
     for _ in range(reps):
-        for s in multi.steps:
-            s.ws.begin(stream)
+        prep()
         flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -418,9 +418,10 @@ def time_bwd_phase(multi, stream, reps, flush):
         e1.record(stream)
         evs.append((e0, e1))
     torch.cuda.synchronize()
-    for s in multi.steps:
-        s.finalize(stream)
-    torch.cuda.synchronize()
+    if which == "bwd":
+        for s in multi.steps:
+            s.finalize(stream)
+        torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in evs]
 
 
@@ -645,6 +646,9 @@ class Multi:
     def bwd_phase(self, stream):
         self._fork(stream, lambda s, st: s.bwd_phase(st))
 
+    def fwd_phase(self, stream):
+        self._fork(stream, lambda s, st: s.fwd_phase(st))
+
 
 def workload_data(wl, device, chain=False):
     """Logical inputs of every normed tensor of a workload: (rows per token, x, dy, w[, r, dres])."""
@@ -700,14 +704,9 @@ def measure(wl, lay, data, args, device, flush, stream, hbm_peak, dist=None, sam
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_step = float(t.item())
     reps = max(3, args.steps // 2)
-    phase_ms = statistics.mean(time_bwd_phase(multi, stream, reps, flush))
+    phase_ms = statistics.mean(time_phase(multi, stream, reps, flush, "bwd"))
     bwd_ms = time_bwd_kernel(steps, stream, 1 if len(lay.calls) > 16 else reps, flush)
-    fwd_ms = []
-    for _ in range(reps):
-        flush()
-        evs = [s.time_fwd_only(stream) for s in steps]
-        torch.cuda.synchronize()
-        fwd_ms.append(sum(a.elapsed_time(b) for a, b in evs))
+    fwd_ms = time_phase(multi, stream, reps, flush, "fwd")
     heff = wl.hidden * sum(wl.heads)
     n_act = wl.n_tokens
     fwd_b, bwd_b = (8.0, 8.0) if args.chain else (4.0, 6.0)

@@ -304,11 +304,18 @@ int rmsnorm_plan_build(const int32_t *host_tok_id, int64_t n_tokens, int32_t row
  *    multiset; rows missing from it are reported in the status word.
  *  - Returns RMSNORM_ERR_WORKSPACE, with nothing enqueued, if
  *    rmsnorm_dweight_workspace_bytes(n_logical_tokens * rows_per_token,
- *    hidden) exceeds RMSNORM_NOALLOC_SCRATCH_BYTES; other errors as for
- *    rmsnorm_bwd_dx.
+ *    hidden) exceeds RMSNORM_NOALLOC_SCRATCH_BYTES; other argument errors
+ *    (NULL or misaligned pointers, layout, hidden size) as for
+ *    rmsnorm_bwd_dx, also with nothing enqueued.
+ *  - Rows of the multiset that the call does not hold (for instance an empty
+ *    call over a non-empty multiset) leave blocks the finalize cannot form;
+ *    only the status word reports them (RMSNORM_STATUS_MISSING), and dweight
+ *    is then not meaningful.  With status == NULL the caller has no way to
+ *    see this.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process: do not use this call on a device after cudaDeviceReset.
  *  - Every call shares the one array and clears its flags and status first;
  *    calls that overlap on the GPU (other streams, other host threads) race
  *    and must be serialised by the caller.

@@ -44,15 +44,12 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(LIBDIR, exist_ok=True)
+def _build_into(out_lib: str, objdir: str, extra_flags=(), verbose: bool = False) -> str:
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
-    objs = []
 
     def compile_one(src):
-        obj = os.path.join(LIBDIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -65,13 +62,31 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out_lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcublas"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out_lib)
+    return out_lib
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    if not force and up_to_date():
+        return LIB
+    return _build_into(LIB, LIBDIR, extra_flags, verbose)
+
+
+def build_test_variant(tag: str, defines: dict) -> str:
+    """A separate copy of the library compiled with extra preprocessor defines,
+    for tests only (e.g. a short wait limit); the product library is untouched.
+    Written to _lib/variant_<tag>/librmsnorm_bi_<tag>.so."""
+    d = os.path.join(LIBDIR, f"variant_{tag}")
+    out = os.path.join(d, f"librmsnorm_bi_{tag}.so")
+    if os.path.exists(out) and all(os.path.getmtime(p) <= os.path.getmtime(out) for p in _deps()):
+        return out
+    flags = [f"-D{k}={v}" if v is not None else f"-D{k}" for k, v in sorted(defines.items())]
+    return _build_into(out, d, flags)
 
 
 if __name__ == "__main__":

@@ -15,6 +15,13 @@ constexpr int kBlockRows = 64;       // logical block of the dweight reduction
 constexpr int kBlockLevels = 6;      // log2(kBlockRows)
 constexpr unsigned kFull = 0xffffffffu;
 
+// Longest wait of any pipeline role before it gives up and reports a timeout
+// (1 s).  A test-only build of the library sets RBI_WAIT_LIMIT_NS lower.
+#ifndef RBI_WAIT_LIMIT_NS
+#define RBI_WAIT_LIMIT_NS 1000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = RBI_WAIT_LIMIT_NS;
+
 // Status bits (mirror RMSNORM_STATUS_* in the public header).
 constexpr int kStDouble = 1, kStMissing = 2, kStHeader = 4, kStPlan = 8, kStTimeout = 16;
 
@@ -163,7 +170,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
-// Waits for the phase with the given parity; gives up after ~1 s of wall time.
+// Waits for the phase with the given parity; gives up after kWaitLimitNs of wall time.
 // Between polls the warp sleeps (32 ns, doubling to 256 ns) so that waiting
 // warps leave the issue slots to the warps that have work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
@@ -175,7 +182,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         __nanosleep(ns);
         if (mbar_try_wait(bar, parity)) return true;
         if (ns < 256) ns <<= 1;
-        if (global_timer_ns() - t0 > 1000000000ull) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 
@@ -220,7 +227,7 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t *bar, uint32_
         __nanosleep(ns);
         if (mbar_try_wait_cluster(bar, parity)) return true;
         if (ns < 256) ns <<= 1;
-        if (global_timer_ns() - t0 > 1000000000ull) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 

@@ -385,6 +385,14 @@ extern "C" int rmsnorm_bwd_noalloc(const uint16_t *x, const uint16_t *weight, co
     int rc = check_layout(layout, hidden);
     if (rc) return rc;
     if (!dweight) return RMSNORM_ERR_NULL;
+    if (!aligned16(dweight)) return RMSNORM_ERR_ALIGN;
+    // every argument error returns before anything is enqueued (the scratch
+    // is cleared by the first launch)
+    if (layout->n_tokens > 0) {
+        if (!x || !weight || !dy) return RMSNORM_ERR_NULL;
+        if (!aligned16(x) || !aligned16(weight) || !aligned16(dy) || (dx && !aligned16(dx)))
+            return RMSNORM_ERR_ALIGN;
+    }
     const int64_t N = layout->n_logical_tokens * layout->rows_per_token;
     const size_t need = rmsnorm_dweight_workspace_bytes(N, hidden);
     if (need == 0) return RMSNORM_ERR_LAYOUT;

@@ -598,7 +598,12 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                 }
             }
             __syncwarp();
+#ifndef RBI_TEST_WITHHOLD_EMPTY
             if (lane == 0) mbar_arrive(&empty[s]);
+#endif
+            // (A test-only build defines RBI_TEST_WITHHOLD_EMPTY: the column warps
+            // never release a stage, so the producer's first wait to reuse one runs
+            // out before it issues any copy into it; see the timeout test.)
             if (++s == S) {
                 s = 0;
                 parity ^= 1u;

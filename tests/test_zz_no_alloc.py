@@ -75,3 +75,28 @@ def test_noalloc_refuses_sizes_beyond_its_scratch():
                                  ctypes.c_void_p(dw.data_ptr()), None,
                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == -6                                          # RMSNORM_ERR_WORKSPACE, nothing enqueued
+
+
+def test_noalloc_without_dx_or_status_and_an_empty_call_reports_missing():
+    hidden, lengths = 4096, [300, 47]
+    wl, xp, dp, w, tok = _case(hidden, lengths, 31)
+    want_dx, want_dw = _with_workspace(wl, xp, dp, w, tok, 1)
+    cl = rb.call_layout(tok, 1, wl.n_tokens)
+    _, dw = rb.rmsnorm_bwd_noalloc(xp, w, dp, cl, wl.eps)            # no dx, no status
+    torch.cuda.synchronize()
+    assert torch.equal(dw.view(torch.int32), want_dw.view(torch.int32))
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    dx = torch.full_like(dp, float("nan"))
+    _, dw = rb.rmsnorm_bwd_noalloc(xp, w, dp, cl, wl.eps, dx=dx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(dx.view(torch.int16), want_dx.view(torch.int16))
+    assert torch.equal(dw.view(torch.int32), want_dw.view(torch.int32))
+    # a call holding none of the multiset's rows, right after a full one: the
+    # scratch still holds the previous call's rows, and only the status word
+    # can tell that this call's rows never arrived
+    empty = rb.call_layout(np.zeros(0, dtype=np.int32), 1, wl.n_tokens)
+    status.fill_(-1)
+    rb.rmsnorm_bwd_noalloc(xp, w, dp, empty, wl.eps, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & rb.STATUS_MISSING
