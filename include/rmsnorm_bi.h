@@ -234,11 +234,13 @@ int dweight_combine(const float *roots, int64_t n_roots, int64_t hidden, float g
  * dW failed the chunk and singleton checks like the norm's dweight).  The
  * pages give no kernel; this is the same cure applied to a contraction.
  *
- * gemm_dw_workspace_bytes: workspace for n_logical_rows tokens (N < 2^31),
+ * gemm_dw_workspace_bytes: workspace for n_logical_rows tokens (N < 2^31 - 64),
  *   in_features I and out_features O (multiples of 8, 8 .. 65536): a header
  *   with the status word, a flag per token, and the logical-order copies of
- *   x [N][I] and dy [N][O] in bf16.  0 for unsupported sizes.
- * gemm_dw_begin: writes the header, clears flags and status.
+ *   x and dy in bf16 (rows padded to multiples of 64 and 128 elements, the
+ *   token count to a multiple of 64).  0 for unsupported sizes.
+ * gemm_dw_begin: writes the header, clears flags and status and zeroes the
+ *   padding token rows.
  * gemm_dw_contrib: places the call's active tokens: x row t (stride
  *   x_stride elements) and dy row t (stride dy_stride) go to logical row
  *   tok_id[t]; -1 slots are skipped.  layout->rows_per_token must be 1;
@@ -247,10 +249,14 @@ int dweight_combine(const float *roots, int64_t n_roots, int64_t hidden, float g
  *   Calls may come in any order and on any stream ordered after begin.
  * gemm_dw_finalize: checks that every token arrived (else
  *   RMSNORM_STATUS_MISSING) and writes dW (FP32 [O][I], row-major) =
- *   grad_scale * sum over logical rows g of dy_g^T x_g as one GEMM with
- *   k = N in logical order (cuBLAS, FP32 compute, atomics off): its
- *   summation order depends on (N, I, O) only, so dW is bitwise the same for
- *   every layout of the multiset.  N == 0 gives dW = +0.0.
+ *   grad_scale * sum over logical rows g of dy_g^T x_g on the tensor cores
+ *   (tcgen05, bf16 operands, FP32 accumulation in tensor memory): each
+ *   128 x 256 tile of dW is summed by one CTA over slabs of 64 tokens in
+ *   logical order, so the summation order depends on (N, I, O) only and dW
+ *   is bitwise the same for every layout of the multiset (and every run on
+ *   the same GPU model).  grad_scale multiplies each element once.  N == 0
+ *   gives dW = +0.0.  A pipeline wait that runs out (about 1 s) sets
+ *   RMSNORM_STATUS_TIMEOUT instead of hanging.
  * gemm_dw_status: synchronises `stream` and reads the status word.
  * Errors: RMSNORM_ERR_NULL, _ALIGN (16-byte data, 256-byte workspace, strides
  * multiple of 8), _STRIDE, _LAYOUT, _HIDDEN (sizes), _WORKSPACE, _VALUE

@@ -7,24 +7,38 @@
 // dweight, an accumulation whose shape follows the rows of each call.  Here
 // a call only places its rows: x_g and dy_g of every active token go to row g
 // (the canonical logical id) of two logical-order buffers in the workspace.
-// The finalize then forms dW = sum_g dy_g^T x_g as one GEMM over all N logical
-// rows, dW[o][i] = sum_g DY[g][o] * X[g][i], in FP32 from the bf16 rows.  Its
-// summation order is the GEMM's and depends only on (N, I, O), never on how
-// the rows arrived.  The contraction is a plain library GEMM (cuBLAS, FP32
-// compute, no atomics); the placement, the contribution flags and the checks
-// are kernels of this file.
-#include <cublas_v2.h>
+// The finalize then forms dW = sum_g dy_g^T x_g over all N logical rows,
+// dW[o][i] = sum_g DY[g][o] * X[g][i], in FP32 from the bf16 rows, with the
+// hand-written tensor-core kernel below: every 128 x 256 tile of dW is owned
+// by one CTA, which walks k = the logical token id upward in slabs of 64
+// tokens and accumulates them in tensor memory in that order.  The summation
+// order therefore depends only on (N, I, O), never on how the rows arrived.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cmath>
 #include <mutex>
 
 #include "host.cuh"
 #include "rmsnorm_bi.h"
+#include "umma.cuh"
 
 namespace {
 
-constexpr uint32_t kGemmMagic = 0x47445731u;   // "GDW1"
+constexpr uint32_t kGemmMagic = 0x47445732u;   // "GDW2"
+
+// Tile shape of the contraction: dW rows (o) in tiles of 128, columns (i) in
+// tiles of up to 256, tokens (k) in slabs of 64; four slabs in flight.
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr int kChunk = 64;                               // elements of one 128-byte swizzle row
+constexpr int kChunkBytes = kChunk * kBK * 2;            // one TMA box: 64 (o or i) x 64 tokens, 8 KB
+constexpr int kABytes = kBM * kBK * 2;                   // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;                   // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kGemmSmem = kStages * kStageBytes + 1024;  // + alignment slack of the swizzle atoms
+constexpr int kGemmThreads = 192;                        // producer, MMA, four epilogue warps
+constexpr uint32_t kTmemCols = 2 * kBN;                  // two accumulators
 
 struct GemmWsHeader {
     uint32_t magic;
@@ -32,38 +46,68 @@ struct GemmWsHeader {
     int64_t n_rows, in_features, out_features;
 };
 
+// Logical-order copies of x and dy.  Row pitches are padded (i to a multiple
+// of 64, o to a multiple of 128) and the token count to a multiple of 64, so
+// every TMA box lies inside its tensor.  Padding rows are zeroed by begin (they
+// enter every sum); padding columns are never written and only ever reach
+// rows or columns of the product that are not stored.
 struct GemmWs {
     GemmWsHeader *hdr;
     int32_t *flag;          // [N] 1 once the row arrived
-    uint16_t *x;            // [N][I] bf16, logical order
-    uint16_t *dy;           // [N][O] bf16, logical order
+    uint16_t *x;            // [Np][Ip] bf16
+    uint16_t *dy;           // [Np][Op] bf16
+    int64_t np, ip, op;
 };
 
-int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
+int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
 bool gemm_sizes_ok(int64_t N, int64_t I, int64_t O) {
-    return N >= 0 && N < (int64_t(1) << 31) && I >= 8 && O >= 8 && I % 8 == 0 && O % 8 == 0 && I <= 65536 &&
+    return N >= 0 && N < (int64_t(1) << 31) - 64 && I >= 8 && O >= 8 && I % 8 == 0 && O % 8 == 0 && I <= 65536 &&
            O <= 65536;
 }
 
-int64_t gemm_ws_bytes(int64_t N, int64_t I, int64_t O) {
-    return 256 + align256(N * 4) + align256(N * I * 2) + align256(N * O * 2);
-}
+struct GemmLayout {
+    int64_t np, ip, op, off_flag, off_x, off_dy, total;
+    GemmLayout(int64_t N, int64_t I, int64_t O) {
+        np = align_up(N, kBK);
+        ip = align_up(I, kChunk);
+        op = align_up(O, kBM);
+        off_flag = 256;
+        off_x = align_up(off_flag + N * 4, 1024);
+        off_dy = align_up(off_x + np * ip * 2, 1024);
+        total = align_up(off_dy + np * op * 2, 1024);
+    }
+};
 
-GemmWs gemm_view(void *ws, int64_t N, int64_t I) {
+GemmWs gemm_view(void *ws, int64_t N, int64_t I, int64_t O) {
+    const GemmLayout L(N, I, O);
     uint8_t *b = static_cast<uint8_t *>(ws);
     GemmWs v;
     v.hdr = reinterpret_cast<GemmWsHeader *>(b);
-    v.flag = reinterpret_cast<int32_t *>(b + 256);
-    v.x = reinterpret_cast<uint16_t *>(b + 256 + align256(N * 4));
-    v.dy = reinterpret_cast<uint16_t *>(b + 256 + align256(N * 4) + align256(N * I * 2));
+    v.flag = reinterpret_cast<int32_t *>(b + L.off_flag);
+    v.x = reinterpret_cast<uint16_t *>(b + L.off_x);
+    v.dy = reinterpret_cast<uint16_t *>(b + L.off_dy);
+    v.np = L.np;
+    v.ip = L.ip;
+    v.op = L.op;
     return v;
 }
 
+__device__ __forceinline__ bool gemm_header_ok(const GemmWs &ws, int64_t N, int64_t I, int64_t O) {
+    return ws.hdr->magic == kGemmMagic && ws.hdr->n_rows == N && ws.hdr->in_features == I &&
+           ws.hdr->out_features == O;
+}
+
+// Clears the flags and the padding token rows [N, Np) of both copies.
 __global__ void gemm_begin_kernel(GemmWs ws, int64_t N, int64_t I, int64_t O) {
     const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = int64_t(gridDim.x) * blockDim.x;
     for (int64_t i = tid; i < N; i += nthr) ws.flag[i] = 0;
+    const int64_t px = (ws.np - N) * ws.ip / 8, pd = (ws.np - N) * ws.op / 8;   // uint4 units
+    uint4 *xz = reinterpret_cast<uint4 *>(ws.x + N * ws.ip);
+    uint4 *dz = reinterpret_cast<uint4 *>(ws.dy + N * ws.op);
+    for (int64_t i = tid; i < px; i += nthr) xz[i] = make_uint4(0, 0, 0, 0);
+    for (int64_t i = tid; i < pd; i += nthr) dz[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         ws.hdr->magic = kGemmMagic;
         ws.hdr->status = 0;
@@ -82,9 +126,7 @@ __global__ void gemm_place_kernel(GemmWs ws, const uint16_t *x, int64_t x_stride
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-    const bool header_ok = ws.hdr->magic == kGemmMagic && ws.hdr->n_rows == N && ws.hdr->in_features == I &&
-                           ws.hdr->out_features == O;
-    if (!header_ok) {
+    if (!gemm_header_ok(ws, N, I, O)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&ws.hdr->status, RMSNORM_STATUS_HEADER);
         return;
     }
@@ -96,10 +138,10 @@ __global__ void gemm_place_kernel(GemmWs ws, const uint16_t *x, int64_t x_stride
             continue;
         }
         const uint4 *xs = reinterpret_cast<const uint4 *>(x + t * x_stride);
-        uint4 *xd = reinterpret_cast<uint4 *>(ws.x + int64_t(g) * I);
+        uint4 *xd = reinterpret_cast<uint4 *>(ws.x + int64_t(g) * ws.ip);
         for (int64_t v = lane; v < I / 8; v += 32) xd[v] = xs[v];
         const uint4 *ds = reinterpret_cast<const uint4 *>(dy + t * dy_stride);
-        uint4 *dd = reinterpret_cast<uint4 *>(ws.dy + int64_t(g) * O);
+        uint4 *dd = reinterpret_cast<uint4 *>(ws.dy + int64_t(g) * ws.op);
         for (int64_t v = lane; v < O / 8; v += 32) dd[v] = ds[v];
         if (lane == 0 && atomicExch(&ws.flag[g], 1) != 0) atomicOr(&ws.hdr->status, RMSNORM_STATUS_DOUBLE);
     }
@@ -108,9 +150,7 @@ __global__ void gemm_place_kernel(GemmWs ws, const uint16_t *x, int64_t x_stride
 __global__ void gemm_check_kernel(GemmWs ws, int64_t N, int64_t I, int64_t O) {
     const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = int64_t(gridDim.x) * blockDim.x;
-    const bool header_ok = ws.hdr->magic == kGemmMagic && ws.hdr->n_rows == N && ws.hdr->in_features == I &&
-                           ws.hdr->out_features == O;
-    if (!header_ok) {
+    if (!gemm_header_ok(ws, N, I, O)) {
         if (tid == 0) atomicOr(&ws.hdr->status, RMSNORM_STATUS_HEADER);
         return;
     }
@@ -125,22 +165,220 @@ __global__ void gemm_zero_kernel(float *p, int64_t n) {
     for (int64_t i = tid; i < n; i += nthr) p[i] = 0.f;
 }
 
-// One cuBLAS handle per device, created on first use; calls are serialised
-// by the mutex (the handle's stream is set per call).
-std::mutex g_blas_mu;
-cublasHandle_t g_blas[64] = {nullptr};
+// ---------------------------------------------------------------- the contraction
 
-int blas_handle(cublasHandle_t *out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RMSNORM_ERR_CUDA;
-    if (g_blas[dev] == nullptr) {
-        if (cublasCreate(&g_blas[dev]) != CUBLAS_STATUS_SUCCESS) return RMSNORM_ERR_CUDA;
-        // atomics stay off (the default): every reduction order is fixed by the shapes
-        if (cublasSetAtomicsMode(g_blas[dev], CUBLAS_ATOMICS_NOT_ALLOWED) != CUBLAS_STATUS_SUCCESS)
-            return RMSNORM_ERR_CUDA;
-        if (cublasSetMathMode(g_blas[dev], CUBLAS_DEFAULT_MATH) != CUBLAS_STATUS_SUCCESS) return RMSNORM_ERR_CUDA;
+struct GemmParams {
+    float *dw;                 // [O][I] row-major
+    int32_t *status;           // workspace status word
+    int32_t O, I;
+    int32_t ip;                // padded i extent (multiple of 64)
+    int32_t m_tiles, n_tiles, k_slabs;
+    float scale;
+};
+
+// dW = scale * DY^T X on the tensor cores.  A = DY^T (o x k) and B = X (k x i)
+// are both read MN-major straight from the logical-order copies: a TMA box is
+// 64 tokens (k) by 64 consecutive o (or i), stored with the 128-byte swizzle,
+// which is the canonical MN-major operand layout of the MMA.
+//
+// Persistent CTAs (one per SM), tiles t = blockIdx.x, +gridDim.x, ... with
+// o-tile = t % m_tiles.  Warp roles:
+//   warp 0, lane 0: producer: per token slab, waits for the stage to be free,
+//                   loads the A box pair and up to four B boxes;
+//   warp 1, lane 0: MMA issuer: per slab four K = 16 MMAs into the tile's
+//                   accumulator (two accumulators in tensor memory, so the
+//                   next tile's MMAs overlap this tile's epilogue); slab
+//                   order is k order, the first MMA of a tile overwrites;
+//   warps 2-5:      epilogue: tensor memory -> registers -> dW (rows < O,
+//                   columns < I), times scale.
+// Every wait gives up after about a second: the CTA then raises its abort
+// flag and RMSNORM_STATUS_TIMEOUT, the producer waits (bounded) for the TMA
+// boxes it issued, the MMA issuer for its MMAs, and tensor memory is freed
+// before the CTA exits.
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_dw_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
+                   const GemmParams p) {
+    using namespace rbi;
+    extern __shared__ uint8_t gemm_smem[];
+    __shared__ uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], mma_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int32_t abort_flag;
+    // swizzle atoms start on 1024-byte boundaries of the shared window
+    uint8_t *tiles = gemm_smem + ((1024u - (smem_addr(gemm_smem) & 1023u)) & 1023u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = p.m_tiles * p.n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 4);
+        }
+        mbar_init(&mma_done, 1);
+        abort_flag = 0;
+        fence_mbar_init();
     }
-    *out = g_blas[dev];
+    if (warp == 1) {
+        umma::tmem_alloc(&tmem_slot, kTmemCols);
+        umma::tmem_relinquish();
+    }
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    auto give_up = [&]() {
+        abort_flag = 1;
+        atomicOr(p.status, RMSNORM_STATUS_TIMEOUT);
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ producer
+        int g = 0;                                            // slabs issued by this CTA
+        for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
+            const int mt = t % p.m_tiles, nt = t / p.m_tiles;
+            const int n0 = nt * kBN;
+            const int nb = min(kBN, p.ip - n0) / kChunk;      // B boxes of this tile (1..4)
+            for (int kb = 0; kb < p.k_slabs; ++kb) {
+                const int s = g % kStages, u = g / kStages;
+                if (u > 0 && !mbar_wait_bounded(&empty[s], uint32_t(u - 1) & 1u)) {
+                    give_up();
+                    break;
+                }
+                if (abort_flag) break;
+                uint8_t *a = tiles + s * kStageBytes;
+                uint8_t *b = a + kABytes;
+                mbar_arrive_expect_tx(&full[s], uint32_t(kABytes + nb * kChunkBytes));
+                umma::tma_load_2d(a, &tmap_dy, mt * kBM, kb * kBK, &full[s]);
+                umma::tma_load_2d(a + kChunkBytes, &tmap_dy, mt * kBM + kChunk, kb * kBK, &full[s]);
+                for (int j = 0; j < nb; ++j) umma::tma_load_2d(b + j * kChunkBytes, &tmap_x, n0 + j * kChunk, kb * kBK, &full[s]);
+                ++g;
+            }
+        }
+        // the boxes of the last slabs issued may still be in flight: let them land
+        for (int i = g - 1; i >= 0 && i >= g - kStages; --i)
+            mbar_wait_bounded(&full[i % kStages], uint32_t(i / kStages) & 1u);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        int g = 0, it = 0;
+        for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x, ++it) {
+            const int nt = t / p.m_tiles;
+            const int bn = min(kBN, p.ip - nt * kBN);
+            const int acc = it & 1, ua = it >> 1;
+            if (ua > 0 && !mbar_wait_bounded(&acc_empty[acc], uint32_t(ua - 1) & 1u)) {
+                give_up();
+                break;
+            }
+            umma::fence_after();
+            const uint32_t d = tmem + uint32_t(acc * kBN);
+            const uint32_t idesc = umma::idesc_bf16_mn(kBM, uint32_t(bn));
+            bool ok = true;
+            for (int kb = 0; kb < p.k_slabs; ++kb, ++g) {
+                const int s = g % kStages, u = g / kStages;
+                if (!mbar_wait_bounded(&full[s], uint32_t(u) & 1u)) {
+                    give_up();
+                    ok = false;
+                    break;
+                }
+                if (abort_flag) {
+                    ok = false;
+                    break;
+                }
+                umma::fence_after();
+                const uint32_t a = smem_addr(tiles + s * kStageBytes);
+                const uint32_t b = a + kABytes;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {             // 16 tokens per MMA: two 8-row groups
+                    const uint64_t ad = umma::desc_sw128(a + kk * 2048, kChunkBytes, 1024);
+                    const uint64_t bd = umma::desc_sw128(b + kk * 2048, kChunkBytes, 1024);
+                    umma::mma_bf16(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma::commit(&empty[s]);                      // the stage is free once these MMAs are done
+            }
+            if (!ok) break;
+            umma::commit(&acc_full[acc]);                     // the tile's sum is complete
+        }
+        umma::commit(&mma_done);
+        mbar_wait_bounded(&mma_done, 0);                      // no MMA in flight past this point
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;                               // the tensor-memory lanes this warp may read
+        int it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const int mt = t % p.m_tiles, nt = t / p.m_tiles;
+            const int n0 = nt * kBN;
+            const int bn = min(kBN, p.ip - n0);
+            const int acc = it & 1, ua = it >> 1;
+            bool ready = mbar_wait_bounded(&acc_full[acc], uint32_t(ua) & 1u);
+            ready = __all_sync(kFull, ready);
+            if (!ready) {
+                if (lane == 0) give_up();
+                break;
+            }
+            umma::fence_after();
+            const int64_t m = int64_t(mt) * kBM + q * 32 + lane;  // dW row of this lane
+            float *row = p.dw + m * p.I;
+            for (int c = 0; c < bn; c += 32) {
+                uint32_t v[32];
+                __syncwarp();
+                umma::ld_32x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * kBN + c), v);
+                umma::wait_ld();
+                if (m < p.O) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const int col = n0 + c + j;
+                        if (col < p.I) {
+                            float f[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                f[e] = __uint_as_float(v[j + e]);
+                                if (p.scale != 1.f) f[e] = __fmul_rn(f[e], p.scale);
+                            }
+                            st_global_f32x4(row + col, f[0], f[1], f[2], f[3]);
+                        }
+                    }
+                }
+            }
+            umma::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
+    }
+    umma::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        umma::fence_after();
+        umma::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int tensor_map_2d(CUtensorMap *map, void *base, int64_t inner, int64_t outer) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return RMSNORM_ERR_CUDA;
+    const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+    const cuuint64_t strides[1] = {cuuint64_t(inner) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(kChunk), cuuint32_t(kBK)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }
 
@@ -157,7 +395,7 @@ int grid_for(int64_t work, int threads, const rbi::DeviceInfo &d) {
 
 extern "C" size_t gemm_dw_workspace_bytes(int64_t n_logical_rows, int64_t in_features, int64_t out_features) {
     if (!gemm_sizes_ok(n_logical_rows, in_features, out_features)) return 0;
-    return size_t(gemm_ws_bytes(n_logical_rows, in_features, out_features));
+    return size_t(GemmLayout(n_logical_rows, in_features, out_features).total);
 }
 
 extern "C" int gemm_dw_begin(void *workspace, size_t bytes, int64_t n_logical_rows, int64_t in_features,
@@ -165,12 +403,13 @@ extern "C" int gemm_dw_begin(void *workspace, size_t bytes, int64_t n_logical_ro
     if (!workspace) return RMSNORM_ERR_NULL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RMSNORM_ERR_ALIGN;
     if (!gemm_sizes_ok(n_logical_rows, in_features, out_features)) return RMSNORM_ERR_HIDDEN;
-    if (bytes < size_t(gemm_ws_bytes(n_logical_rows, in_features, out_features))) return RMSNORM_ERR_WORKSPACE;
+    if (bytes < gemm_dw_workspace_bytes(n_logical_rows, in_features, out_features)) return RMSNORM_ERR_WORKSPACE;
     rbi::DeviceInfo *d = nullptr;
     int rc = rbi::device_info(&d);
     if (rc) return rc;
-    GemmWs ws = gemm_view(workspace, n_logical_rows, in_features);
-    gemm_begin_kernel<<<grid_for(n_logical_rows, 256, *d), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+    GemmWs ws = gemm_view(workspace, n_logical_rows, in_features, out_features);
+    const int64_t work = n_logical_rows + (ws.np - n_logical_rows) * (ws.ip + ws.op) / 8;
+    gemm_begin_kernel<<<grid_for(work, 256, *d), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         ws, n_logical_rows, in_features, out_features);
     if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
     rbi::count_launch();
@@ -193,7 +432,7 @@ extern "C" int gemm_dw_contrib(const uint16_t *x, int64_t x_stride, const uint16
     int rc = rbi::device_info(&d);
     if (rc) return rc;
     const int64_t N = layout->n_logical_tokens;
-    GemmWs ws = gemm_view(workspace, N, in_features);
+    GemmWs ws = gemm_view(workspace, N, in_features, out_features);
     const int threads = 256;
     gemm_place_kernel<<<grid_for(layout->n_tokens * 32, threads, *d), threads, 0,
                         reinterpret_cast<cudaStream_t>(stream)>>>(ws, x, x_stride, dy, dy_stride, layout->tok_id,
@@ -214,7 +453,7 @@ extern "C" int gemm_dw_finalize(void *workspace, int64_t n_logical_rows, int64_t
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t N = n_logical_rows, I = in_features, O = out_features;
-    GemmWs ws = gemm_view(workspace, N, I);
+    GemmWs ws = gemm_view(workspace, N, I, O);
     gemm_check_kernel<<<grid_for(N, 256, *d), 256, 0, s>>>(ws, N, I, O);
     if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
     rbi::count_launch();
@@ -224,17 +463,30 @@ extern "C" int gemm_dw_finalize(void *workspace, int64_t n_logical_rows, int64_t
         rbi::count_launch();
         return RMSNORM_OK;
     }
-    std::lock_guard<std::mutex> lk(g_blas_mu);
-    cublasHandle_t h = nullptr;
-    if ((rc = blas_handle(&h))) return rc;
-    if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return RMSNORM_ERR_CUDA;
-    // column-major view: X is I x N (ld I), DY is O x N (ld O), dW (row-major
-    // [O][I]) is I x O (ld I):  dW = X * DY^T, k = N in logical order
-    const float alpha = grad_scale, beta = 0.f;
-    if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, int(I), int(O), int(N), &alpha, ws.x, CUDA_R_16BF, int(I), ws.dy,
-                     CUDA_R_16BF, int(O), &beta, dw, CUDA_R_32F, int(I), CUBLAS_COMPUTE_32F,
-                     CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-        return RMSNORM_ERR_CUDA;
+    CUtensorMap tm_dy, tm_x;
+    if ((rc = tensor_map_2d(&tm_dy, ws.dy, ws.op, ws.np)) || (rc = tensor_map_2d(&tm_x, ws.x, ws.ip, ws.np)))
+        return rc;
+    GemmParams gp;
+    gp.dw = dw;
+    gp.status = &ws.hdr->status;
+    gp.O = int32_t(O);
+    gp.I = int32_t(I);
+    gp.ip = int32_t(ws.ip);
+    gp.m_tiles = int32_t(ws.op / kBM);
+    gp.n_tiles = int32_t((ws.ip + kBN - 1) / kBN);
+    gp.k_slabs = int32_t(ws.np / kBK);
+    gp.scale = grad_scale;
+    static std::once_flag attr_once;
+    static cudaError_t attr_rc = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_rc = cudaFuncSetAttribute(gemm_dw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    });
+    if (attr_rc != cudaSuccess) return RMSNORM_ERR_CUDA;
+    const int64_t tiles = int64_t(gp.m_tiles) * gp.n_tiles;
+    const int grid = int(tiles < d->sms ? tiles : d->sms);
+    gemm_dw_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(tm_dy, tm_x, gp);
+    if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
+    rbi::count_launch();
     return RMSNORM_OK;
 }
 

@@ -46,6 +46,26 @@ def test_layout_invariant_and_accurate(cfg, I, O):
     assert r["violations"] == 0, r
 
 
+@pytest.mark.parametrize("n,I,O", [(1000, 328, 200), (2000, 4096, 4096), (77, 8, 4104), (64, 264, 136)])
+def test_tile_edges_and_many_tiles_per_cta(n, I, O):
+    """dW tiles are 128 (o) x up to 256 (i) over slabs of 64 tokens: partial
+    tiles in both directions, a token count that is not a multiple of 64, and
+    (4096 x 4096) more tiles than CTAs, so each CTA alternates its two
+    tensor-memory accumulators.  Chunked and permuted layouts must give the
+    packed call's bits, and the oracle's values within tolerance."""
+    lengths = np.array([n // 3, n - n // 3 - n // 5, n // 5]) if n >= 15 else np.array([n])
+    lengths = lengths[lengths > 0]
+    wl = synth.Workload("tiles", 8, lengths, seed=n + I + O, x_std=1.0, dy_std=1e-2, chunk_rows=37)
+    x, dy = _inputs(wl, I, O)
+    lays = L.workload_layouts(wl, kinds=["full", "chunked", "permuted"])
+    runs = {k: harness.run_layout_gemm(v, x, dy) for k, v in lays.items()}
+    rep = harness.assert_batch_invariant(runs, lays)
+    assert rep.green, rep.summary()
+    ref, s = ogemm.dw(x.cpu(), dy.cpu())
+    r = tol.check("dW", runs["full"].dweight.cpu().numpy(), ref, tol.bound_dw(ref, s))
+    assert r["violations"] == 0, r
+
+
 def test_exact_sums_are_exact():
     """Small integers: every product and partial sum is exact in FP32, so the GPU
     result must equal the FP64 oracle bit for bit whatever its order."""
