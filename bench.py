@@ -480,7 +480,7 @@ def e2e_steps(wl, lay, norms, steps, warmup, device, chunk_tokens=4096, copy_lan
         dh[torch.as_tensor(act)] = dy_log_host[idx]
         host.append((xh, dh, torch.empty_like(xh).pin_memory(), torch.empty_like(xh).pin_memory()))
         dev.append(tuple(torch.empty(xh.shape, dtype=torch.bfloat16, device=device) for _ in range(4)))
-        cap = max(int(np.ceil(tok.size * rpt / 64)) * 2 + 2, 1) * rb.PLAN_ITEM_BYTES
+        cap = rb.plan_capacity(tok.size, rpt)
         meta_h.append((torch.empty(tok.size, dtype=torch.int32).pin_memory(),
                        torch.empty(cap, dtype=torch.uint8).pin_memory()))
         meta_d.append((torch.empty(tok.size, dtype=torch.int32, device=device),

@@ -278,9 +278,15 @@ int rmsnorm_dweight_status(const void *workspace, rmsnorm_stream_t stream, int32
 /*
  * Host-side planner (no GPU needed).  From a HOST copy of a call's tok_id it
  * writes the work items that rmsnorm_bwd_dx / rmsnorm_bwd_dweight_contrib
- * execute: one item per logical block wholly inside the call (its 64 rows in
- * logical order) and items of up to 64 rows from blocks cut by a call
- * boundary.  rmsnorm_plan_bytes gives a capacity that always suffices.
+ * execute (528 bytes each: kind, block, count, quarter mask, 64 physical
+ * rows, 64 logical rows): one item per logical block wholly inside the call
+ * (kind 0, its rows in logical order); for a block cut by a call boundary,
+ * one item holding the block's quarters (16 aligned logical rows) that the
+ * call holds completely (kind 2, each row at its place in the block, bit q
+ * of the mask set for quarter q); and items of up to 64 of the remaining
+ * rows of cut blocks (kind 1).  *whole_blocks counts kind-0 items,
+ * *spill_rows the rows of kind-1 items.  rmsnorm_plan_bytes gives a capacity
+ * that always suffices.
  * Errors: RMSNORM_ERR_ID, RMSNORM_ERR_DUPLICATE, RMSNORM_ERR_CAPACITY
  * (host_plan's contents are then unspecified).  The plan depends only on
  * tok_id, rows_per_token and n_logical_tokens.  Cost: linear in the call's

@@ -118,6 +118,13 @@ def kernel_launches() -> int:
 
 # ------------------------------------------------------------------ planning
 
+def plan_capacity(n_tokens: int, rows_per_token: int) -> int:
+    """Bytes of a plan buffer that always suffices for a call of n_tokens token slots."""
+    cap = ctypes.c_size_t(0)
+    _check(_load().rmsnorm_plan_bytes(int(n_tokens), int(rows_per_token), ctypes.byref(cap)), "rmsnorm_plan_bytes")
+    return max(int(cap.value), PLAN_ITEM_BYTES)
+
+
 def plan_build(tok_id: np.ndarray, rows_per_token: int, n_logical_tokens: int, out: np.ndarray = None):
     """Host planner (C++ in the library).  Returns (plan bytes as np.uint8, items,
     whole blocks, spilled rows).  `out` (contiguous np.uint8, e.g. a view of pinned

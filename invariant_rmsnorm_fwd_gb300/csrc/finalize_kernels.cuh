@@ -38,9 +38,10 @@ __global__ void ws_begin_kernel(WsView ws) {
 // In the first pass (from_blocks) an input is a block partial: the four
 // quarter partials as (q0 + q1) + (q2 + q3) (levels 5 and 6 of the 64-leaf
 // tree), a whole-block partial as is, or, for a block cut by a call boundary,
-// the 64-leaf tree over its spilled rows, rebuilt by each lane for its own
-// 8-column vector (pairs (0,1), (2,3), ... at every level): the same tree as
-// the in-kernel path.
+// its four quarters, each one a quarter partial computed by the call that
+// held the whole quarter or the 16-leaf tree over the quarter's spilled rows,
+// rebuilt by each lane for its own 8-column vector (pairs (0,1), (2,3), ...
+// at every level): the same tree as the in-kernel path.
 __device__ __forceinline__ void load8(const float *src, float (&v)[8]) {
     const float4 a = ld_global_f32x4(src), b = ld_global_f32x4(src + 4);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
@@ -64,6 +65,37 @@ __device__ __forceinline__ void add_second_eighth(uint32_t state, int q, const f
     load8(src, e);
 #pragma unroll
     for (int c = 0; c < 8; ++c) v[c] = __fadd_rn(v[c], e[c]);
+}
+
+// The 16-leaf subtree of quarter q of a block from its spilled rows, for one
+// 8-column vector (src points at the block's row 0 of that vector): rows at or
+// beyond `rows` (past the multiset) are +0.0 leaves.  Eight rows are loaded
+// at a time (levels 1-3 of the tree over them), and the two eights are added
+// (level 4), earlier rows always on the left.
+__device__ __forceinline__ void quarter_from_spill(const float *src, int H, int q, int64_t rows, float (&out)[8]) {
+    float n0[8];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        float x[8][8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int r = 16 * q + 8 * half + k;
+            if (r < rows) {
+                load8(src + int64_t(r) * H, x[k]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) x[k][c] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float a01 = __fadd_rn(x[0][c], x[1][c]), a23 = __fadd_rn(x[2][c], x[3][c]);
+            const float a45 = __fadd_rn(x[4][c], x[5][c]), a67 = __fadd_rn(x[6][c], x[7][c]);
+            const float e = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
+            if (half == 0) n0[c] = e;
+            else out[c] = __fadd_rn(n0[c], e);
+        }
+    }
 }
 
 constexpr int kTreeWarps = 16;                           // warps per CTA: 2 inputs each
@@ -116,45 +148,51 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, c
             }
         } else if (state == kStateWhole) {
             if (has_vec) load8(ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8, val);
-        } else if (state == 0) {
-            // cut block: each lane rebuilds its own vector from the spilled rows,
-            // eight rows per step with all their loads in flight (levels 1-3 of the
-            // tree over those eight, then the carry stack from level 3 up)
+        } else {
+            // a block cut by a call boundary: each quarter arrived as a partial
+            // (byte 1), as two eighth partials (byte 12), or as spilled rows
+            // (byte 0), which each lane rebuilds for its own 8-column vector;
+            // then the block is (q0 + q1) + (q2 + q3) as in the other paths
             const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
-            const int64_t r0 = b * kBlockRows + 2 * lane;
-            const bool have0 = 2 * lane < rows, have1 = 2 * lane + 1 < rows;
-            const bool missing = (have0 && ws.leaf_flag[r0] == 0) || (have1 && ws.leaf_flag[r0 + 1] == 0);
+            bool bad = false;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t by = (state >> (8 * q)) & 0xffu;
+                bad |= by != 0 && by != kStateQuarter && by != (kStateEighth0 | kStateEighth1);
+            }
+            bool missing = bad;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int r = 2 * lane + k;
+                if (r < rows && ((state >> (8 * (r / 16))) & 0xffu) == 0 && ws.leaf_flag[b * kBlockRows + r] == 0)
+                    missing = true;
+            }
             if (__any_sync(kFull, missing) && lane == 0 && blockIdx.y == 0) set_status(ws.hdr, kStMissing);
             if (has_vec) {
+                const float *part = ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8;
+                const float *part2 = ws.eighth + b * 4 * int64_t(H) + int64_t(v) * 8;
                 const float *src = ws.spill + b * kBlockRows * int64_t(H) + int64_t(v) * 8;
-                TreeStack<8> st;
+                float h0[8], acc[8];
 #pragma unroll 1
-                for (int r = 0; r < kBlockRows; r += 8) {
-                    float x[8][8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        if (r + k < rows) {
-                            load8(src + int64_t(r + k) * H, x[k]);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) x[k][c] = 0.f;     // leaves past the multiset
-                        }
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t by = (state >> (8 * q)) & 0xffu;
+                    float qv[8];
+                    if (by == kStateQuarter) {
+                        load8(part + q * int64_t(H), qv);
+                    } else if (by == (kStateEighth0 | kStateEighth1)) {
+                        load8(part + q * int64_t(H), qv);
+                        add_second_eighth(state, q, part2 + q * int64_t(H), qv);
+                    } else {
+                        quarter_from_spill(src, H, q, rows, qv);
                     }
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const float a01 = __fadd_rn(x[0][c], x[1][c]), a23 = __fadd_rn(x[2][c], x[3][c]);
-                        const float a45 = __fadd_rn(x[4][c], x[5][c]), a67 = __fadd_rn(x[6][c], x[7][c]);
-                        x[0][c] = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
-                    }
-                    st.push(x[0], r >> 3, 3);
-                    if (r == kBlockRows - 8) {
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) val[c] = x[0][c];           // the whole block
+                        if (q == 0 || q == 2) acc[c] = qv[c];
+                        else if (q == 1) h0[c] = __fadd_rn(acc[c], qv[c]);
+                        else val[c] = __fadd_rn(h0[c], __fadd_rn(acc[c], qv[c]));
                     }
                 }
             }
-        } else {
-            if (lane == 0 && blockIdx.y == 0) set_status(ws.hdr, kStMissing);   // partly contributed block
         }
 #pragma unroll
         for (int c = 0; c < 8; ++c) pair[c] = h == 0 ? val[c] : __fadd_rn(pair[c], val[c]);

@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int nb = min(kBN, p.ip - n0) / kChunk;      // B boxes of this tile (1..4)
             for (int kb = 0; kb < p.k_slabs; ++kb) {
                 const int s = g % kStages, u = g / kStages;
-                if (u > 0 && !mbar_wait_bounded(&empty[s], uint32_t(u - 1) & 1u)) {
+                if (u > 0 && !mbar_wait_spin_bounded(&empty[s], uint32_t(u - 1) & 1u)) {
                     give_up();
                     break;
                 }
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int nt = t / p.m_tiles;
             const int bn = min(kBN, p.ip - nt * kBN);
             const int acc = it & 1, ua = it >> 1;
-            if (ua > 0 && !mbar_wait_bounded(&acc_empty[acc], uint32_t(ua - 1) & 1u)) {
+            if (ua > 0 && !mbar_wait_spin_bounded(&acc_empty[acc], uint32_t(ua - 1) & 1u)) {
                 give_up();
                 break;
             }
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bool ok = true;
             for (int kb = 0; kb < p.k_slabs; ++kb, ++g) {
                 const int s = g % kStages, u = g / kStages;
-                if (!mbar_wait_bounded(&full[s], uint32_t(u) & 1u)) {
+                if (!mbar_wait_spin_bounded(&full[s], uint32_t(u) & 1u)) {
                     give_up();
                     ok = false;
                     break;

@@ -3,13 +3,19 @@
 //
 // A logical block b holds logical rows [64b, 64b+64) (the last block holds
 // the rows below N).  If every row of the block is in this call the block
-// becomes one "whole" item listing the block's physical rows in logical
-// order, and its 64-leaf tree is formed on chip.  Rows of blocks that the
-// call holds only partly go, in logical order, into "spill" items of up to
-// 64 rows; their FP32 contributions are written to the workspace and the
-// block is reduced later by dweight_finalize with the same tree.  Padding
-// slots (id -1) appear in no item.  The plan depends only on the ids, so a
-// layout always gets the same plan.
+// becomes one "whole" item (kind 0) listing the block's physical rows in
+// logical order, and its 64-leaf tree is formed on chip.  A block that the
+// call holds only partly is cut; each of its quarters (16 aligned logical
+// rows, the subtrees of the block's tree one level below its two halves)
+// that the call holds completely goes into one "quarter" item of that block
+// (kind 2: the present quarters' rows at their places, a bit per present
+// quarter), and the kernels reduce such a quarter on chip like a quarter of
+// a whole block.  The remaining rows of cut blocks go, in logical order,
+// into "spill" items of up to 64 rows (kind 1); their FP32 contributions are
+// written to the workspace and their quarters are reduced by
+// dweight_finalize with the same tree.  Padding slots (id -1) appear in no
+// item.  The plan depends only on the ids, so a layout always gets the same
+// plan.
 #include <algorithm>
 #include <cstring>
 #include <utility>
@@ -22,7 +28,7 @@ namespace {
 constexpr int kBlockRows = 64;
 
 struct Item {                       // must match rbi::PlanItem (528 bytes)
-    int32_t kind, block, count, reserved;
+    int32_t kind, block, count, quarters;
     int32_t prow[kBlockRows];
     int32_t lrow[kBlockRows];
 };
@@ -32,7 +38,7 @@ void fill_item(Item &it, int32_t kind, int32_t block, const int32_t *prow, const
     it.kind = kind;
     it.block = block;
     it.count = int32_t(n);
-    it.reserved = 0;
+    it.quarters = 0;
     std::memcpy(it.prow, prow, n * sizeof(int32_t));
     std::memcpy(it.lrow, lrow, n * sizeof(int32_t));
     for (size_t q = n; q < size_t(kBlockRows); ++q) it.prow[q] = it.lrow[q] = -1;
@@ -42,7 +48,7 @@ void fill_item(Item &it, int32_t kind, int32_t block, const int32_t *prow, const
 // step does not map and fault in fresh pages each time.
 struct Scratch {
     std::vector<std::pair<int32_t, int32_t>> tok;
-    std::vector<int32_t> lrows, prows, sp_lrow, sp_prow;
+    std::vector<int32_t> lrows, prows, sp_lrow, sp_prow, q_lrow, q_prow, q_block, q_mask, q_at;
 
     template <class T>
     T *reserve(std::vector<T> &v, size_t n) {                 // grows only; contents are scratch
@@ -58,12 +64,15 @@ Scratch &scratch() {
 
 }  // namespace
 
+// Items of a call of `rows` physical rows: at most one whole item per 64
+// rows, one quarter item per complete quarter (16 rows, or fewer at the end
+// of the multiset) and one spill item per 64 cut rows.
+int64_t max_items(int64_t rows) { return 2 * ((rows + kBlockRows - 1) / kBlockRows) + (rows + 15) / 16 + 3; }
+
 extern "C" int rmsnorm_plan_bytes(int64_t n_tokens, int32_t rows_per_token, size_t *bytes) {
     if (!bytes) return RMSNORM_ERR_NULL;
     if (n_tokens < 0 || rows_per_token < 1) return RMSNORM_ERR_LAYOUT;
-    const int64_t rows = n_tokens * rows_per_token;
-    const int64_t items = 2 * ((rows + kBlockRows - 1) / kBlockRows) + 2;
-    *bytes = size_t(items) * sizeof(Item);
+    *bytes = size_t(max_items(n_tokens * rows_per_token)) * sizeof(Item);
     return RMSNORM_OK;
 }
 
@@ -110,30 +119,75 @@ extern "C" int rmsnorm_plan_build(const int32_t *tok_id, int64_t n_tokens, int32
         }
     }
 
-    // whole blocks go straight to the output, cut rows are gathered for the spill items
-    const size_t max_items = capacity / sizeof(Item);
+    // whole blocks go straight to the output; complete quarters of cut blocks
+    // are gathered for the quarter items, the other cut rows for the spill items
+    const size_t max_out = capacity / sizeof(Item);
     Item *out = static_cast<Item *>(plan);
-    size_t n_items = 0, n_sp = 0;
+    size_t n_items = 0, n_sp = 0, n_qb = 0;
+    int32_t *q_prow = sc.reserve(sc.q_prow, n_act_max), *q_lrow = sc.reserve(sc.q_lrow, n_act_max);
+    int32_t *q_block = sc.reserve(sc.q_block, n_act_max / 16 + 2), *q_mask = sc.reserve(sc.q_mask, n_act_max / 16 + 2);
+    int32_t *q_at = sc.reserve(sc.q_at, n_act_max / 16 + 2);
+    size_t n_q = 0;                                              // rows gathered for quarter items
     size_t i = 0;
     while (i < n_act) {
         const int32_t b = lrows[i] / kBlockRows;
-        const int64_t b_rows = std::min<int64_t>(kBlockRows, N - int64_t(b) * kBlockRows);
+        const int64_t b0 = int64_t(b) * kBlockRows;
+        const int64_t b_rows = std::min<int64_t>(kBlockRows, N - b0);
         size_t j = i;                                          // rows of block b in this call: [i, j)
         while (j < n_act && lrows[j] / kBlockRows == b) ++j;
         if (int64_t(j - i) == b_rows) {                        // rows [64b, 64b + b_rows) in order
-            if (n_items == max_items) return RMSNORM_ERR_CAPACITY;
+            if (n_items == max_out) return RMSNORM_ERR_CAPACITY;
             if (!out) return RMSNORM_ERR_NULL;
             fill_item(out[n_items++], 0, b, prows + i, lrows + i, size_t(b_rows));
         } else {
-            std::memcpy(sp_lrow + n_sp, lrows + i, (j - i) * sizeof(int32_t));
-            std::memcpy(sp_prow + n_sp, prows + i, (j - i) * sizeof(int32_t));
-            n_sp += j - i;
+            int32_t mask = 0;
+            const size_t q_first = n_q;
+            for (size_t k = i; k < j;) {                       // runs of rows within one quarter
+                const int32_t q = int32_t((lrows[k] - b0) / 16);
+                size_t e = k;
+                while (e < j && (lrows[e] - b0) / 16 == q) ++e;
+                const int64_t q_rows = std::min<int64_t>(16, N - (b0 + 16 * q));
+                if (int64_t(e - k) == q_rows) {                // the whole quarter is in this call
+                    mask |= 1 << q;
+                    std::memcpy(q_lrow + n_q, lrows + k, (e - k) * sizeof(int32_t));
+                    std::memcpy(q_prow + n_q, prows + k, (e - k) * sizeof(int32_t));
+                    n_q += e - k;
+                } else {
+                    std::memcpy(sp_lrow + n_sp, lrows + k, (e - k) * sizeof(int32_t));
+                    std::memcpy(sp_prow + n_sp, prows + k, (e - k) * sizeof(int32_t));
+                    n_sp += e - k;
+                }
+                k = e;
+            }
+            if (mask) {
+                q_block[n_qb] = b;
+                q_mask[n_qb] = mask;
+                q_at[n_qb] = int32_t(q_first);
+                ++n_qb;
+            }
         }
         i = j;
     }
     const size_t n_whole = n_items;
+    for (size_t k = 0; k < n_qb; ++k) {
+        if (n_items == max_out) return RMSNORM_ERR_CAPACITY;
+        if (!out) return RMSNORM_ERR_NULL;
+        Item &it = out[n_items++];
+        const size_t r0 = size_t(q_at[k]), r1 = k + 1 < n_qb ? size_t(q_at[k + 1]) : n_q;
+        it.kind = 2;
+        it.block = q_block[k];
+        it.count = int32_t(r1 - r0);
+        it.quarters = q_mask[k];
+        for (int s = 0; s < kBlockRows; ++s) it.prow[s] = it.lrow[s] = -1;
+        const int64_t b0 = int64_t(q_block[k]) * kBlockRows;
+        for (size_t r = r0; r < r1; ++r) {                     // each row at its place in the block
+            const int32_t slot = int32_t(q_lrow[r] - b0);
+            it.prow[slot] = q_prow[r];
+            it.lrow[slot] = q_lrow[r];
+        }
+    }
     for (size_t k = 0; k < n_sp; k += kBlockRows) {
-        if (n_items == max_items) return RMSNORM_ERR_CAPACITY;
+        if (n_items == max_out) return RMSNORM_ERR_CAPACITY;
         if (!out) return RMSNORM_ERR_NULL;
         fill_item(out[n_items++], 1, -1, sp_prow + k, sp_lrow + k, std::min<size_t>(kBlockRows, n_sp - k));
     }

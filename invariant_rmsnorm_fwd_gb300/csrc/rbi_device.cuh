@@ -106,13 +106,22 @@ __device__ __forceinline__ bool header_ok(const WsView &ws) {
 // ----------------------------------------------------------------- plan items
 
 struct PlanItem {                    // written by the host planner
-    int32_t kind;                    // 0 = whole logical block, 1 = rows of cut blocks
-    int32_t block;                   // block id for kind 0, -1 otherwise
+    int32_t kind;                    // 0 = whole logical block, 1 = rows of cut blocks,
+                                     // 2 = complete quarters of a cut block
+    int32_t block;                   // block id for kinds 0 and 2, -1 otherwise
     int32_t count;                   // used slots
-    int32_t reserved;
+    int32_t quarters;                // kind 2: bit q set = quarter q present (slots 16q..16q+15)
     int32_t prow[kBlockRows];        // physical row within the call, -1 = empty slot
     int32_t lrow[kBlockRows];        // logical row id, -1 = empty slot
 };
+
+// Item kinds as staged for the kernels: the low byte is the kind, bits 8-11
+// the quarter mask of a kind-2 item; kBadItem marks a malformed item, which
+// contributes nothing.
+constexpr int kItemWhole = 0, kItemSpill = 1, kItemQuarters = 2, kBadItem = 3;
+__device__ __forceinline__ int32_t staged_kind(const PlanItem &it) {
+    return it.kind == kItemQuarters ? (kItemQuarters | ((it.quarters & 15) << 8)) : it.kind;
+}
 static_assert(sizeof(PlanItem) == 528, "plan item layout is part of the ABI");
 
 // ----------------------------------------------------------------- PTX wrappers
@@ -183,6 +192,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (mbar_try_wait(bar, parity)) return true;
         if (ns < 256) ns <<= 1;
         if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// The same bounded wait without sleeping between polls, for the few threads
+// whose latency sets the pace (the MMA issuer and the producer of a tensor-core
+// pipeline): try_wait itself suspends the thread for a short hardware time
+// window, and the clock is read only every 256 polls.
+__device__ __forceinline__ bool mbar_wait_spin_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 

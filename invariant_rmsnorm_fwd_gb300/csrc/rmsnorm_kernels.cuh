@@ -129,8 +129,10 @@ __device__ __forceinline__ void mark_eighth(const WsView &ws, int64_t b, int q, 
     atomicOr(reinterpret_cast<unsigned int *>(st), unsigned(bit) << (8 * q));
 }
 
+// A spilled row meets an earlier contribution if it was spilled before or if
+// its quarter arrived as a partial (a whole block sets all four quarter bytes).
 __device__ __forceinline__ void mark_spilled_row(const WsView &ws, int64_t lrow) {
-    const uint32_t st = reinterpret_cast<const uint32_t *>(ws.block_state)[lrow / kBlockRows];
+    const uint8_t st = ws.block_state[(lrow / kBlockRows) * 4 + (lrow % kBlockRows) / 16];
     if (ws.leaf_flag[lrow] != 0 || st != 0) set_status(ws.hdr, kStDouble);
     ws.leaf_flag[lrow] = 1;
 }
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
         mb.kind = 0;
         mb.block = -1;
         if (item_units) {
-            mb.kind = p.items[item].kind;
+            mb.kind = staged_kind(p.items[item]);
             mb.block = p.items[item].block;
         }
 #pragma unroll
@@ -489,7 +491,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
         if (MODE != kDw && has_vec) f2_unpack8(*reinterpret_cast<const uint4 *>(p.w + my_col), wv);
         const float gscale = p.grad_scale;
         TreeStackF2<4, 4> tree;            // levels log2(R)..3 of the 16-leaf unit
-        int32_t kind = 0, block = -1, quarter = 0;
+        int32_t kind = 0, block = -1, quarter = 0, qmask = 0;
         int s = 0;
         uint32_t parity = 0;
         int64_t u = cluster_id;                               // current quarter unit
@@ -518,11 +520,13 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
             if (T::kLeaves && sub == 0) {                    // item header, staged by the producer
                 const int2 hd = item_hdr[s];
                 quarter = half_unit ? int((q_full * n_clusters + (cluster_id >> 1)) & 3) : int(u & 3);
-                kind = hd.x;
+                kind = hd.x & 0xff;
+                qmask = hd.x >> 8;
                 block = hd.y;
-                if ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1)) {
+                const bool blocked = kind == kItemWhole || kind == kItemQuarters;
+                if ((blocked && (block < 0 || block >= p.ws.n_blocks)) || (!blocked && kind != kItemSpill)) {
                     if (t == 0 && rank == 0) set_status(p.ws.hdr, kStPlan);
-                    kind = 2;
+                    kind = kBadItem;
                 }
             }
             const StageMeta *m = meta + s * R;
@@ -576,22 +580,24 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     }
                 }
                 if (T::kLeaves) {
-                    if (kind == 0) {
+                    if (kind == kItemWhole || kind == kItemQuarters) {
+                        // a quarter of a kind-2 item that the call does not hold is skipped
+                        const bool keep = kind == kItemWhole || ((qmask >> quarter) & 1);
                         if (R > 1) mini.template push_static<0>(leaf, r);
                         if (r == R - 1) {
                             tree.template push_static<kLogR>(leaf, sub);
-                            if (sub == kUnitBatches - 1) {           // leaf[] is the quarter partial
+                            if (sub == kUnitBatches - 1 && keep) {   // leaf[] is the quarter partial
                                 if (has_vec)
                                     st_global_f2x4(p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + my_col, leaf);
                                 if (t == 0 && rank == 0) mark_quarter(p.ws, block, quarter);
-                            } else if (half_unit && sub == kUnitBatches / 2 - 1) {   // leaf[] is the eighth partial
+                            } else if (half_unit && sub == kUnitBatches / 2 - 1 && keep) {   // the eighth partial
                                 const int half = int(cluster_id & 1);
                                 float *dst = half ? p.ws.eighth : p.ws.block_partial;
                                 if (has_vec) st_global_f2x4(dst + (int64_t(block) * 4 + quarter) * H + my_col, leaf);
                                 if (t == 0 && rank == 0) mark_eighth(p.ws, block, quarter, half);
                             }
                         }
-                    } else if (kind == 1 && act) {
+                    } else if (kind == kItemSpill && act) {
                         if (has_vec) st_global_f2x4(p.ws.spill + int64_t(m[r].lrow) * H + my_col, leaf);
                         if (t == 0 && rank == 0) mark_spilled_row(p.ws, m[r].lrow);
                     }
@@ -771,11 +777,15 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
             // moved on to the next unit already (D < kGroups), so it is kept
             // with the table
             const int2 hd = *reinterpret_cast<const int2 *>(reinterpret_cast<const uint8_t *>(tb) + 64 * 16);
-            kind = hd.x;
+            // quarter items (kind 2) are spilled row by row here: a unit of this
+            // kernel is a whole block, and the finalize rebuilds those quarters
+            kind = hd.x & 0xff;
             block = hd.y;
-            if (T::kLeaves && ((kind == 0 && (block < 0 || block >= p.ws.n_blocks)) || (kind != 0 && kind != 1))) {
+            if (kind == kItemQuarters) kind = kItemSpill;
+            if (T::kLeaves && ((kind == kItemWhole && (block < 0 || block >= p.ws.n_blocks)) ||
+                               (kind != kItemWhole && kind != kItemSpill))) {
                 if (lane == 0) set_status(p.ws.hdr, kStPlan);
-                kind = 2;                                  // malformed item: contributes nothing
+                kind = kBadItem;                           // malformed item: contributes nothing
             }
         }
         {

@@ -82,7 +82,9 @@ def test_plan_covers_every_active_row_once(cfg, kind, rpt):
     for tok in lay.calls[:40]:
         buf, n, whole, spill = _plan(tok, rpt, wl.n_tokens)
         kind_a, block, count, prow, lrow = _items(buf, n)
-        assert np.all(kind_a[:whole] == 0) and np.all(kind_a[whole:] == 1)
+        n_sp_items = (spill + 63) // 64
+        assert np.all(kind_a[:whole] == 0) and np.all(kind_a[n - n_sp_items:] == 1)
+        assert np.all(kind_a[whole:n - n_sp_items] == 2)
         for i in range(n):
             used = lrow[i][lrow[i] >= 0]
             pr = prow[i][lrow[i] >= 0]
@@ -94,7 +96,18 @@ def test_plan_covers_every_active_row_once(cfg, kind, rpt):
                 b = block[i]
                 assert np.array_equal(used, np.arange(b * 64, min(b * 64 + 64, N)))
                 whole_blocks.append(b)
-        assert int(np.sum(count[whole:])) == spill
+            if kind_a[i] == 2:                        # complete quarters of a cut block, each row at its place
+                b = block[i]
+                slots = np.nonzero(lrow[i] >= 0)[0]
+                assert np.array_equal(lrow[i][slots], b * 64 + slots)
+                mask = np.frombuffer(buf.tobytes(), dtype=np.int32).reshape(n, 132)[i, 3]
+                for q in range(4):
+                    q_rows = np.arange(b * 64 + 16 * q, min(b * 64 + 16 * q + 16, N))
+                    if (mask >> q) & 1:
+                        assert q_rows.size and np.isin(q_rows, used).all()
+                    else:
+                        assert not np.isin(q_rows, used).any()
+        assert int(np.sum(count[n - n_sp_items:])) == spill
     assert seen.max() <= 1
     assert len(set(whole_blocks)) == len(whole_blocks)
 
@@ -102,7 +115,19 @@ def test_plan_covers_every_active_row_once(cfg, kind, rpt):
 def test_plan_whole_vs_cut_blocks():
     tok = np.arange(0, 130, dtype=np.int32)              # ids 0..129 of N=200: blocks 0,1 whole, block 2 cut
     buf, n, whole, spill = _plan(tok, 1, 200)
-    assert (whole, spill) == (2, 2)
+    assert (n, whole, spill) == (3, 2, 2)
+    tok = np.arange(0, 150, dtype=np.int32)              # block 2 cut after its first quarter (128..143) and 6 rows
+    buf, n, whole, spill = _plan(tok, 1, 200)
+    assert (n, whole, spill) == (4, 2, 6)
+    kind_a, block, count, prow, lrow = _items(buf, n)
+    assert list(kind_a) == [0, 0, 2, 1] and block[2] == 2 and count[2] == 16
+    assert np.frombuffer(buf.tobytes(), dtype=np.int32).reshape(n, 132)[2, 3] == 0b0001
+    tok = np.arange(190, 200, dtype=np.int32)            # block 2's last 2 rows, block 3 (192..199) whole
+    buf, n, whole, spill = _plan(tok, 1, 200)
+    assert (n, whole, spill) == (2, 1, 2)
+    tok = np.arange(176, 199, dtype=np.int32)            # block 2's last quarter; block 3 cut short of row 199
+    buf, n, whole, spill = _plan(tok, 1, 200)
+    assert (n, whole, spill) == (2, 0, 7)
     tok = np.arange(128, 200, dtype=np.int32)            # block 2 (128..191) whole, block 3 (192..199) whole
     buf, n, whole, spill = _plan(tok, 1, 200)
     assert (whole, spill) == (2, 0)
@@ -136,20 +161,39 @@ def _plan_ref(tok, rpt, ntok):
     lrows = (tok[order].astype(np.int64)[:, None] * rpt + np.arange(rpt)).ravel()
     prows = (order.astype(np.int64)[:, None] * rpt + np.arange(rpt)).ravel()
     n_rows = ntok * rpt
-    whole, sp_l, sp_p = [], [], []
+    whole, quarter, sp_l, sp_p = [], [], [], []
     for b in np.unique(lrows // 64):
         sel = lrows // 64 == b
         if sel.sum() == min(64, n_rows - 64 * b):
             whole.append((0, b, prows[sel], lrows[sel]))
-        else:
-            sp_l.append(lrows[sel])
-            sp_p.append(prows[sel])
+            continue
+        mask, slots, qp = 0, [], []
+        for q in range(4):
+            q_rows = np.arange(64 * b + 16 * q, min(64 * b + 16 * q + 16, n_rows))
+            inq = sel & (lrows // 16 == 4 * b + q)
+            if q_rows.size and inq.sum() == q_rows.size:
+                mask |= 1 << q
+                slots.append(lrows[inq] - 64 * b)
+                qp.append((prows[inq], lrows[inq]))
+            elif inq.any():
+                sp_l.append(lrows[inq])
+                sp_p.append(prows[inq])
+        if mask:
+            quarter.append((b, mask, qp))
     sp_l = np.concatenate(sp_l) if sp_l else np.zeros(0, np.int64)
     sp_p = np.concatenate(sp_p) if sp_p else np.zeros(0, np.int64)
-    items = whole + [(1, -1, sp_p[k:k + 64], sp_l[k:k + 64]) for k in range(0, sp_l.size, 64)]
+    items = [(k, b, p, l, 0) for k, b, p, l in whole]
+    for b, mask, qp in quarter:
+        p64 = np.full(64, -1, np.int64)
+        l64 = np.full(64, -1, np.int64)
+        for p, l in qp:
+            p64[l - 64 * b] = p
+            l64[l - 64 * b] = l
+        items.append((2, b, p64, l64, mask))
+    items += [(1, -1, sp_p[k:k + 64], sp_l[k:k + 64], 0) for k in range(0, sp_l.size, 64)]
     out = np.full((len(items), 132), -1, dtype=np.int32)
-    for i, (kind, b, p, l) in enumerate(items):
-        out[i, :4] = (kind, b, p.size, 0)
+    for i, (kind, b, p, l, mask) in enumerate(items):
+        out[i, :4] = (kind, b, int((l >= 0).sum()), mask)
         out[i, 4:4 + p.size] = p
         out[i, 68:68 + l.size] = l
     return out, len(whole), int(sp_l.size)
