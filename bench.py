@@ -56,7 +56,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph")
-    ap.add_argument("--streams", type=int, default=32, help="streams the calls of a multi-call layout fork over")
+    ap.add_argument("--streams", type=int, default=64, help="streams the calls of a multi-call layout fork over")
+    ap.add_argument("--schedule", default="lpt", choices=["lpt", "rr"],
+                    help="how calls are dealt to the streams: largest first to the least-loaded stream, or round robin")
     ap.add_argument("--clock-log", default=None, help="keep the nvidia-smi clock samples in this CSV file")
     ap.add_argument("--max-tokens", type=int, default=0,
                     help="cut the workload to its first N logical tokens (profiling runs only)")
@@ -223,7 +225,8 @@ class Step:
     With `chain`, the step is the residual add + norm forward and the backward
     with the residual gradient, scaled by the loss seed's 1/D."""
 
-    def __init__(self, wl, lay, x_log, dy_log, w, rpt, device, r_log=None, dres_log=None, n_streams=32):
+    def __init__(self, wl, lay, x_log, dy_log, w, rpt, device, r_log=None, dres_log=None, n_streams=64,
+                 schedule="lpt"):
         import torch
         import invariant_rmsnorm_fwd_gb300 as rb
         self.rb = rb
@@ -252,6 +255,7 @@ class Step:
         self.dw = torch.empty(H, dtype=torch.float32, device=device)
         self.n_active = wl.n_tokens
         self.n_streams = n_streams
+        self.schedule = schedule
         self.bwd_events = []
 
     def fwd_call(self, c, st):
@@ -270,9 +274,27 @@ class Step:
     def finalize(self, st):
         self.ws.finalize(self.dw, st, grad_scale=self.scale)
 
+    def _assignment(self, n_lanes):
+        """(call index, lane) pairs in issue order.  Calls without active tokens
+        launch nothing and are left out; with schedule "lpt" the others go, largest
+        first, to the lane with the fewest active rows so far (longest processing
+        time first), so the lanes end close together; "rr" deals them round robin
+        in layout order."""
+        sizes = [int((c.cl.tok_id >= 0).sum().item()) if c.cl.n_tokens else 0 for c in self.calls]
+        idx = [i for i, n in enumerate(sizes) if n > 0]
+        if self.schedule == "rr":
+            return [(i, k % n_lanes) for k, i in enumerate(idx)]
+        load = [0] * n_lanes
+        out = []
+        for i in sorted(idx, key=lambda i: -sizes[i]):
+            lane = min(range(n_lanes), key=lambda j: load[j])
+            load[lane] += sizes[i]
+            out.append((i, lane))
+        return out
+
     def _fan(self, fn, stream):
         """Calls of a multi-call layout are independent (they touch disjoint rows and
-        blocks of the workspace), so they are spread over n_streams streams (32 by default) that
+        blocks of the workspace), so they are spread over n_streams streams (64 by default) that
         fork from and join back into `stream`; one-call layouts stay on `stream`."""
         import torch
         lanes = self._lanes(stream)
@@ -280,16 +302,18 @@ class Step:
             for c in self.calls:
                 fn(c, stream)
             return
+        if getattr(self, "_plan", None) is None:
+            self._plan = self._assignment(len(lanes))
         ev = torch.cuda.Event()
         ev.record(stream)
-        for i, c in enumerate(self.calls):
-            st = lanes[i % len(lanes)]
-            if i < len(lanes):
-                st.wait_event(ev)
-            fn(c, st)
-        for st in lanes[:min(len(lanes), len(self.calls))]:
+        used = sorted({lane for _, lane in self._plan})
+        for lane in used:
+            lanes[lane].wait_event(ev)
+        for i, lane in self._plan:
+            fn(self.calls[i], lanes[lane])
+        for lane in used:
             e = torch.cuda.Event()
-            e.record(st)
+            e.record(lanes[lane])
             stream.wait_event(e)
 
     def run(self, stream):
@@ -675,7 +699,8 @@ def measure(wl, lay, data, args, device, flush, stream, hbm_peak, dist=None, sam
     alone.  Returns (dict of figures, the Multi of steps)."""
     import torch
     import invariant_rmsnorm_fwd_gb300 as rb
-    steps = [Step(wl, lay, d[1], d[2], d[3], d[0], device, *d[4:], n_streams=args.streams) for d in data]
+    steps = [Step(wl, lay, d[1], d[2], d[3], d[0], device, *d[4:], n_streams=args.streams,
+                  schedule=args.schedule) for d in data]
     multi = Multi(steps, device)
     multi.run(stream)                           # kernels of one step, counted on an eager step
     torch.cuda.synchronize()
@@ -817,8 +842,8 @@ def main():
         ref_out = None
         bitwise = True
         for k, v in L.workload_layouts(wl).items():
-            so = [Step(wl, v, d[1], d[2], d[3], d[0], device, *d[4:], n_streams=args.streams)
-                  for d in steps_data]
+            so = [Step(wl, v, d[1], d[2], d[3], d[0], device, *d[4:], n_streams=args.streams,
+                       schedule=args.schedule) for d in steps_data]
             mm = Multi(so, device)
             t, _ = time_steps(mm, stream, max(3, args.steps // 2), 2, flush, graph=not args.no_graph)
             per[k] = {"ms": round(statistics.mean(t), 4), "calls": len(v.calls),

@@ -4,6 +4,11 @@
 #pragma once
 #include "host.cuh"
 
+// Fewest rows a team of a small call is given (see launch_split_t).
+#ifndef RBI_MIN_TEAM_ROWS
+#define RBI_MIN_TEAM_ROWS 128
+#endif
+
 namespace rbi {
 
 // ---------------------------------------------------------------- launches
@@ -47,14 +52,15 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
         teams = int64_t(per_sm) * d.sms;
     }
     // Every team pays the pipeline's ramp (barrier set-up, first metadata and
-    // bulk-copy latency), so a small call gives each team at least 64 rows
+    // bulk-copy latency), so a small call gives each team at least 128 rows
     // instead of spreading a few rows over every SM, but keeps at least an
     // eighth of the resident teams; calls issued on other streams fill the
-    // rest (measured on the many-call layouts with 32 streams: c2 1.06 ->
-    // 0.99 ms, c4 2.79 -> 2.73 ms against a quarter with 8 streams).
+    // rest.  Measured on the many-call layouts (calls of 4096 slots at hidden
+    // 5120, 2048 slots at hidden 8192, on 32 streams): 128 rows beat 64 by
+    // 1-2%, 32 and 256 rows lost 2-9%.
     {
         const int64_t rows_per_unit = (p.use_plan && ModeTraits<MODE>::kLeaves) ? kSplitUnitRows : R;
-        const int64_t min_units = (64 + rows_per_unit - 1) / rows_per_unit;
+        const int64_t min_units = (RBI_MIN_TEAM_ROWS + rows_per_unit - 1) / rows_per_unit;
         int64_t want = (p.n_units + min_units - 1) / min_units;
         if (want < teams / 8) want = teams / 8;
         if (want < teams) teams = want;

@@ -315,10 +315,14 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
 #pragma unroll
         for (int i = 0; i < kPrefetch; ++i) load(i, ring[i]);
     }
-    if (MODE != kDw && T::kNeedGx) {
-        for (int i = tid; i < HS; i += blockDim.x) wsm[i] = __uint_as_float(uint32_t(p.w[col0 + i]) << 16);
-    }
     if (K > 1) cluster_barrier(); else __syncthreads();
+    // The weights in shared memory are read by the stats warps only: they fill
+    // them after the barrier, so the producer's first copies are not held up by
+    // these loads.
+    if (T::kNeedGx && warp >= NC && warp < NC + NS) {
+        for (int i = tid - NC * 32; i < HS; i += NS * 32) wsm[i] = __uint_as_float(uint32_t(p.w[col0 + i]) << 16);
+        asm volatile("bar.sync 1, %0;" ::"r"(NS * 32) : "memory");
+    }
 
     if (warp == NC + NS) {
         // ------------------------------------------------ producer
