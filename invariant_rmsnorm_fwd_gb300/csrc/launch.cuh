@@ -52,18 +52,22 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
         teams = int64_t(per_sm) * d.sms;
     }
     // Every team pays the pipeline's ramp (barrier set-up, first metadata and
-    // bulk-copy latency), so a small call gives each team at least 128 rows
-    // instead of spreading a few rows over every SM, but keeps at least an
-    // eighth of the resident teams; calls issued on other streams fill the
-    // rest.  Measured on the many-call layouts (calls of 4096 slots at hidden
-    // 5120, 2048 slots at hidden 8192, on 32 streams): 128 rows beat 64 by
-    // 1-2%, 32 and 256 rows lost 2-9%.
+    // bulk-copy latency).  A call too small to give every resident team 64 rows
+    // gives each team at least 128 rows instead of spreading a few rows over
+    // every SM, but keeps at least an eighth of the resident teams; calls
+    // issued on other streams fill the rest.  Measured on the many-call layouts
+    // (calls of 4096 slots at hidden 5120, 2048 slots at hidden 8192): 128 rows
+    // beat 64 by 1-2%, 32 and 256 rows lost 2-9%; a call that fills the GPU at
+    // 64 rows per team (13,322 rows at hidden 4096) keeps every team.
     {
         const int64_t rows_per_unit = (p.use_plan && ModeTraits<MODE>::kLeaves) ? kSplitUnitRows : R;
-        const int64_t min_units = (RBI_MIN_TEAM_ROWS + rows_per_unit - 1) / rows_per_unit;
-        int64_t want = (p.n_units + min_units - 1) / min_units;
-        if (want < teams / 8) want = teams / 8;
-        if (want < teams) teams = want;
+        const int64_t units64 = (64 + rows_per_unit - 1) / rows_per_unit;
+        if ((p.n_units + units64 - 1) / units64 < teams) {
+            const int64_t min_units = (RBI_MIN_TEAM_ROWS + rows_per_unit - 1) / rows_per_unit;
+            int64_t want = (p.n_units + min_units - 1) / min_units;
+            if (want < teams / 8) want = teams / 8;
+            if (want < teams) teams = want;
+        }
     }
     if (teams > p.n_units) teams = p.n_units;
     if (teams < 1) return RMSNORM_OK;

@@ -796,7 +796,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
             int64_t off[kU];
             int32_t lrow[kU], prow[kU];
             uint4 xv[kU], dv[kU];
-            constexpr int kRv = (T::kRes && T::kNeedDy) ? kU : 1;   // dres registers (kAddDx*)
+            constexpr bool kDres = T::kRes && T::kNeedDy;           // dres streamed (kAddDx*)
+            constexpr int kRv = kDres ? kU : 1;                     // its registers
             uint4 rv[kRv];
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
@@ -806,11 +807,11 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                 prow[q] = e.prow;
                 xv[q] = make_uint4(0, 0, 0, 0);
                 dv[q] = make_uint4(0, 0, 0, 0);
-                if (kRv > 1) rv[q % kRv] = make_uint4(0, 0, 0, 0);
+                if (kDres) rv[q % kRv] = make_uint4(0, 0, 0, 0);
                 if (e.off >= 0 && has_vec) {
                     xv[q] = ld_shared_v4(buf + (q * kT + 0) * 512 + lane * 16);
                     if (T::kNeedDy || MODE == kAddFwd) dv[q] = ld_shared_v4(buf + (q * kT + 1) * 512 + lane * 16);
-                    if (kRv > 1) rv[q % kRv] = ld_shared_v4(buf + (q * kT + T::kResSlot) * 512 + lane * 16);
+                    if (kDres) rv[q % kRv] = ld_shared_v4(buf + (q * kT + T::kResSlot) * 512 + lane * 16);
                 }
             }
             // phase 1: the lane partials of every row sum of the group (two FMA
@@ -931,7 +932,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                             const f2_t rs2 = f2_make(rs, rs);
 #pragma unroll
                             for (int i = 0; i < 4; ++i) o[i] = f2_mul(rs2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
-                            if (kRv > 1) {
+                            if (kDres) {
                                 f2_t rf[4];
                                 f2_unpack8_v(rv[q % kRv], rf);
 #pragma unroll
