@@ -31,10 +31,11 @@ __global__ void ws_begin_kernel(WsView ws) {
 // reduces inputs [32g, 32g+32) for the 32 vectors (256 columns) of chunk c:
 // lane l owns vector 32c+l, so every load of a warp is one contiguous 512-byte
 // row piece.  Warp w forms inputs 2w and 2w+1 and adds them (level 1); the 16
-// pair results go through shared memory and warp 0 folds them with the
-// binary-counter stack (levels 2-5).  Pairs are added only when their right
-// half is non-empty, which is the pairwise tree with odd carry restricted to
-// an aligned group of 32; later passes reduce the group results the same way.
+// pair results go through shared memory and are added level by level (levels
+// 2-5), warp i forming element i of each level.  Pairs are added only when
+// their right half is non-empty, which is the pairwise tree with odd carry
+// restricted to an aligned group of 32; later passes reduce the group results
+// the same way.
 // In the first pass (from_blocks) an input is a block partial: the four
 // quarter partials as (q0 + q1) + (q2 + q3) (levels 5 and 6 of the 64-leaf
 // tree), a whole-block partial as is, or, for a block cut by a call boundary,
@@ -69,17 +70,17 @@ __device__ __forceinline__ void add_second_eighth(uint32_t state, int q, const f
 
 // The 16-leaf subtree of quarter q of a block from its spilled rows, for one
 // 8-column vector (src points at the block's row 0 of that vector): rows at or
-// beyond `rows` (past the multiset) are +0.0 leaves.  Eight rows are loaded
-// at a time (levels 1-3 of the tree over them), and the two eights are added
-// (level 4), earlier rows always on the left.
+// beyond `rows` (past the multiset) are +0.0 leaves.  Four rows are loaded at a
+// time (levels 1-2 of the tree over them), then the four quads are added
+// pairwise (levels 3-4), earlier rows always on the left.
 __device__ __forceinline__ void quarter_from_spill(const float *src, int H, int q, int64_t rows, float (&out)[8]) {
-    float n0[8];
+    float n[2][8];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        float x[8][8];
+    for (int quad = 0; quad < 4; ++quad) {
+        float x[4][8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int r = 16 * q + 8 * half + k;
+        for (int k = 0; k < 4; ++k) {
+            const int r = 16 * q + 4 * quad + k;
             if (r < rows) {
                 load8(src + int64_t(r) * H, x[k]);
             } else {
@@ -89,13 +90,13 @@ __device__ __forceinline__ void quarter_from_spill(const float *src, int H, int 
         }
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const float a01 = __fadd_rn(x[0][c], x[1][c]), a23 = __fadd_rn(x[2][c], x[3][c]);
-            const float a45 = __fadd_rn(x[4][c], x[5][c]), a67 = __fadd_rn(x[6][c], x[7][c]);
-            const float e = __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67));
-            if (half == 0) n0[c] = e;
-            else out[c] = __fadd_rn(n0[c], e);
+            const float e = __fadd_rn(__fadd_rn(x[0][c], x[1][c]), __fadd_rn(x[2][c], x[3][c]));
+            if ((quad & 1) == 0) n[quad >> 1][c] = e;
+            else n[quad >> 1][c] = __fadd_rn(n[quad >> 1][c], e);
         }
     }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) out[c] = __fadd_rn(n[0][c], n[1][c]);
 }
 
 constexpr int kTreeWarps = 16;                           // warps per CTA: 2 inputs each
@@ -199,21 +200,34 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, c
     }
 #pragma unroll
     for (int c = 0; c < 8; ++c) part[w][c][lane] = pair[c];
+    // the pair results, level by level: element i of the next level is
+    // (2i) + (2i + 1), an odd last element carried up unchanged; warp i forms
+    // element i (operands into registers, barrier, store, barrier)
+    for (int n = (m + 1) / 2; n > 1; n = (n + 1) / 2) {    // uniform across the CTA
+        __syncthreads();
+        float a[8];
+        const bool act = w < (n + 1) / 2;
+        if (act) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) a[c] = part[2 * w][c][lane];
+            if (2 * w + 1 < n) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) a[c] = __fadd_rn(a[c], part[2 * w + 1][c][lane]);
+            }
+        }
+        __syncthreads();
+        if (act) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) part[w][c][lane] = a[c];
+        }
+    }
     __syncthreads();
     if (w == 0 && has_vec) {
-        const int np = (m + 1) / 2;                      // pair results present
-        TreeStack<8> st;
-        for (int i = 0; i < np; ++i) {
-            float x[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) x[c] = part[i][c][lane];
-            st.push(x, i, 0);
-        }
         float res[8];
-        st.fold(np, res);
-        if (scale != 1.f) {                              // only on the root of a scaled finalize
 #pragma unroll
-            for (int c = 0; c < 8; ++c) res[c] = __fmul_rn(res[c], scale);
+        for (int c = 0; c < 8; ++c) {
+            res[c] = part[0][c][lane];
+            if (scale != 1.f) res[c] = __fmul_rn(res[c], scale);   // only on the root of a scaled finalize
         }
         float *dst = out + g * int64_t(H) + int64_t(v) * 8;
         st_global_f32x4(dst, res[0], res[1], res[2], res[3]);
