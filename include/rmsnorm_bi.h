@@ -237,7 +237,7 @@ int dweight_combine(const float *roots, int64_t n_roots, int64_t hidden, float g
  * gemm_dw_workspace_bytes: workspace for n_logical_rows tokens (N < 2^31 - 64),
  *   in_features I and out_features O (multiples of 8, 8 .. 65536): a header
  *   with the status word, a flag per token, and the logical-order copies of
- *   x and dy in bf16 (rows padded to multiples of 64 and 128 elements, the
+ *   x and dy in bf16 (rows padded to multiples of 128 and 256 elements, the
  *   token count to a multiple of 64).  0 for unsupported sizes.
  * gemm_dw_begin: writes the header, clears flags and status and zeroes the
  *   padding token rows.
@@ -251,8 +251,8 @@ int dweight_combine(const float *roots, int64_t n_roots, int64_t hidden, float g
  *   RMSNORM_STATUS_MISSING) and writes dW (FP32 [O][I], row-major) =
  *   grad_scale * sum over logical rows g of dy_g^T x_g on the tensor cores
  *   (tcgen05, bf16 operands, FP32 accumulation in tensor memory): each
- *   128 x 256 tile of dW is summed by one CTA over slabs of 64 tokens in
- *   logical order, so the summation order depends on (N, I, O) only and dW
+ *   256 x 256 tile of dW is summed by one pair of CTAs over slabs of 64
+ *   tokens in logical order, so the summation order depends on (N, I, O) only and dW
  *   is bitwise the same for every layout of the multiset (and every run on
  *   the same GPU model).  grad_scale multiplies each element once.  N == 0
  *   gives dW = +0.0.  A pipeline wait that runs out (about 1 s) sets

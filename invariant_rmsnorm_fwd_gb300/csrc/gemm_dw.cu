@@ -9,10 +9,11 @@
 // (the canonical logical id) of two logical-order buffers in the workspace.
 // The finalize then forms dW = sum_g dy_g^T x_g over all N logical rows,
 // dW[o][i] = sum_g DY[g][o] * X[g][i], in FP32 from the bf16 rows, with the
-// hand-written tensor-core kernel below: every 128 x 256 tile of dW is owned
-// by one CTA, which walks k = the logical token id upward in slabs of 64
-// tokens and accumulates them in tensor memory in that order.  The summation
-// order therefore depends only on (N, I, O), never on how the rows arrived.
+// hand-written tensor-core kernel below: every 256 x 256 tile of dW is owned
+// by one pair of CTAs, which walks k = the logical token id upward in slabs
+// of 64 tokens and accumulates them in tensor memory in that order.  The
+// summation order therefore depends only on (N, I, O), never on how the rows
+// arrived.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -30,15 +31,10 @@ constexpr uint32_t kGemmMagic = 0x47445732u;   // "GDW2"
 
 // Tile shape of the contraction: dW rows (o) in tiles of 128, columns (i) in
 // tiles of up to 256, tokens (k) in slabs of 64; four slabs in flight.
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr int kBM = 128, kBK = 64;                       // rows of a CTA's half tile, tokens per slab
 constexpr int kChunk = 64;                               // elements of one 128-byte swizzle row
 constexpr int kChunkBytes = kChunk * kBK * 2;            // one TMA box: 64 (o or i) x 64 tokens, 8 KB
-constexpr int kABytes = kBM * kBK * 2;                   // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;                   // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kGemmSmem = kStages * kStageBytes + 1024;  // + alignment slack of the swizzle atoms
 constexpr int kGemmThreads = 192;                        // producer, MMA, four epilogue warps
-constexpr uint32_t kTmemCols = 2 * kBN;                  // two accumulators
 
 struct GemmWsHeader {
     uint32_t magic;
@@ -47,7 +43,7 @@ struct GemmWsHeader {
 };
 
 // Logical-order copies of x and dy.  Row pitches are padded (i to a multiple
-// of 64, o to a multiple of 128) and the token count to a multiple of 64, so
+// of 128, o to a multiple of 256) and the token count to a multiple of 64, so
 // every TMA box lies inside its tensor.  Padding rows are zeroed by begin (they
 // enter every sum); padding columns are never written and only ever reach
 // rows or columns of the product that are not stored.
@@ -70,8 +66,8 @@ struct GemmLayout {
     int64_t np, ip, op, off_flag, off_x, off_dy, total;
     GemmLayout(int64_t N, int64_t I, int64_t O) {
         np = align_up(N, kBK);
-        ip = align_up(I, kChunk);
-        op = align_up(O, kBM);
+        ip = align_up(I, 2 * kChunk);                    // a CTA pair splits each tile's columns in two
+        op = align_up(O, 2 * kBM);                       // a CTA pair's tile has 256 rows
         off_flag = 256;
         off_x = align_up(off_flag + N * 4, 1024);
         off_dy = align_up(off_x + np * ip * 2, 1024);
@@ -171,7 +167,7 @@ struct GemmParams {
     float *dw;                 // [O][I] row-major
     int32_t *status;           // workspace status word
     int32_t O, I;
-    int32_t ip;                // padded i extent (multiple of 64)
+    int32_t ip;                // padded i extent (multiple of 128)
     int32_t m_tiles, n_tiles, k_slabs;
     float scale;
 };
@@ -179,56 +175,84 @@ struct GemmParams {
 // dW = scale * DY^T X on the tensor cores.  A = DY^T (o x k) and B = X (k x i)
 // are both read MN-major straight from the logical-order copies: a TMA box is
 // 64 tokens (k) by 64 consecutive o (or i), stored with the 128-byte swizzle,
-// which is the canonical MN-major operand layout of the MMA.
+// which is the canonical MN-major operand layout of the MMA.  Persistent CTA
+// pairs take the tiles t = pair, pair + pairs, ... with o-tile t % m_tiles;
+// each tile walks the token slabs in ascending order and its first MMA
+// overwrites the accumulator, so every element's summation order depends on
+// (N, I, O) only.
+// ---------------------------------------------------------------- the contraction on CTA pairs
 //
-// Persistent CTAs (one per SM), tiles t = blockIdx.x, +gridDim.x, ... with
-// o-tile = t % m_tiles.  Warp roles:
-//   warp 0, lane 0: producer: per token slab, waits for the stage to be free,
-//                   loads the A box pair and up to four B boxes;
-//   warp 1, lane 0: MMA issuer: per slab four K = 16 MMAs into the tile's
-//                   accumulator (two accumulators in tensor memory, so the
-//                   next tile's MMAs overlap this tile's epilogue); slab
-//                   order is k order, the first MMA of a tile overwrites;
-//   warps 2-5:      epilogue: tensor memory -> registers -> dW (rows < O,
-//                   columns < I), times scale.
-// Every wait gives up after about a second: the CTA then raises its abort
-// flag and RMSNORM_STATUS_TIMEOUT, the producer waits (bounded) for the TMA
-// boxes it issued, the MMA issuer for its MMAs, and tensor memory is freed
-// before the CTA exits.
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_dw_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
-                   const GemmParams p) {
+// The same product with 256 x 256 tiles of dW per pair of CTAs (a 2-CTA
+// cluster on two SMs): CTA r holds rows [128 r, 128 r + 128) of the tile's A
+// and columns [r N/2, (r + 1) N/2) of its B, and one K = 16 MMA of the pair
+// (tcgen05.mma.cta_group::2, M = 256) reads both halves of both operands, so
+// each CTA's shared memory carries half of B instead of all of it.  Each
+// CTA's tensor memory receives its 128 rows of the tile.
+// Roles (per CTA, both ranks unless noted):
+//   warp 0, lane 0: producer: the CTA's A and B boxes of each slab into its
+//                   own ring.  Both producers arrive on rank 0's full[s]
+//                   (count 2) with the bytes they expect; rank 1's copies
+//                   count their bytes there too (cta_group::2 copies);
+//   warp 1, lane 0, rank 0: MMA issuer: waits for full[s], four pair MMAs,
+//                   then one commit that arrives on empty[s] of both CTAs;
+//                   after a tile's last slab, on acc_full[a] of both;
+//   warps 2-5:      epilogue of the CTA's 128 rows; each warp then arrives on
+//                   rank 0's acc_empty[a] (count 8), which the MMA issuer
+//                   waits for before it overwrites that accumulator (two of
+//                   256 columns, so one tile's epilogue overlaps the next).
+// Every wait is bounded.  At the end rank 1's producer tells rank 0 how many
+// slabs it issued; rank 0's producer makes the arrivals that either side did
+// not make for the last slabs and waits for those phases, so no copy of
+// either CTA is in flight when the pair meets at the final cluster barrier
+// and frees its tensor memory.
+constexpr int kPairStages = 7;
+constexpr int kPairABytes = kBM * kBK * 2;               // 16 KB: this CTA's 128 rows of A
+constexpr int kPairBBytes = kBM * kBK * 2;               // 16 KB: this CTA's half (<= 128 columns) of B
+constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
+constexpr int kPairSmem = kPairStages * kPairStageBytes + 1024;
+constexpr uint32_t kPairTmemCols = 512;                  // two 256-column accumulators per CTA
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm_dw_pair_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
+                        const GemmParams p) {
     using namespace rbi;
     extern __shared__ uint8_t gemm_smem[];
-    __shared__ uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], mma_done;
+    __shared__ uint64_t full[kPairStages], empty[kPairStages], acc_full[2], acc_empty[2], mma_done, peer_done;
     __shared__ uint32_t tmem_slot;
+    __shared__ uint32_t peer_issued;                      // rank 0: slabs rank 1 issued (written by rank 1)
     __shared__ volatile int32_t abort_flag;
-    // swizzle atoms start on 1024-byte boundaries of the shared window
     uint8_t *tiles = gemm_smem + ((1024u - (smem_addr(gemm_smem) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int pair = int(blockIdx.x >> 1), n_pairs = int(gridDim.x >> 1);
     const int total = p.m_tiles * p.n_tiles;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&full[s], 2);
             mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 4);
+            mbar_init(&acc_empty[a], 8);
         }
         mbar_init(&mma_done, 1);
+        mbar_init(&peer_done, 1);
+        peer_issued = 0;
         abort_flag = 0;
         fence_mbar_init();
     }
+    cluster_barrier();                                    // both CTAs' barriers exist before any remote arrival
     if (warp == 1) {
-        umma::tmem_alloc(&tmem_slot, kTmemCols);
-        umma::tmem_relinquish();
+        umma::tmem_alloc_pair(&tmem_slot, kPairTmemCols);
+        umma::tmem_relinquish_pair();
     }
     umma::fence_before();
-    __syncthreads();
+    cluster_barrier();
     umma::fence_after();
     const uint32_t tmem = tmem_slot;
+    const uint32_t leader_full = map_to_rank(smem_addr(&full[0]), 0);
+    const uint32_t leader_acc_empty = map_to_rank(smem_addr(&acc_empty[0]), 0);
 
     auto give_up = [&]() {
         abort_flag = 1;
@@ -236,48 +260,84 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     };
 
     if (warp == 0 && lane == 0) {
-        // ------------------------------------------------ producer
-        int g = 0;                                            // slabs issued by this CTA
-        for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x) {
+        // ------------------------------------------------ producer (both CTAs)
+        int g = 0;
+        for (int t = pair; t < total && !abort_flag; t += n_pairs) {
             const int mt = t % p.m_tiles, nt = t / p.m_tiles;
-            const int n0 = nt * kBN;
-            const int nb = min(kBN, p.ip - n0) / kChunk;      // B boxes of this tile (1..4)
+            const int n0 = nt * 2 * kBM;
+            const int half = min(2 * kBM, p.ip - n0) / 2;          // this CTA's columns: 64 or 128
+            const int nb = half / kChunk;
+            const int m0 = mt * 2 * kBM + int(rank) * kBM;
+            const int c0 = n0 + int(rank) * half;
+            const uint32_t bytes = uint32_t(kPairABytes + nb * kChunkBytes);
+            bool ok = true;
             for (int kb = 0; kb < p.k_slabs; ++kb) {
-                const int s = g % kStages, u = g / kStages;
+                const int s = g % kPairStages, u = g / kPairStages;
                 if (u > 0 && !mbar_wait_spin_bounded(&empty[s], uint32_t(u - 1) & 1u)) {
                     give_up();
+                    ok = false;
                     break;
                 }
-                if (abort_flag) break;
-                uint8_t *a = tiles + s * kStageBytes;
-                uint8_t *b = a + kABytes;
-                mbar_arrive_expect_tx(&full[s], uint32_t(kABytes + nb * kChunkBytes));
-                umma::tma_load_2d(a, &tmap_dy, mt * kBM, kb * kBK, &full[s]);
-                umma::tma_load_2d(a + kChunkBytes, &tmap_dy, mt * kBM + kChunk, kb * kBK, &full[s]);
-                for (int j = 0; j < nb; ++j) umma::tma_load_2d(b + j * kChunkBytes, &tmap_x, n0 + j * kChunk, kb * kBK, &full[s]);
+                if (abort_flag) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *a = tiles + s * kPairStageBytes;
+                uint8_t *b = a + kPairABytes;
+                if (rank == 0) {
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    umma::tma_load_2d(a, &tmap_dy, m0, kb * kBK, &full[s]);
+                    umma::tma_load_2d(a + kChunkBytes, &tmap_dy, m0 + kChunk, kb * kBK, &full[s]);
+                    for (int j = 0; j < nb; ++j)
+                        umma::tma_load_2d(b + j * kChunkBytes, &tmap_x, c0 + j * kChunk, kb * kBK, &full[s]);
+                } else {
+                    const uint32_t fb = leader_full + uint32_t(s) * 8u;
+                    mbar_arrive_expect_tx_remote(fb, bytes);
+                    umma::tma_load_2d_to_peer_bar(a, &tmap_dy, m0, kb * kBK, fb);
+                    umma::tma_load_2d_to_peer_bar(a + kChunkBytes, &tmap_dy, m0 + kChunk, kb * kBK, fb);
+                    for (int j = 0; j < nb; ++j)
+                        umma::tma_load_2d_to_peer_bar(b + j * kChunkBytes, &tmap_x, c0 + j * kChunk, kb * kBK, fb);
+                }
                 ++g;
             }
+            if (!ok) break;
         }
-        // the boxes of the last slabs issued may still be in flight: let them land
-        for (int i = g - 1; i >= 0 && i >= g - kStages; --i)
-            mbar_wait_bounded(&full[i % kStages], uint32_t(i / kStages) & 1u);
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------ MMA issuer
+        if (rank == 1) {
+            // tell rank 0 how many slabs this CTA issued
+            st_cluster_u32(map_to_rank(smem_addr(&peer_issued), 0), uint32_t(g));
+            mbar_arrive_remote(map_to_rank(smem_addr(&peer_done), 0));
+        } else {
+            // the last slabs of either CTA: make the arrivals the other side did
+            // not make, then wait until every copy of those phases has landed
+            int gp = g;
+            // rank 1 may itself be in a wait that runs out: allow it two limits
+            if (mbar_wait_bounded_cluster(&peer_done, 0) || mbar_wait_bounded_cluster(&peer_done, 0))
+                gp = int(peer_issued);
+            const int hi = g > gp ? g : gp;
+            for (int i = hi - 1; i >= 0 && i >= hi - kPairStages; --i) {
+                const int s = i % kPairStages;
+                if (i >= g) mbar_arrive(&full[s]);          // rank 0 never armed this phase
+                if (i >= gp) mbar_arrive(&full[s]);         // rank 1 never armed it
+                mbar_wait_bounded_cluster(&full[s], uint32_t(i / kPairStages) & 1u);
+            }
+        }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ------------------------------------------------ rank 0: MMA issuer for the pair
         int g = 0, it = 0;
-        for (int t = blockIdx.x; t < total && !abort_flag; t += gridDim.x, ++it) {
+        for (int t = pair; t < total && !abort_flag; t += n_pairs, ++it) {
             const int nt = t / p.m_tiles;
-            const int bn = min(kBN, p.ip - nt * kBN);
+            const int bn = min(2 * kBM, p.ip - nt * 2 * kBM);
             const int acc = it & 1, ua = it >> 1;
-            if (ua > 0 && !mbar_wait_spin_bounded(&acc_empty[acc], uint32_t(ua - 1) & 1u)) {
+            if (ua > 0 && !mbar_wait_spin_bounded_cluster(&acc_empty[acc], uint32_t(ua - 1) & 1u)) {
                 give_up();
                 break;
             }
             umma::fence_after();
-            const uint32_t d = tmem + uint32_t(acc * kBN);
-            const uint32_t idesc = umma::idesc_bf16_mn(kBM, uint32_t(bn));
+            const uint32_t d = tmem + uint32_t(acc * 2 * kBM);
+            const uint32_t idesc = umma::idesc_bf16_mn(2 * kBM, uint32_t(bn));
             bool ok = true;
             for (int kb = 0; kb < p.k_slabs; ++kb, ++g) {
-                const int s = g % kStages, u = g / kStages;
+                const int s = g % kPairStages, u = g / kPairStages;
                 if (!mbar_wait_spin_bounded(&full[s], uint32_t(u) & 1u)) {
                     give_up();
                     ok = false;
@@ -288,43 +348,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 }
                 umma::fence_after();
-                const uint32_t a = smem_addr(tiles + s * kStageBytes);
-                const uint32_t b = a + kABytes;
+                const uint32_t a = smem_addr(tiles + s * kPairStageBytes);
+                const uint32_t b = a + kPairABytes;
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {             // 16 tokens per MMA: two 8-row groups
+                for (int kk = 0; kk < kBK / 16; ++kk) {
                     const uint64_t ad = umma::desc_sw128(a + kk * 2048, kChunkBytes, 1024);
                     const uint64_t bd = umma::desc_sw128(b + kk * 2048, kChunkBytes, 1024);
-                    umma::mma_bf16(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    umma::mma_bf16_pair(d, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma::commit(&empty[s]);                      // the stage is free once these MMAs are done
+                umma::commit_pair_multicast(&empty[s], 3);   // the stage is free in both CTAs
             }
             if (!ok) break;
-            umma::commit(&acc_full[acc]);                     // the tile's sum is complete
+            umma::commit_pair_multicast(&acc_full[acc], 3); // the tile is complete in both CTAs
         }
-        umma::commit(&mma_done);
+        umma::commit_pair_multicast(&mma_done, 1);
         mbar_wait_bounded(&mma_done, 0);                      // no MMA in flight past this point
     } else if (warp >= 2) {
-        // ------------------------------------------------ epilogue
-        const int q = warp & 3;                               // the tensor-memory lanes this warp may read
+        // ------------------------------------------------ epilogue (both CTAs): this CTA's 128 rows
+        const int q = warp & 3;
         int it = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+        for (int t = pair; t < total; t += n_pairs, ++it) {
             const int mt = t % p.m_tiles, nt = t / p.m_tiles;
-            const int n0 = nt * kBN;
-            const int bn = min(kBN, p.ip - n0);
+            const int n0 = nt * 2 * kBM;
+            const int bn = min(2 * kBM, p.ip - n0);
             const int acc = it & 1, ua = it >> 1;
-            bool ready = mbar_wait_bounded(&acc_full[acc], uint32_t(ua) & 1u);
-            ready = __all_sync(kFull, ready);
-            if (!ready) {
+            bool done = mbar_wait_bounded(&acc_full[acc], uint32_t(ua) & 1u);
+            done = __all_sync(kFull, done);
+            if (!done) {
                 if (lane == 0) give_up();
                 break;
             }
             umma::fence_after();
-            const int64_t m = int64_t(mt) * kBM + q * 32 + lane;  // dW row of this lane
+            const int64_t m = int64_t(mt) * 2 * kBM + int64_t(rank) * kBM + q * 32 + lane;
             float *row = p.dw + m * p.I;
             for (int c = 0; c < bn; c += 32) {
                 uint32_t v[32];
                 __syncwarp();
-                umma::ld_32x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * kBN + c), v);
+                umma::ld_32x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * 2 * kBM + c), v);
                 umma::wait_ld();
                 if (m < p.O) {
 #pragma unroll
@@ -344,15 +404,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             umma::fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (lane == 0) {
+                if (rank == 0) mbar_arrive(&acc_empty[acc]);
+                else mbar_arrive_remote(leader_acc_empty + uint32_t(acc) * 8u);
+            }
         }
     }
+    __syncwarp();
     umma::fence_before();
-    __syncthreads();
+    cluster_barrier();                                    // no remote arrival, copy or MMA targets an exited CTA
     if (warp == 1) {
         __syncwarp();
         umma::fence_after();
-        umma::tmem_dealloc(tmem, kTmemCols);
+        umma::tmem_dealloc_pair(tmem, kPairTmemCols);
     }
 }
 
@@ -472,19 +536,26 @@ extern "C" int gemm_dw_finalize(void *workspace, int64_t n_logical_rows, int64_t
     gp.O = int32_t(O);
     gp.I = int32_t(I);
     gp.ip = int32_t(ws.ip);
-    gp.m_tiles = int32_t(ws.op / kBM);
-    gp.n_tiles = int32_t((ws.ip + kBN - 1) / kBN);
     gp.k_slabs = int32_t(ws.np / kBK);
     gp.scale = grad_scale;
+    gp.m_tiles = int32_t(ws.op / (2 * kBM));
+    gp.n_tiles = int32_t((ws.ip + 2 * kBM - 1) / (2 * kBM));
     static std::once_flag attr_once;
     static cudaError_t attr_rc = cudaSuccess;
+    static int max_pairs = 0;
     std::call_once(attr_once, [] {
-        attr_rc = cudaFuncSetAttribute(gemm_dw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+        attr_rc = cudaFuncSetAttribute(gemm_dw_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+        if (attr_rc != cudaSuccess) return;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kGemmThreads);
+        cfg.dynamicSmemBytes = kPairSmem;
+        attr_rc = cudaOccupancyMaxActiveClusters(&max_pairs, gemm_dw_pair_kernel, &cfg);
     });
-    if (attr_rc != cudaSuccess) return RMSNORM_ERR_CUDA;
-    const int64_t tiles = int64_t(gp.m_tiles) * gp.n_tiles;
-    const int grid = int(tiles < d->sms ? tiles : d->sms);
-    gemm_dw_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(tm_dy, tm_x, gp);
+    if (attr_rc != cudaSuccess || max_pairs < 1) return RMSNORM_ERR_CUDA;
+    const int64_t tiles = int64_t(gp.m_tiles) * gp.n_tiles;   // persistent pairs, one per SM pair
+    const int pairs = int(tiles < max_pairs ? tiles : max_pairs);
+    gemm_dw_pair_kernel<<<2 * pairs, kGemmThreads, kPairSmem, s>>>(tm_dy, tm_x, gp);
     if (cudaGetLastError() != cudaSuccess) return RMSNORM_ERR_CUDA;
     rbi::count_launch();
     return RMSNORM_OK;

@@ -209,6 +209,10 @@ __device__ __forceinline__ bool mbar_wait_spin_bounded(uint64_t *bar, uint32_t p
     }
 }
 
+// The spinning wait with cluster-scope acquire, for an mbarrier that threads
+// of another CTA of the cluster arrive on.
+__device__ __forceinline__ bool mbar_wait_spin_bounded_cluster(uint64_t *bar, uint32_t parity);
+
 // One-dimensional bulk copy global -> this CTA's shared memory, completion
 // counted in bytes on `bar`.  Both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -241,6 +245,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_wait_spin_bounded_cluster(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
 __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
@@ -258,6 +272,18 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t *bar, uint32_
 // CTA's), releasing this thread's earlier shared-memory stores at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// Arrival with an expected transaction count on the mbarrier at shared::cluster
+// address `addr` (possibly another CTA's).  CTA-scope release: the arriving
+// thread publishes no data of its own (the bytes counted are asynchronous
+// copies, which complete on the barrier themselves).
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t addr, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(addr), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {

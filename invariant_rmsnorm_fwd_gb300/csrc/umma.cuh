@@ -70,6 +70,44 @@ __device__ __forceinline__ void ld_32x32(uint32_t taddr, uint32_t (&v)[32]) {
 }
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---------------------------------------------------------------- CTA pairs (cta_group::2)
+//
+// A pair of CTAs (ranks 0 and 1 of a 2-CTA cluster, on two SMs) runs one MMA
+// of twice the rows: each CTA holds half of A (its M/2 rows) and half of B
+// (its N/2 columns) in its own shared memory at the same offsets, the MMA is
+// issued by one thread of rank 0, and each CTA's tensor memory receives its
+// M/2 rows of D (all N columns).  Allocation and release of tensor memory are
+// performed by one warp of each CTA of the pair.
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// One arrival on the mbarrier at this offset in every CTA of `cta_mask` once
+// the pair MMAs this thread issued so far have completed.
+__device__ __forceinline__ void commit_pair_multicast(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 // Box of a 2-D tiled tensor map at element coordinates (x inner, y outer) into
@@ -81,6 +119,18 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// The same load issued by rank 1 of a CTA pair into its own shared memory,
+// with completion counted on an mbarrier of rank 0 (`bar_cluster`: a
+// shared::cluster address of the peer's barrier).
+__device__ __forceinline__ void tma_load_2d_to_peer_bar(void *dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                                        uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
         : "memory");
 }
 
