@@ -107,18 +107,11 @@ int launch_split(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStr
     }
 }
 
-template <int MODE, int P2>
+template <int MODE, int P>
 int launch_small(const KParams &p, const DeviceInfo &d, cudaStream_t stream) {
-    // warp steps per group: the fused backward keeps the leaf trees in
-    // registers, and two steps per group avoid spills (measured faster than
-    // four at hidden 128); two-tensor modes take four, the forward eight
-    using T = ModeTraits<MODE>;
-    constexpr int U = (T::kLeaves && (T::kTensors >= 3 || MODE == kDxDw)) ? 2 : T::kTensors >= 2 ? 4 : 8;
-    constexpr int kSteps = kBlockRows / (32 / P2);
-    constexpr int kU = U < kSteps ? U : kSteps;
-    constexpr int smem = kSmallWarps * small_warp_bytes(kU, T::kTensors, kSteps / kU);
+    constexpr int smem = kSmallWarps * SmallShape<MODE, P>::kWarpBytes;
     constexpr int threads = kSmallWarps * 32;
-    auto kern = small_row_kernel<MODE, P2, U>;
+    auto kern = small_row_kernel<MODE, P>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
     int per_sm = 0;

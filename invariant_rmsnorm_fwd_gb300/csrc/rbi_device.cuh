@@ -537,6 +537,43 @@ __device__ __forceinline__ void st_global_f2x4(float *p, const f2_t (&f)[4]) {
     asm volatile("st.global.v2.b64 [%0], {%1, %2};" ::"l"(p + 4), "l"(f[2]), "l"(f[3]) : "memory");
 }
 
+// ----------------------------------------------------------------- lane vectors of 8 bf16 columns
+
+__device__ __forceinline__ void vec_unpack(const uint4 &v, f2_t (&f)[4]) { f2_unpack8(v, f); }
+__device__ __forceinline__ void vec_unpack_v(const uint4 &v, f2_t (&f)[4]) { f2_unpack8_v(v, f); }
+__device__ __forceinline__ void vec_pack(const f2_t (&f)[4], uint4 &r) { r = f2_pack8(f); }
+__device__ __forceinline__ void vec_zero(uint4 &r) { r = make_uint4(0, 0, 0, 0); }
+
+// Asynchronous 16-byte copy of one lane vector global -> shared (L2 only), of
+// which the first src_bytes are read and the rest written as zeros
+// (src_bytes = 0: nothing is read; src must still be a valid address);
+// completion through the cp.async groups.  dst is a shared-memory address.
+__device__ __forceinline__ void cp_async_zfill(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void ld_shared_vec(uint32_t addr, uint4 &v) {
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+}
+// Stores that take effect only when pred != 0 (no branch).
+__device__ __forceinline__ void st_global_vec_if(void *p, const uint4 &v, uint32_t pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t@q st.global.v4.u32 [%0], {%1,%2,%3,%4};\n\t}" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(pred)
+                 : "memory");
+}
+__device__ __forceinline__ void st_global_f2_if(float *p, const f2_t (&f)[4], uint32_t pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t@q st.global.v2.b64 [%0], {%1, %2};\n\t}" ::"l"(p),
+                 "l"(f[0]), "l"(f[1]), "r"(pred)
+                 : "memory");
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t@q st.global.v2.b64 [%0], {%1, %2};\n\t}" ::"l"(p + 4),
+                 "l"(f[2]), "l"(f[3]), "r"(pred)
+                 : "memory");
+}
+__device__ __forceinline__ void st_global_f32_if(float *p, float v, uint32_t pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.f32 [%0], %1;\n\t}" ::"l"(p), "f"(v),
+                 "r"(pred)
+                 : "memory");
+}
+
 template <int NC, int LEVELS>
 struct TreeStackF2 {
     f2_t s[LEVELS][NC];
@@ -570,7 +607,56 @@ struct TreeStackF2 {
             }
         }
     }
+
+    // The same as push_static<0> for a run-time index that is uniform across
+    // the warp: a chain of uniform branches, so only the levels that the item
+    // closes are added.
+    __device__ __forceinline__ void push_uniform(f2_t (&v)[NC], int idx) {
+        bool carry = true;
+#pragma unroll
+        for (int l = 0; l < LEVELS; ++l) {
+            if (carry) {
+                if ((idx >> l) & 1) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) v[c] = f2_add(s[l][c], v[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) s[l][c] = v[c];
+                    carry = false;
+                }
+            }
+        }
+    }
 };
+
+// The same push for a run-time index uniform across the warp, with the
+// pending partials in shared memory (level l at base + l * stride, NC pairs
+// per lane): only the levels that the item closes are read.
+template <int NC, int LEVELS>
+__device__ __forceinline__ void push_group_subtree(f2_t (&v)[NC], int idx, uint32_t base, uint32_t stride) {
+    bool carry = true;
+#pragma unroll
+    for (int l = 0; l < LEVELS; ++l) {
+        if (carry) {
+            const uint32_t a = base + l * stride;
+            if ((idx >> l) & 1) {
+#pragma unroll
+                for (int c = 0; c < NC; c += 2) {
+                    f2_t s0, s1;
+                    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(s0), "=l"(s1) : "r"(a + c * 8));
+                    v[c] = f2_add(s0, v[c]);
+                    v[c + 1] = f2_add(s1, v[c + 1]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < NC; c += 2)
+                    asm volatile("st.shared.v2.b64 [%0], {%1, %2};" ::"r"(a + c * 8), "l"(v[c]), "l"(v[c + 1])
+                                 : "memory");
+                carry = false;
+            }
+        }
+    }
+}
 
 // ----------------------------------------------------------------- row sums
 //

@@ -8,11 +8,12 @@
 //    transaction counts), stats warps publish each row's rstd and mean, and
 //    column warps write y or dx and reduce the dweight leaves.
 //
-//  * small_row_kernel (hidden <= 256): a team is P2 = next_pow2(hidden/8)
-//    lanes of one warp, so a warp works on 32/P2 rows at once; rows reach
-//    each lane's 16-byte pieces through a per-warp shared-memory ring filled
-//    by cp.async ahead of use; the rows of a step are combined across teams
-//    by a butterfly before entering the 64-leaf tree.
+//  * small_row_kernel (hidden <= 256): a team is P = next_pow2(hidden/8)
+//    lanes of one warp (8 columns per lane), so a warp works on 32/P rows at
+//    once; rows reach each lane's 16-byte pieces through a per-warp
+//    shared-memory ring filled by cp.async ahead of use; each team owns
+//    consecutive slots of a unit, so a lane's leaves are reduced in the lane,
+//    and the team subtrees meet once per unit.
 //
 // Work units are either plan items (64 row slots: a whole logical block in
 // logical order, or rows of blocks cut by a call boundary) or, without a
@@ -628,72 +629,133 @@ __device__ __forceinline__ f2_t shfl_xor_f2(f2_t v, int k) {
     return (f2_t(__shfl_xor_sync(kFull, uint32_t(v >> 32), k)) << 32) | __shfl_xor_sync(kFull, uint32_t(v), k);
 }
 
-constexpr int kSmallWarps = 8;                          // warps per CTA
-constexpr int kSmallTable = 64 * 16 + 16;               // one unit's slot table (off, lrow, prow), then its header
+// Launch shape of the small-row kernel (overridable for measurements).
+#ifndef RBI_SMALL_WARPS
+#define RBI_SMALL_WARPS 4                               // warps per CTA
+#endif
+#ifndef RBI_SMALL_DEPTH
+#define RBI_SMALL_DEPTH 2                               // most ring buffers per warp
+#endif
+#ifndef RBI_SMALL_LEAF_U
+#define RBI_SMALL_LEAF_U 4                              // rows per team and group, two-tensor leaf modes
+#endif
+constexpr int kSmallWarps = RBI_SMALL_WARPS;
+constexpr int kSmallTable = 64 * 16 + 16;               // one unit's slot table, then its header
+constexpr int kSmallMinBlocks = 65536 / (128 * 32 * kSmallWarps);   // 128 registers per thread
 
-// Shared memory of one warp of small_row_kernel: two unit tables, then a
-// ring of (D + 1) group buffers of kU warp steps x kT tensors x 512 bytes;
-// three buffers when they fit in 12 KB (two CTAs of eight warps per SM).
-__host__ __device__ constexpr int small_ring_depth(int groups, int group_bytes) {
-    return (groups > 2 && 3 * group_bytes <= 12288) ? 3 : (groups < 2 ? groups : 2);
-}
-__host__ __device__ constexpr int small_warp_bytes(int kU, int kT, int groups) {
-    return 2 * kSmallTable + small_ring_depth(groups, kU * kT * 512) * kU * kT * 512;
-}
+__host__ __device__ constexpr int small_log2(int v) { return v <= 1 ? 0 : 1 + small_log2(v >> 1); }
+__host__ __device__ constexpr int small_min(int a, int b) { return a < b ? a : b; }
 
-// Small hidden sizes: each warp works through its units (64 row slots) in
-// groups of kU warp steps.  The rows of a group are copied into a per-warp
-// shared-memory ring with 16-byte cp.async, D = depth - 1 groups ahead of the
-// group being computed, so the bytes in flight are not bounded by registers.
-// Each lane copies and later reads only its own 16-byte pieces, so the ring
-// needs no barrier; the slot table of a unit (row offset, logical and
-// physical row of each slot) is written once per unit by the warp and read
-// by broadcast.  Per group: (1) row sums of the kU steps, (2) rstd and
-// mean(g*xhat) once per row, (3) outputs and leaves, the group's steps
-// folded into a subtree with static positions.
-template <int MODE, int P2, int U>
-__global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KParams p) {
+// Everything the small-row kernel and its launcher derive from (mode, team
+// lanes P).  A lane holds one 16-byte vector (8 columns) of a row.  Shared
+// memory of one warp: two unit tables, a ring of kDepth group buffers (kU
+// warp steps x kT tensors x 32 lane vectors; never more than one unit's
+// groups ahead, since there are two tables), and in the leaf modes the
+// lane's stack of pending group subtrees (kStackLevels x 32 lanes x 8 FP32).
+// Measured on head_dim 128 (teams of 16 lanes, two rows per warp step): four
+// rows per team and group with two ring buffers beat two rows with three
+// buffers by 19% on the fused backward; 8 columns per lane beat 4 (teams of
+// a whole warp, one row per step) by 12% on the step.
+template <int MODE, int P>
+struct SmallShape {
     using T = ModeTraits<MODE>;
-    constexpr int TPW = 32 / P2;                         // teams (rows) per warp step
-    constexpr int kSteps = kBlockRows / TPW;             // steps per 64-slot unit
-    constexpr int kLogTPW = (TPW == 1) ? 0 : (TPW == 2) ? 1 : (TPW == 4) ? 2 : (TPW == 8) ? 3 : (TPW == 16) ? 4 : 5;
-    constexpr int kU = U < kSteps ? U : kSteps;
-    static_assert(kSteps % kU == 0, "steps per unit must be a multiple of the prefetch depth");
-    constexpr int kLogU = (kU == 1) ? 0 : (kU == 2) ? 1 : (kU == 4) ? 2 : (kU == 8) ? 3 : (kU == 16) ? 4 : 5;
-    constexpr int kGroupLevel = kLogTPW + kLogU;          // tree level of one group of kU steps
-    constexpr int kT = T::kTensors;
-    constexpr int kGroups = kSteps / kU;
-    constexpr int kDepth = small_ring_depth(kGroups, kU * kT * 512);
+    static constexpr int kStepBytes = 32 * 16;           // one tensor of one warp step
+    static constexpr int TPW = 32 / P;                   // row teams per warp
+    static constexpr int kTeamRows = kBlockRows / TPW;   // slots of a unit per team
+    // rows per team in one group (the warp steps whose row sums share one
+    // reduction): fewer for the three-tensor leaf mode (registers)
+    static constexpr int U = T::kLeaves ? (T::kTensors >= 3 ? 2 : RBI_SMALL_LEAF_U) : (T::kTensors >= 2 ? 4 : 8);
+    static constexpr int kU = small_min(U, kTeamRows);
+    static constexpr int kGroups = kTeamRows / kU;
+    static constexpr int kLogGroups = small_log2(kGroups);
+    static constexpr int kT = T::kTensors;
+    static constexpr int kGroupBytes = kU * kT * kStepBytes;
+    static constexpr int kDepth = small_min(small_min(RBI_SMALL_DEPTH, 3 * kGroupBytes <= 12288 ? 3 : 2), kGroups + 1);
+    static constexpr int kStackLevels = T::kLeaves ? kLogGroups : 0;
+    static constexpr int kStackBytes = kStackLevels * 32 * 32;
+    static constexpr int kWarpBytes = 2 * kSmallTable + kDepth * kGroupBytes + kStackBytes;
+};
+
+// Small hidden sizes.  Lane tl of a team holds columns 8tl .. 8tl+7; team t
+// of a warp owns the consecutive slots [t*64/TPW, (t+1)*64/TPW) of each unit
+// (64 row slots), TPW = 32/P teams per warp.  Each warp works through its
+// units in groups of kU warp steps; the rows of a group are copied into a
+// per-warp shared-memory ring with cp.async, D = depth - 1 groups ahead of the
+// group being computed, so the bytes in flight are not bounded by registers.
+// An empty slot, and the columns past the row of the last lanes of a team,
+// are filled with zeros by the copy itself, so every value in the ring is a
+// number.  Each lane copies and later reads only its own pieces, so the ring
+// needs no barrier; the slot table of a unit (byte offset of the row, bytes
+// to copy, logical or physical row) is written once per unit by the warp and
+// read by broadcast.  Per group: (1) row sums of the kU steps, (2) rstd and
+// mean(g*xhat) once per row, (3) outputs and leaves, stored under predicates.
+// A lane's leaves stay in the lane: the group's kU rows form a subtree with
+// static positions, the groups of a team a subtree through a stack of pending
+// partials in shared memory, and at the end of the unit the TPW team subtrees
+// are added across teams (adjacent teams first) into the block partial.
+template <int MODE, int P>
+__global__ void __launch_bounds__(kSmallWarps * 32, kSmallMinBlocks) small_row_kernel(const KParams p) {
+    using Sh = SmallShape<MODE, P>;
+    using T = ModeTraits<MODE>;
+    constexpr int NF = 4;                                // FP32 pairs of a lane vector
+    constexpr int kVB = 16;                              // bytes of a lane vector
+    constexpr int kStepBytes = Sh::kStepBytes;
+    constexpr int TPW = Sh::TPW;
+    constexpr int kLogP = small_log2(P);
+    constexpr int kTeamRows = Sh::kTeamRows;
+    constexpr int kU = Sh::kU;                           // warp steps per group
+    constexpr int kLogU = small_log2(kU);
+    constexpr int kGroups = Sh::kGroups;
+    constexpr int kLogGroups = Sh::kLogGroups;
+    constexpr int kT = Sh::kT;
+    constexpr int kGroupBytes = Sh::kGroupBytes;
+    constexpr int kDepth = Sh::kDepth;
     constexpr int kAhead = kDepth - 1;                   // groups issued ahead of the one computed
-    constexpr int kGroupBytes = kU * kT * 512;
+    static_assert(P * TPW == 32 && kGroups * kU == kTeamRows && (1 << kLogGroups) == kGroups, "small shape");
+    static_assert(kAhead >= 1 && kAhead <= kGroups, "the issue side stays within the next unit");
 
     extern __shared__ __align__(16) uint8_t small_smem[];
     const int lane = threadIdx.x & 31;
-    uint8_t *wbase = small_smem + (threadIdx.x >> 5) * small_warp_bytes(kU, kT, kGroups);
-    uint8_t *ring = wbase + 2 * kSmallTable;
-    const int team = lane / P2, tl = lane % P2;
-    const int H = p.hidden, V = H >> 3;
-    const bool has_vec = tl < V;
+    uint8_t *wbase = small_smem + (threadIdx.x >> 5) * Sh::kWarpBytes;
+    const uint32_t ring_lane = smem_addr(wbase + 2 * kSmallTable) + lane * kVB;   // this lane's piece, slot 0
+    // the lane's stack of pending group subtrees (leaf modes): level l at
+    // stack_lane + l * 32 * 32
+    const uint32_t stack_lane = smem_addr(wbase + 2 * kSmallTable + kDepth * kGroupBytes) + lane * 32;
+    const int team = lane >> kLogP, tl = lane & (P - 1);
+    const int H = p.hidden;
+    const bool has_vec = tl * 8 < H;
+    const int col0 = has_vec ? tl * 8 : 0;              // a lane past the row reads nothing, at column 0
+    const uint32_t vec_mask = has_vec ? ~0u : 0u;
     const float Hf = float(H);
     const float inv_h = row_inv_h(H);
     const int64_t gwarp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const int64_t my_units = p.n_units > gwarp ? (p.n_units - gwarp + nwarps - 1) / nwarps : 0;
-    const int64_t total = my_units * kGroups;
+    // this lane's columns of row 0 of each tensor; a row adds its byte offset
+    const uint8_t *gx = reinterpret_cast<const uint8_t *>(p.x + col0);
+    const uint8_t *gdy = reinterpret_cast<const uint8_t *>(T::kNeedDy ? p.dy + col0 : p.x);
+    const uint8_t *gres = reinterpret_cast<const uint8_t *>(T::kRes ? p.res + col0 : p.x);
+    uint8_t *gout = reinterpret_cast<uint8_t *>(p.out + col0);
+    const uint32_t out_mask = (T::kWritesOut && p.out != nullptr) ? vec_mask : 0u;
 
-    f2_t wv[4] = {0ull, 0ull, 0ull, 0ull};
-    if (MODE != kDw && has_vec) f2_unpack8(*reinterpret_cast<const uint4 *>(p.w + tl * 8), wv);
+    f2_t wv[NF];
+#pragma unroll
+    for (int i = 0; i < NF; ++i) wv[i] = 0ull;
+    if (MODE != kDw && has_vec) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(p.w + col0);
+        vec_unpack(w, wv);
+    }
 
-    // unit tables: entry = (row offset + tl * 8 of the lane's columns is added
-    // by the reader; -1 = inactive), logical row, physical row; plus the item
-    // header (kind, block) after the 64 entries
+    // unit tables: per slot the byte offset of the row (0 when empty), the
+    // bytes a lane copies (kVB, or 0 when empty), and the logical row (leaf
+    // modes) or the physical row (forward modes); the item header (kind,
+    // block) after the 64 entries
     struct SlotEntry {
-        int64_t off;
-        int32_t lrow, prow;
+        int64_t boff;
+        int32_t row;
+        uint32_t nb;
     };
     auto table = [&](int64_t ord) { return reinterpret_cast<SlotEntry *>(wbase + int(ord & 1) * kSmallTable); };
-    int2 hdr_next = make_int2(0, -1);
-    int2 pr_next = make_int2(-1, -1), lr_next = make_int2(-1, -1);
     // slot metadata of unit `ord` (lane l: slots 2l, 2l+1) into registers
     auto fetch_unit = [&](int64_t ord, int2 &pr2, int2 &lr2, int2 &hd) {
         pr2 = make_int2(-1, -1);
@@ -712,23 +774,18 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
             if (r0 + 1 < p.n_rows && p.tok_id[(r0 + 1) / p.rpt] >= 0) pr2.y = int32_t(r0 + 1);
         }
     };
-    int64_t issue_ord = -1;
-    auto issue = [&](int64_t gi) {
-        if (gi < total) {
-            const int64_t ord = gi / kGroups;
-            const int gg = int(gi % kGroups);
-            if (ord != issue_ord) {                      // entering a unit: its table, the next one's metadata
-                int2 pr2, lr2, hd;
-                if (ord == issue_ord + 1 && issue_ord >= 0) {
-                    pr2 = pr_next;
-                    lr2 = lr_next;
-                    hd = hdr_next;
-                } else {
-                    fetch_unit(ord, pr2, lr2, hd);
-                }
+    int2 pr_next, lr_next, hdr_next;
+    fetch_unit(0, pr_next, lr_next, hdr_next);
+
+    // the issue side walks the groups in order: unit i_ord, group i_g, ring slot i_slot
+    int64_t i_ord = 0;
+    int i_g = 0, i_slot = 0;
+    auto issue_next = [&]() {
+        if (i_ord < my_units) {
+            if (i_g == 0) {                              // entering a unit: its table, the next one's metadata
                 __syncwarp();                            // readers of the table being replaced are done
-                SlotEntry *tb = table(ord);
-                int32_t prs[2] = {pr2.x, pr2.y}, lrs[2] = {lr2.x, lr2.y};
+                SlotEntry *tb = table(i_ord);
+                const int32_t prs[2] = {pr_next.x, pr_next.y}, lrs[2] = {lr_next.x, lr_next.y};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int32_t pr = prs[h], lr = lrs[h];
@@ -738,49 +795,44 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                         act = false;
                     }
                     SlotEntry e;
-                    e.off = act ? row_offset(p, pr) : -1;
-                    e.lrow = lr;
-                    e.prow = pr;
+                    e.boff = act ? row_offset(p, pr) * 2 : 0;
+                    e.row = T::kLeaves ? lr : pr;
+                    e.nb = act ? uint32_t(kVB) : 0u;
                     tb[2 * lane + h] = e;
                 }
-                if (lane == 0) *reinterpret_cast<int2 *>(reinterpret_cast<uint8_t *>(tb) + 64 * 16) = hd;
-                issue_ord = ord;
-                fetch_unit(ord + 1, pr_next, lr_next, hdr_next);
+                if (lane == 0) *reinterpret_cast<int2 *>(reinterpret_cast<uint8_t *>(tb) + 64 * 16) = hdr_next;
+                fetch_unit(i_ord + 1, pr_next, lr_next, hdr_next);
                 __syncwarp();
             }
-            const SlotEntry *tb = table(ord);
-            uint8_t *buf = ring + int(gi % kDepth) * kGroupBytes;
+            const SlotEntry *tb = table(i_ord) + team * kTeamRows + i_g * kU;
+            const uint32_t dst = ring_lane + i_slot * kGroupBytes;
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
-                const int slot = (gg * kU + q) * TPW + team;
-                const int64_t off = tb[slot].off;
-                if (off >= 0 && has_vec) {
-                    cp_async_16(buf + (q * kT + 0) * 512 + lane * 16, p.x + off + tl * 8);
-                    if (T::kNeedDy) cp_async_16(buf + (q * kT + 1) * 512 + lane * 16, p.dy + off + tl * 8);
-                    if (T::kRes) cp_async_16(buf + (q * kT + T::kResSlot) * 512 + lane * 16, p.res + off + tl * 8);
-                }
+                const SlotEntry e = tb[q];
+                const uint32_t nb = e.nb & vec_mask;
+                cp_async_zfill(dst + (q * kT + 0) * kStepBytes, gx + e.boff, nb);
+                if (T::kNeedDy) cp_async_zfill(dst + (q * kT + 1) * kStepBytes, gdy + e.boff, nb);
+                if (T::kRes) cp_async_zfill(dst + (q * kT + T::kResSlot) * kStepBytes, gres + e.boff, nb);
             }
+            if (++i_g == kGroups) {
+                i_g = 0;
+                ++i_ord;
+            }
+            if (++i_slot == kDepth) i_slot = 0;
         }
         cp_async_commit();
     };
 
-    for (int a = 0; a < kAhead; ++a) issue(a);
-    TreeStackF2<4, kBlockLevels> tree;                // levels kGroupLevel.. of the 64-leaf tree
-    int32_t kind = 0, block = -1;
+#pragma unroll
+    for (int a = 0; a < kAhead; ++a) issue_next();
+    int c_slot = 0;
 #pragma unroll 1
-    for (int64_t gi = 0; gi < total; ++gi) {
-        __syncwarp();                                // every lane is done with the buffer reused next
-        issue(gi + kAhead);
-        cp_async_wait<kAhead>();                     // this lane's copies of group gi have landed
-        const int64_t ord = gi / kGroups;
-        const int st0 = int(gi % kGroups) * kU;
-        const SlotEntry *tb = table(ord);
-        const uint8_t *buf = ring + int(gi % kDepth) * kGroupBytes;
-        if (st0 == 0) {
-            // the header of the unit being computed: the issue side may have
-            // moved on to the next unit already (D < kGroups), so it is kept
-            // with the table
-            const int2 hd = *reinterpret_cast<const int2 *>(reinterpret_cast<const uint8_t *>(tb) + 64 * 16);
+    for (int64_t ord = 0; ord < my_units; ++ord) {
+        // the unit's header is kept with its table: the issue side may have
+        // moved on to the next unit already
+        int32_t kind, block;
+        {
+            const int2 hd = *reinterpret_cast<const int2 *>(reinterpret_cast<const uint8_t *>(table(ord)) + 64 * 16);
             // quarter items (kind 2) are spilled row by row here: a unit of this
             // kernel is a whole block, and the finalize rebuilds those quarters
             kind = hd.x & 0xff;
@@ -792,65 +844,71 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                 kind = kBadItem;                           // malformed item: contributes nothing
             }
         }
-        {
-            int64_t off[kU];
-            int32_t lrow[kU], prow[kU];
+        // whole: the leaves enter the tree; spill_mask: they are spilled (the
+        // stores are predicated on it, so no row branches on the kind)
+        const bool whole = T::kLeaves && kind == kItemWhole;
+        const uint32_t spill_mask = (T::kLeaves && kind == kItemSpill) ? vec_mask : 0u;
+        f2_t node[NF];                                     // the last group's subtree, then the team's
+#pragma unroll
+        for (int i = 0; i < NF; ++i) node[i] = 0ull;
+#pragma unroll 1
+        for (int g = 0; g < kGroups; ++g) {
+            __syncwarp();                                  // every lane is done with the buffer reused next
+            issue_next();
+            cp_async_wait<kAhead>();                       // this lane's copies of this group have landed
+            const SlotEntry *tb = table(ord) + team * kTeamRows + g * kU;
+            const uint32_t src = ring_lane + c_slot * kGroupBytes;
+            if (++c_slot == kDepth) c_slot = 0;
+
             uint4 xv[kU], dv[kU];
             constexpr bool kDres = T::kRes && T::kNeedDy;           // dres streamed (kAddDx*)
             constexpr int kRv = kDres ? kU : 1;                     // its registers
             uint4 rv[kRv];
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
-                const SlotEntry e = tb[(st0 + q) * TPW + team];
-                off[q] = e.off >= 0 ? e.off + tl * 8 : -1;
-                lrow[q] = e.lrow;
-                prow[q] = e.prow;
-                xv[q] = make_uint4(0, 0, 0, 0);
-                dv[q] = make_uint4(0, 0, 0, 0);
-                if (kDres) rv[q % kRv] = make_uint4(0, 0, 0, 0);
-                if (e.off >= 0 && has_vec) {
-                    xv[q] = ld_shared_v4(buf + (q * kT + 0) * 512 + lane * 16);
-                    if (T::kNeedDy || MODE == kAddFwd) dv[q] = ld_shared_v4(buf + (q * kT + 1) * 512 + lane * 16);
-                    if (kDres) rv[q % kRv] = ld_shared_v4(buf + (q * kT + T::kResSlot) * 512 + lane * 16);
-                }
+                ld_shared_vec(src + (q * kT + 0) * kStepBytes, xv[q]);
+                if (T::kNeedDy || MODE == kAddFwd) ld_shared_vec(src + (q * kT + 1) * kStepBytes, dv[q]);
+                else vec_zero(dv[q]);
+                if (kDres) ld_shared_vec(src + (q * kT + T::kResSlot) * kStepBytes, rv[q % kRv]);
             }
             // phase 1: the lane partials of every row sum of the group (two FMA
-            // chains per 8-column vector); values 0..kU-1 are the sums of squares
-            // of the kU steps, kU..2kU-1 the sums of g*x
+            // chains per lane vector, even and odd columns, then added); values
+            // 0..kU-1 are the sums of squares of the kU steps, kU..2kU-1 the
+            // sums of g*x
             constexpr int kNV = kU * (T::kNeedGx ? 2 : 1);
-            constexpr int kLogNV = (kNV == 1) ? 0 : (kNV == 2) ? 1 : (kNV == 4) ? 2 : (kNV == 8) ? 3 : (kNV == 16) ? 4 : 5;
-            constexpr int kLogP2 = 5 - kLogTPW;
-            constexpr int kHalvings = kLogNV < kLogP2 ? kLogNV : kLogP2;
+            constexpr int kLogNV = small_log2(kNV);
+            constexpr int kHalvings = kLogNV < kLogP ? kLogNV : kLogP;
             constexpr int kCnt = kNV >> kHalvings;       // values a lane holds after the reduction
             float vals[kNV];
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
-                f2_t xf[4], df[4];
-                f2_unpack8(xv[q], xf);
-                f2_unpack8(dv[q], df);
+                f2_t xf[NF], df[NF];
+                vec_unpack(xv[q], xf);
+                vec_unpack(dv[q], df);
                 if (MODE == kAddFwd) {                              // the row is h = bf16(x + r)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) xf[i] = f2_add(xf[i], df[i]);
-                    xv[q] = f2_pack8(xf);                            // h replaces x from here on
-                    f2_unpack8(xv[q], xf);
+                    for (int i = 0; i < NF; ++i) xf[i] = f2_add(xf[i], df[i]);
+                    vec_pack(xf, xv[q]);                             // h replaces x from here on
+                    vec_unpack(xv[q], xf);
                 }
-                f2_t a2 = 0ull, b2 = 0ull;
+                f2_t a2 = f2_mul(xf[0], xf[0]);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) a2 = f2_fma(xf[i], xf[i], a2);
+                for (int i = 1; i < NF; ++i) a2 = f2_fma(xf[i], xf[i], a2);
                 vals[q] = __fadd_rn(f2_lo(a2), f2_hi(a2));
                 if (T::kNeedGx) {
+                    f2_t b2 = f2_mul(f2_mul(df[0], wv[0]), xf[0]);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) b2 = f2_fma(f2_mul(df[i], wv[i]), xf[i], b2);
+                    for (int i = 1; i < NF; ++i) b2 = f2_fma(f2_mul(df[i], wv[i]), xf[i], b2);
                     vals[kU + q] = __fadd_rn(f2_lo(b2), f2_hi(b2));
                 }
             }
-            // the team tree over the P2 lanes (lanes 1 apart first, then 2, 4, ...)
+            // the team tree over the P lanes (lanes 1 apart first, then 2, 4, ...)
             // as a transposing reduction: at distance d a lane keeps half of its
             // values and adds its partner's copy of them, so every value is still
             // the sum over the same lane pairs (addition is commutative) but the
-            // kNV trees cost kNV - 1 exchanges instead of kNV * log2(P2)
+            // kNV trees cost kNV - 1 exchanges instead of kNV * log2(P)
 #pragma unroll
-            for (int lv = 0; lv < kLogP2; ++lv) {
+            for (int lv = 0; lv < kLogP; ++lv) {
                 const int d = 1 << lv;
                 if (lv < kHalvings) {
                     constexpr int kMaxHalf = kNV / 2;
@@ -875,7 +933,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                 int l = 0;
 #pragma unroll
                 for (int lv = 0; lv < kHalvings; ++lv) l |= ((idx >> (kLogNV - 1 - lv)) & 1) << lv;
-                return team * P2 + l;
+                return team * P + l;
             };
             // phase 2: rstd and mean(g*xhat), once per row: each lane evaluates the
             // values it holds; a lane holding g*x of step q takes rstd of step q
@@ -892,86 +950,81 @@ __global__ void __launch_bounds__(kSmallWarps * 32, 2) small_row_kernel(const KP
                     mloc[jj] = row_mean_gxhat(vals[jj], rs_q, Hf, inv_h);
                 }
             }
-            float rsv[kU], mgv[kU];
+            // phase 3: outputs and leaves.  An empty slot holds zeros; its rstd is
+            // taken as 0, so its leaf is exactly +0 (the tree of a whole block adds
+            // +0 for ids past the last row) whatever eps is.  The group's rows form
+            // a complete subtree with static positions (sub: its pending partials)
+            TreeStackF2<NF, (kLogU > 0 ? kLogU : 1)> sub;
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
-                const int jr = q & (kCnt - 1);
-                rsv[q] = __shfl_sync(kFull, rloc[jr], holder(q));
-                mgv[q] = 0.f;
-                if (T::kNeedGx) {
-                    const int jg = (kU + q) & (kCnt - 1);
-                    mgv[q] = __shfl_sync(kFull, mloc[jg], holder(kU + q));
-                }
-            }
-            // phase 3: outputs and leaves; the group's steps form a subtree of the
-            // 64-leaf tree with static positions, pushed once per group
-            TreeStackF2<4, (kLogU > 0 ? kLogU : 1)> mini;
-            f2_t node[4] = {0ull, 0ull, 0ull, 0ull};
+                const SlotEntry e = tb[q];
+                const uint32_t act = e.nb;
+                const float rs_row = __shfl_sync(kFull, rloc[q & (kCnt - 1)], holder(q));   // every lane
+                const float rstd = act ? rs_row : 0.f;
+                const f2_t r2 = f2_make(rstd, rstd);
+                f2_t xf[NF], xh[NF], o[NF];
+                vec_unpack_v(xv[q], xf);
 #pragma unroll
-            for (int q = 0; q < kU; ++q) {
-                const bool act = off[q] >= 0;
-                const float rstd = rsv[q];
-                f2_t leaf[4] = {0ull, 0ull, 0ull, 0ull};
-                if (act && has_vec) {
-                    const f2_t r2 = f2_make(rstd, rstd);
-                    f2_t xf[4], xh[4], o[4];
-                    f2_unpack8_v(xv[q], xf);
+                for (int i = 0; i < NF; ++i) xh[i] = f2_mul(xf[i], r2);
+                if (T::kFwdLike) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) xh[i] = f2_mul(xf[i], r2);
-                    if (T::kFwdLike) {
+                    for (int i = 0; i < NF; ++i) o[i] = f2_mul(xh[i], wv[i]);
+                    uint4 ov;
+                    vec_pack(o, ov);
+                    st_global_vec_if(gout + e.boff, ov, act & out_mask);
+                    if (MODE == kAddFwd)
+                        st_global_vec_if(reinterpret_cast<uint8_t *>(p.out2 + col0) + e.boff, xv[q], act & vec_mask);
+                    if (p.rstd_out != nullptr) st_global_f32_if(p.rstd_out + e.row, rstd, act && tl == 0);
+                } else {
+                    f2_t df[NF];
+                    vec_unpack_v(dv[q], df);
+                    if (T::kNeedGx) {
+                        const float mg = __shfl_sync(kFull, mloc[(kU + q) & (kCnt - 1)], holder(kU + q));
+                        const f2_t nm2 = f2_make(-mg, -mg);
+                        const float rs = __fmul_rn(rstd, p.grad_scale);    // == rstd when unscaled
+                        const f2_t rs2 = f2_make(rs, rs);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) o[i] = f2_mul(xh[i], wv[i]);
-                        st_global_v4(p.out + off[q], f2_pack8(o));
-                        if (MODE == kAddFwd) st_global_v4(p.out2 + off[q], xv[q]);
-                    } else {
-                        f2_t df[4];
-                        f2_unpack8_v(dv[q], df);
-                        if (T::kNeedGx && p.out != nullptr) {
-                            const f2_t nm2 = f2_make(-mgv[q], -mgv[q]);
-                            const float rs = __fmul_rn(rstd, p.grad_scale);    // == rstd when unscaled
-                            const f2_t rs2 = f2_make(rs, rs);
+                        for (int i = 0; i < NF; ++i) o[i] = f2_mul(rs2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
+                        if (kDres) {
+                            f2_t rf[NF];
+                            vec_unpack_v(rv[q % kRv], rf);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) o[i] = f2_mul(rs2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
-                            if (kDres) {
-                                f2_t rf[4];
-                                f2_unpack8_v(rv[q % kRv], rf);
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) o[i] = f2_add(o[i], rf[i]);
-                            }
-                            st_global_v4(p.out + off[q], f2_pack8(o));
+                            for (int i = 0; i < NF; ++i) o[i] = f2_add(o[i], rf[i]);
                         }
-                        if (T::kLeaves) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) leaf[i] = f2_mul(df[i], xh[i]);
-                        }
+                        uint4 ov;
+                        vec_pack(o, ov);
+                        st_global_vec_if(gout + e.boff, ov, act & out_mask);
                     }
-                }
-                if (T::kFwdLike && act && p.rstd_out != nullptr && tl == 0) p.rstd_out[prow[q]] = rstd;
-                if (T::kLeaves) {
-                    if (kind == 0) {
-                        // the TPW rows of this step: adjacent teams first
+                    if (T::kLeaves) {
+                        f2_t leaf[NF];
 #pragma unroll
-                        for (int kk = P2; kk < 32; kk <<= 1)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) leaf[i] = f2_add(leaf[i], shfl_xor_f2(leaf[i], kk));
-                        if (kLogU > 0) mini.template push_static<0>(leaf, q);
+                        for (int i = 0; i < NF; ++i) leaf[i] = f2_mul(df[i], xh[i]);
+                        st_global_f2_if(p.ws.spill + int64_t(e.row) * H + col0, leaf, act ? spill_mask : 0u);
+                        if (kLogU > 0) sub.template push_static<0>(leaf, q);
                         if (q == kU - 1) {
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) node[i] = leaf[i];   // the group's subtree
+                            for (int i = 0; i < NF; ++i) node[i] = leaf[i];   // the group's subtree
                         }
-                    } else if (kind == 1 && act) {
-                        if (has_vec) st_global_f2x4(p.ws.spill + int64_t(lrow[q]) * H + tl * 8, leaf);
-                        if (tl == 0) mark_spilled_row(p.ws, lrow[q]);
                     }
                 }
             }
-            if (T::kLeaves && kind == 0) {
-                if (kGroupLevel < kBlockLevels) tree.template push_dyn<kGroupLevel>(node, st0 / kU);
-                if (st0 + kU == kSteps) {                    // node is the block partial
-                    if (team == 0 && has_vec) st_global_f2x4(p.ws.block_partial + int64_t(block) * 4 * H + tl * 8, node);
-                    if (lane == 0) mark_whole_block(p.ws, block);
+            if (spill_mask != 0 && tl == 0) {                // the spilled rows' flags
+#pragma unroll
+                for (int q = 0; q < kU; ++q) {
+                    const SlotEntry e = tb[q];
+                    if (e.nb) mark_spilled_row(p.ws, e.row);
                 }
             }
+            if (whole && kLogGroups > 0) push_group_subtree<NF, kLogGroups>(node, g, stack_lane, 32 * 32);
+        }
+        if (whole) {
+            // node is the team's subtree; the TPW subtrees, adjacent teams first
+#pragma unroll
+            for (int kk = P; kk < 32; kk <<= 1)
+#pragma unroll
+                for (int i = 0; i < NF; ++i) node[i] = f2_add(node[i], shfl_xor_f2(node[i], kk));
+            if (team == 0) st_global_f2_if(p.ws.block_partial + int64_t(block) * 4 * H + col0, node, vec_mask);
+            if (lane == 0) mark_whole_block(p.ws, block);
         }
     }
     cp_async_wait<0>();
