@@ -80,7 +80,9 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
 // The stats-warp count: a K-CTA team (K > 1) exchanges row partials through
 // distributed shared memory, and a stats warp waits for its peers on every
 // stage, so more stats warps keep more stages' exchanges in flight (measured
-// on hidden 8192: forward best with 3, backward with 6; a single CTA keeps 2).
+// on hidden 8192: forward best with 3, backward with 6).  A single CTA keeps
+// 2 for the forward and takes 3 for the backward when they fit in 640
+// threads (hidden 4096: backward 0.73 -> 0.75 of the peak, step -3%).
 // Bounded by the 23 warps of the widest launch.  Thread counts up to 640 get
 // the 96-register budget, wider ones 80.
 template <int MODE, int R, int K, int NS>
@@ -91,8 +93,10 @@ int launch_split_ns(const KParams &p, const Shape &sh, const DeviceInfo &d, cuda
 
 template <int MODE, int R, int K>
 int launch_split_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
-    constexpr int kWant = K == 1 ? kSplitStatsWarps : (ModeTraits<MODE>::kFwdLike ? 3 : 6);
-    if (kWant > kSplitStatsWarps && sh.nc + kWant + 1 <= 736 / 32)
+    constexpr int kWant = K == 1 ? (ModeTraits<MODE>::kFwdLike ? kSplitStatsWarps : 3)
+                                 : (ModeTraits<MODE>::kFwdLike ? 3 : 6);
+    constexpr int kMaxWarps = K == 1 ? 640 / 32 : 736 / 32;
+    if (kWant > kSplitStatsWarps && sh.nc + kWant + 1 <= kMaxWarps)
         return launch_split_ns<MODE, R, K, kWant>(p, sh, d, stream);
     return launch_split_ns<MODE, R, K, kSplitStatsWarps>(p, sh, d, stream);
 }

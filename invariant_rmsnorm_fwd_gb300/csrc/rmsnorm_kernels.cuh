@@ -402,37 +402,52 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                 break;
             }
             const StageMeta *m = meta + s * R;
+            // The R rows of the stage are folded in one pass over the slice: each
+            // row keeps its own two chains (the canonical order), so the rows'
+            // chains are independent and run side by side, and a weight vector
+            // is read once for all of them.  A row the stage does not hold is
+            // folded too (its buffer holds stale bytes) and its sums are dropped.
+            f2_t a2[R], b2[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) a2[r] = b2[r] = 0ull;   // +0.0 in both lanes
+#pragma unroll 2
+            for (int v = lane; v < VS; v += 32) {
+                f2_t wf[4];
+                if (T::kNeedGx) {
+                    const float4 w0 = *reinterpret_cast<const float4 *>(wsm + v * 8);
+                    const float4 w1 = *reinterpret_cast<const float4 *>(wsm + v * 8 + 4);
+                    wf[0] = f2_make(w0.x, w0.y);
+                    wf[1] = f2_make(w0.z, w0.w);
+                    wf[2] = f2_make(w1.x, w1.y);
+                    wf[3] = f2_make(w1.z, w1.w);
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    f2_t xf[4];
+                    f2_unpack8(ld_shared_v4(stage_ptr(s, 0, r) + v * 16), xf);
+                    if (MODE == kAddFwd) {                  // the row is h = bf16(x + r)
+                        f2_t rf[4];
+                        f2_unpack8(ld_shared_v4(stage_ptr(s, T::kResSlot, r) + v * 16), rf);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) xf[i] = f2_add(xf[i], rf[i]);
+                        f2_unpack8(f2_pack8(xf), xf);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) a2[r] = f2_fma(xf[i], xf[i], a2[r]);
+                    if (T::kNeedGx) {
+                        f2_t df[4];
+                        f2_unpack8(ld_shared_v4(stage_ptr(s, 1, r) + v * 16), df);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) b2[r] = f2_fma(f2_mul(df[i], wf[i]), xf[i], b2[r]);
+                    }
+                }
+            }
             float vals[2 * R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                f2_t a2 = 0ull, b2 = 0ull;                      // +0.0 in both lanes
-                if (m[r].off >= 0) {
-                    const uint8_t *xr = stage_ptr(s, 0, r);
-                    const uint8_t *dr = stage_ptr(s, 1, r);
-#pragma unroll 4
-                    for (int v = lane; v < VS; v += 32) {
-                        f2_t xf[4];
-                        f2_unpack8(ld_shared_v4(xr + v * 16), xf);
-                        if (MODE == kAddFwd) {                  // the row is h = bf16(x + r)
-                            f2_t rf[4];
-                            f2_unpack8(ld_shared_v4(stage_ptr(s, T::kResSlot, r) + v * 16), rf);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) xf[i] = f2_add(xf[i], rf[i]);
-                            f2_unpack8(f2_pack8(xf), xf);
-                        }
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) a2 = f2_fma(xf[i], xf[i], a2);
-                        if (T::kNeedGx) {
-                            f2_t df[4];
-                            f2_unpack8(ld_shared_v4(dr + v * 16), df);
-                            const f2_t *wf = reinterpret_cast<const f2_t *>(wsm + v * 8);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) b2 = f2_fma(f2_mul(df[i], wf[i]), xf[i], b2);
-                        }
-                    }
-                }
-                vals[r] = __fadd_rn(f2_lo(a2), f2_hi(a2));
-                vals[R + r] = __fadd_rn(f2_lo(b2), f2_hi(b2));
+                const bool held = m[r].off >= 0;
+                vals[r] = held ? __fadd_rn(f2_lo(a2[r]), f2_hi(a2[r])) : 0.f;
+                vals[R + r] = held ? __fadd_rn(f2_lo(b2[r]), f2_hi(b2[r])) : 0.f;
             }
             // complete tree over the 32 lanes, pairing 16 apart first
 #pragma unroll
