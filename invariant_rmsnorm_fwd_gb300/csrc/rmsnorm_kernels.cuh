@@ -321,7 +321,15 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     // them after the barrier, so the producer's first copies are not held up by
     // these loads.
     if (T::kNeedGx && warp >= NC && warp < NC + NS) {
-        for (int i = tid - NC * 32; i < HS; i += NS * 32) wsm[i] = __uint_as_float(uint32_t(p.w[col0 + i]) << 16);
+        // 16-byte loads (8 weights each), so that a CTA's start does not wait
+        // for a chain of 2-byte loads
+        for (int i = tid - NC * 32; i < VS; i += NS * 32) {
+            f2_t wf[4];
+            f2_unpack8(*reinterpret_cast<const uint4 *>(p.w + col0 + int64_t(i) * 8), wf);
+            uint4 *dst = reinterpret_cast<uint4 *>(wsm + i * 8);
+            dst[0] = make_uint4(uint32_t(wf[0]), uint32_t(wf[0] >> 32), uint32_t(wf[1]), uint32_t(wf[1] >> 32));
+            dst[1] = make_uint4(uint32_t(wf[2]), uint32_t(wf[2] >> 32), uint32_t(wf[3]), uint32_t(wf[3] >> 32));
+        }
         asm volatile("bar.sync 1, %0;" ::"r"(NS * 32) : "memory");
     }
 
