@@ -98,7 +98,6 @@ int launch_split_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
     constexpr int kMaxWarps = K == 1 ? 640 / 32 : 736 / 32;
     if (kWant > kSplitStatsWarps && sh.nc + kWant + 1 <= kMaxWarps)
         return launch_split_ns<MODE, R, K, kWant>(p, sh, d, stream);
-
     return launch_split_ns<MODE, R, K, kSplitStatsWarps>(p, sh, d, stream);
 }
 
