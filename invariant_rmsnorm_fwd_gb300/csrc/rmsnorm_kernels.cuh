@@ -520,6 +520,8 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
         const float gscale = p.grad_scale;
         TreeStackF2<4, 4> tree;            // levels log2(R)..3 of the 16-leaf unit
         int32_t kind = 0, block = -1, quarter = 0, qmask = 0;
+        bool keep = false, spill_unit = false;           // of the current unit
+        const uint32_t vec_mask = has_vec ? ~0u : 0u;
         int s = 0;
         uint32_t parity = 0;
         int64_t u = cluster_id;                               // current quarter unit
@@ -556,6 +558,9 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     if (t == 0 && rank == 0) set_status(p.ws.hdr, kStPlan);
                     kind = kBadItem;
                 }
+                // a quarter of a kind-2 item that the call does not hold is skipped
+                keep = kind == kItemWhole || (kind == kItemQuarters && ((qmask >> quarter) & 1));
+                spill_unit = kind == kItemSpill;
             }
             const StageMeta *m = meta + s * R;
             TreeStackF2<4, (kLogR > 0 ? kLogR : 1)> mini;
@@ -608,28 +613,29 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     }
                 }
                 if (T::kLeaves) {
-                    if (kind == kItemWhole || kind == kItemQuarters) {
-                        // a quarter of a kind-2 item that the call does not hold is skipped
-                        const bool keep = kind == kItemWhole || ((qmask >> quarter) & 1);
-                        if (R > 1) mini.template push_static<0>(leaf, r);
-                        if (r == R - 1) {
-                            tree.template push_static<kLogR>(leaf, sub);
-                            if (sub == kUnitBatches - 1 && keep) {   // leaf[] is the quarter partial
-                                if (has_vec)
-                                    st_global_f2x4(p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + my_col, leaf);
-                                if (t == 0 && rank == 0) mark_quarter(p.ws, block, quarter);
-                            } else if (half_unit && sub == kUnitBatches / 2 - 1 && keep) {   // the eighth partial
-                                const int half = int(cluster_id & 1);
-                                float *dst = half ? p.ws.eighth : p.ws.block_partial;
-                                if (has_vec) st_global_f2x4(dst + (int64_t(block) * 4 + quarter) * H + my_col, leaf);
-                                if (t == 0 && rank == 0) mark_eighth(p.ws, block, quarter, half);
-                            }
+                    // the tree runs for every unit (a quarter or eighth partial is
+                    // stored only for a kept quarter of a block)
+                    if (spill_unit && act && has_vec) st_global_f2x4(p.ws.spill + int64_t(m[r].lrow) * H + my_col, leaf);
+                    if (R > 1) mini.template push_static<0>(leaf, r);
+                    if (r == R - 1) {
+                        tree.template push_static<kLogR>(leaf, sub);
+                        if (sub == kUnitBatches - 1) {               // leaf[] is the quarter partial
+                            st_global_f2_if(p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + my_col, leaf,
+                                            keep ? vec_mask : 0u);
+                            if (keep && t == 0 && rank == 0) mark_quarter(p.ws, block, quarter);
+                        } else if (half_unit && sub == kUnitBatches / 2 - 1) {   // the eighth partial
+                            const int half = int(cluster_id & 1);
+                            float *dst = half ? p.ws.eighth : p.ws.block_partial;
+                            st_global_f2_if(dst + (int64_t(block) * 4 + quarter) * H + my_col, leaf, keep ? vec_mask : 0u);
+                            if (keep && t == 0 && rank == 0) mark_eighth(p.ws, block, quarter, half);
                         }
-                    } else if (kind == kItemSpill && act) {
-                        if (has_vec) st_global_f2x4(p.ws.spill + int64_t(m[r].lrow) * H + my_col, leaf);
-                        if (t == 0 && rank == 0) mark_spilled_row(p.ws, m[r].lrow);
                     }
                 }
+            }
+            if (T::kLeaves && spill_unit && t == 0 && rank == 0) {   // the spilled rows' flags
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (m[r].off >= 0) mark_spilled_row(p.ws, m[r].lrow);
             }
             __syncwarp();
 #ifndef RBI_TEST_WITHHOLD_EMPTY
