@@ -268,6 +268,16 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t *bar, uint32_
     }
 }
 
+// Asynchronous store of two floats to shared::cluster address `addr` (another
+// CTA's shared memory, or this CTA's); its completion decrements the
+// transaction count of the mbarrier at shared::cluster address `bar` (in the
+// same CTA as `addr`) by 8 bytes.
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+                 "f"(a), "f"(b), "r"(bar)
+                 : "memory");
+}
+
 // Arrive on the mbarrier at shared::cluster address `addr` (possibly another
 // CTA's), releasing this thread's earlier shared-memory stores at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
@@ -286,9 +296,6 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
-}
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;

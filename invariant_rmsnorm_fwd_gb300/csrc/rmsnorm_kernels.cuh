@@ -170,8 +170,9 @@ constexpr int kMaxBatch = 8;                     // rows per pipeline stage <= 8
 // stats[s] when the stats warp has published rstd and mean(g*xhat) of its
 // rows, empty[s] when every column warp is done with it.  With K > 1 the
 // stats warps exchange their slice partials through distributed shared
-// memory: each stores its partials into every CTA of the cluster and arrives
-// on that CTA's xchg[s] barrier, then waits for all K arrivals on its own.
+// memory: each sends its partials to every CTA of the cluster with st.async,
+// counted in bytes on that CTA's exchange barrier of the stage, then waits
+// for all K slices on its own.
 // No CTA-wide barrier is used after set-up.  Rows of the dweight modes are
 // processed in 16-row units (a quarter of a logical block): the column warps
 // reduce the unit's 16 leaves with the 64-leaf tree's lower four levels and
@@ -194,9 +195,9 @@ struct SplitStats {
     float mg;
 };
 
-constexpr int kSplitFlagOff = 384;                                   // after 4 x 12 barriers (384 B)
-constexpr int kSplitItemOff = 400;                                   // [kSplitMaxStages] int2 item headers
-constexpr int kSplitMetaOff = 512;
+constexpr int kSplitFlagOff = 480;                                   // after 5 x 12 barriers (480 B)
+constexpr int kSplitItemOff = 496;                                   // [kSplitMaxStages] int2 item headers
+constexpr int kSplitMetaOff = 608;
 constexpr int kSplitStatsOff = kSplitMetaOff + kSplitMaxStages * kMaxBatch * 16;
 constexpr int kSplitXbufOff = kSplitStatsOff + kSplitMaxStages * kMaxBatch * 8;   // [S][2][K][R] float2
 constexpr int kSplitWOff = kSplitXbufOff + kSplitMaxStages * 2 * kSplitMaxK * kMaxBatch * 8;
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *stats_bar = full + kSplitMaxStages;
     uint64_t *empty = stats_bar + kSplitMaxStages;
-    uint64_t *xchg = empty + kSplitMaxStages;
+    uint64_t *xchg = empty + kSplitMaxStages;              // [S][2]: one per parity of a stage's use
     volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + kSplitFlagOff);
     int2 *item_hdr = reinterpret_cast<int2 *>(smem + kSplitItemOff);          // [S] (kind, block)
     StageMeta *meta = reinterpret_cast<StageMeta *>(smem + kSplitMetaOff);   // [S][R]
@@ -254,7 +255,8 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
             mbar_init(&full[s], 1);
             mbar_init(&stats_bar[s], 1);
             mbar_init(&empty[s], NC);
-            mbar_init(&xchg[s], K);
+            mbar_init(&xchg[2 * s], 1);
+            mbar_init(&xchg[2 * s + 1], 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -465,14 +467,24 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     vals[j] = __fadd_rn(vals[j], __shfl_xor_sync(kFull, vals[j], d));
             if (K > 1) {
                 // send this slice's partials to every CTA of the cluster
+                // Each lane c < K sends this slice's R partials to CTA c with
+                // st.async, whose completion counts 8 bytes on CTA c's barrier of
+                // this parity of the stage; the local arrival registers the K * R
+                // * 8 bytes expected (a peer's bytes may land first).  A barrier
+                // serves every second use of the stage, so its own phase parity is
+                // that of k / (2S), and a peer can never be a whole phase ahead on
+                // it.  The wait acquires at cluster scope (the peers' stores).
                 float2 *xb = xbuf + ((s * 2 + int(ph)) * K) * R;   // [K][R] for this use of stage s
+                uint64_t *xb_bar = &xchg[2 * s + int(ph)];
+                const uint32_t bp = uint32_t(k / S / 2) & 1u;
+                if (lane == 0) mbar_arrive_expect_tx(xb_bar, uint32_t(K * R * 8));
                 if (lane < K) {
+                    const uint32_t bar_c = map_to_rank(smem_addr(xb_bar), uint32_t(lane));
 #pragma unroll
                     for (int r = 0; r < R; ++r)
-                        st_cluster_f32x2(map_to_rank(smem_addr(xb + rank * R + r), uint32_t(lane)), vals[r], vals[R + r]);
-                    mbar_arrive_remote(map_to_rank(smem_addr(&xchg[s]), uint32_t(lane)));
+                        st_async_f32x2(map_to_rank(smem_addr(xb + rank * R + r), uint32_t(lane)), vals[r], vals[R + r], bar_c);
                 }
-                if (!mbar_wait_bounded_cluster(&xchg[s], ph)) {
+                if (!mbar_wait_bounded_cluster(xb_bar, bp)) {
                     *abort_flag = 1;
                     if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
                     break;
