@@ -165,20 +165,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// try_wait that lets the hardware suspend the thread for up to `hint_ns`
-// while the phase is incomplete, instead of spinning on issue slots.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Waits for the phase with the given parity; gives up after kWaitLimitNs of wall time.
 // Between polls the warp sleeps (32 ns, doubling to 256 ns) so that waiting
 // warps leave the issue slots to the warps that have work.
@@ -223,11 +209,7 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared (L2 only) and its groups: each
-// thread waits only for its own copies.
-__device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
+// cp.async groups: each thread waits only for its own copies.
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -327,14 +309,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(const void *p) {
     return v;
 }
 
-__device__ __forceinline__ uint4 ld_global_stream_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
@@ -350,119 +324,14 @@ __device__ __forceinline__ float4 ld_global_f32x4(const float *p) {
     return v;
 }
 
-// ----------------------------------------------------------------- bf16
-
-// bf16 -> f32 is exact: the bf16 bits are the top half of the binary32.
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-}
-
-// f32 -> bf16 round-to-nearest-even (hardware cvt.rn.bf16x2.f32).
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-        w[i] = *reinterpret_cast<uint32_t *>(&b);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// ----------------------------------------------------------------- packed FP32x2
+// ----------------------------------------------------------------- f2: FP32 pairs in 64-bit registers
 //
 // sm_100-class GPUs execute two FP32 lanes per instruction (add/mul/fma
 // .rn.f32x2).  Each lane is an ordinary IEEE binary32 round-to-nearest-even
 // operation, so values are the same as with scalar __fadd_rn/__fmul_rn/
-// __fmaf_rn; only the instruction count halves.
-
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-    float2 r;
-    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    float2 r;
-    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    float2 r;
-    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return r;
-}
-
-// 8 bf16 (one uint4) -> 4 float2 holding columns (0,1), (2,3), (4,5), (6,7).
-__device__ __forceinline__ void unpack8x2(const uint4 &v, float2 (&f)[4]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
-}
-
-__device__ __forceinline__ uint4 pack8x2(const float2 (&f)[4]) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 b = __floats2bfloat162_rn(f[i].x, f[i].y);
-        w[i] = *reinterpret_cast<uint32_t *>(&b);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// Vector sum of the large-hidden kernels: columns 0,2,4,6 and 1,3,5,7 are
-// folded in two FMA chains (a0*b0, then fma with the next column of the
-// chain), and the two chains are added: (even chain) + (odd chain).
-__device__ __forceinline__ float dot8x2(const float2 (&a)[4], const float2 (&b)[4]) {
-    float2 s = mul2(a[0], b[0]);
-#pragma unroll
-    for (int i = 1; i < 4; ++i) s = fma2(a[i], b[i], s);
-    return __fadd_rn(s.x, s.y);
-}
-
-// Warp "transpose-reduce" of NV values per lane (NV a power of two <= 32):
-// value j's 32 lane terms are added by a complete tree that pairs lanes 16
-// apart first, then 8, 4, 2, 1.  On return lane l holds the warp total of
-// value j = l >> (5 - log2 NV).  Each pair sum is formed once, by the lane
-// that keeps it; NV-1 exchanges plus log2(32/NV) butterflies in all.
-template <int NV>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[NV], int lane) {
-#pragma unroll
-    for (int c = NV, d = 16; c > 1; c >>= 1, d >>= 1) {
-        const bool upper = (lane & d) != 0;
-        const int h = c >> 1;
-#pragma unroll
-        for (int i = 0; i < h; ++i) {
-            const float send = upper ? v[i] : v[i + h];
-            const float keep = upper ? v[i + h] : v[i];
-            v[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, d));
-        }
-    }
-    float r = v[0];
-#pragma unroll
-    for (int d = 16 / NV; d >= 1; d >>= 1) r = __fadd_rn(r, __shfl_xor_sync(kFull, r, d));
-    return r;
-}
-
-// ----------------------------------------------------------------- f2: FP32 pairs in 64-bit registers
-//
-// The same packed arithmetic as add2/mul2/fma2, but the pair lives in one
-// 64-bit register from the bf16 unpack to the bf16 pack, so no moves are
-// needed to assemble or split register pairs around each operation.
+// __fmaf_rn; only the instruction count halves.  The pair lives in one
+// 64-bit register from the bf16 unpack (exact: the bf16 bits are the top
+// half of the binary32) to the bf16 pack.
 
 typedef unsigned long long f2_t;
 
@@ -581,6 +450,18 @@ __device__ __forceinline__ void st_global_f32_if(float *p, float v, uint32_t pre
                  : "memory");
 }
 
+// ----------------------------------------------------------------- 64-leaf tree
+//
+// Streaming form of the complete pairwise tree over the 64 leaves of a
+// logical block: leaf n (0..63) is combined with the pending partials whose
+// bits are set in n (binary counter), earlier leaves always on the left.
+// After leaf 63 the returned value is the block partial.  Any subtree of 2^k
+// aligned leaves can be pushed as one item at level k.
+//
+// TreeStackF2 holds the pending partials of NC FP32 column pairs per lane in
+// registers, for compile-time item indices (push_static);
+// push_group_subtree keeps them in shared memory for a run-time index that is
+// uniform across the warp.
 template <int NC, int LEVELS>
 struct TreeStackF2 {
     f2_t s[LEVELS][NC];
@@ -596,41 +477,6 @@ struct TreeStackF2 {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) s[l][c] = v[c];
                 break;
-            }
-        }
-    }
-
-    template <int LEVEL>
-    __device__ __forceinline__ void push_dyn(f2_t (&v)[NC], int idx) {
-        const int t = __ffs(~idx) - 1;
-#pragma unroll
-        for (int l = LEVEL; l < LEVELS; ++l) {
-            if (l - LEVEL < t) {
-#pragma unroll
-                for (int c = 0; c < NC; ++c) v[c] = f2_add(s[l][c], v[c]);
-            } else if (l - LEVEL == t) {
-#pragma unroll
-                for (int c = 0; c < NC; ++c) s[l][c] = v[c];
-            }
-        }
-    }
-
-    // The same as push_static<0> for a run-time index that is uniform across
-    // the warp: a chain of uniform branches, so only the levels that the item
-    // closes are added.
-    __device__ __forceinline__ void push_uniform(f2_t (&v)[NC], int idx) {
-        bool carry = true;
-#pragma unroll
-        for (int l = 0; l < LEVELS; ++l) {
-            if (carry) {
-                if ((idx >> l) & 1) {
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) v[c] = f2_add(s[l][c], v[c]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) s[l][c] = v[c];
-                    carry = false;
-                }
             }
         }
     }
@@ -682,22 +528,6 @@ __device__ __forceinline__ void push_group_subtree(f2_t (&v)[NC], int idx, uint3
 // The forward and the backward use the same kernel family for a given H, so
 // rstd is bitwise the same in both.
 
-__device__ __forceinline__ float dot8(const float (&a)[8], const float (&b)[8]) {
-    float s = __fmul_rn(a[0], b[0]);
-#pragma unroll
-    for (int i = 1; i < 8; ++i) s = __fmaf_rn(a[i], b[i], s);
-    return s;
-}
-
-// Butterfly over lanes xor 1 .. width/2 (width a power of two <= 32): every
-// lane of each aligned group of `width` lanes ends with the group's sum.
-__device__ __forceinline__ float lane_tree(float v, int width) {
-#pragma unroll
-    for (int k = 1; k < 32; k <<= 1)
-        if (k < width) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, k));
-    return v;
-}
-
 // v / H, correctly rounded.  For a power-of-two H it is the product with the
 // exact reciprocal 2^-k: both operations round the same real number, so the
 // result is the same bit pattern and the division's longer sequence is
@@ -718,101 +548,5 @@ __device__ __forceinline__ float row_rstd(float ss, float Hf, float inv_h, float
 __device__ __forceinline__ float row_mean_gxhat(float gx, float rstd, float Hf, float inv_h) {
     return div_h(__fmul_rn(gx, rstd), Hf, inv_h);
 }
-
-// ----------------------------------------------------------------- 64-leaf tree
-//
-// Streaming form of the complete pairwise tree over the 64 leaves of a
-// logical block: leaf n (0..63) is combined with the pending partials whose
-// bits are set in n (binary counter), earlier leaves always on the left.
-// After leaf 63 the returned value is the block partial.  Any subtree of 2^k
-// aligned leaves can be pushed as one item at level k.
-
-template <int NCOL>
-struct TreeStack {
-    float s[kBlockLevels][NCOL];
-
-    // Push v (a complete subtree of 2^level leaves) as item `idx` at that
-    // level; on return v holds the partial that was just completed (the whole
-    // block after the last item).  idx is uniform across the threads that
-    // share the tree.
-    __device__ __forceinline__ void push(float (&v)[NCOL], int idx, int level) {
-        bool carry = true;
-#pragma unroll
-        for (int l = 0; l < kBlockLevels; ++l) {
-            if (l < level || !carry) continue;
-            const bool bit = (idx >> (l - level)) & 1;
-#pragma unroll
-            for (int c = 0; c < NCOL; ++c) {
-                const float sum = __fadd_rn(s[l][c], v[c]);
-                s[l][c] = bit ? s[l][c] : v[c];
-                v[c] = bit ? sum : v[c];
-            }
-            carry = bit;
-        }
-    }
-
-    // Carry-tree result of n items (1 <= n <= 63) pushed as push(v, i, 0),
-    // i = 0..n-1: the pending partials (set bits of n) folded from the lowest
-    // level up, later items always on the right.  This is the pairwise tree
-    // that pairs (2i, 2i+1) at every level and carries an odd last element.
-    __device__ __forceinline__ void fold(int n, float (&res)[NCOL]) const {
-        bool have = false;
-#pragma unroll
-        for (int c = 0; c < NCOL; ++c) res[c] = 0.f;
-#pragma unroll
-        for (int l = 0; l < kBlockLevels; ++l) {
-            if (!((n >> l) & 1)) continue;
-            if (!have) {
-#pragma unroll
-                for (int c = 0; c < NCOL; ++c) res[c] = s[l][c];
-                have = true;
-            } else {
-#pragma unroll
-                for (int c = 0; c < NCOL; ++c) res[c] = __fadd_rn(s[l][c], res[c]);
-            }
-        }
-    }
-};
-
-// Same tree over float2 column pairs.  push_static is for compile-time item
-// indices (the rows of one batch); push_dyn for a run-time index that is
-// uniform across the team (the batch within a block): the trailing one bits
-// of idx say how many pending partials the new subtree closes.
-template <int NC, int LEVELS = kBlockLevels>
-struct TreeStack2 {
-    float2 s[LEVELS][NC];
-
-    template <int LEVEL>
-    __device__ __forceinline__ void push_static(float2 (&v)[NC], int idx) {
-#pragma unroll
-        for (int l = LEVEL; l < LEVELS; ++l) {
-            if ((idx >> (l - LEVEL)) & 1) {
-#pragma unroll
-                for (int c = 0; c < NC; ++c) v[c] = add2(s[l][c], v[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < NC; ++c) s[l][c] = v[c];
-                break;
-            }
-        }
-    }
-
-    // The subtree completed by the last item of a tree of 2^LEVELS leaves is
-    // returned in v and not stored.
-    template <int LEVEL>
-    __device__ __forceinline__ void push_dyn(float2 (&v)[NC], int idx) {
-        const int t = __ffs(~idx) - 1;                   // trailing ones of idx
-#pragma unroll
-        for (int l = LEVEL; l < LEVELS; ++l) {
-            if (l - LEVEL < t) {
-#pragma unroll
-                for (int c = 0; c < NC; ++c) v[c] = add2(s[l][c], v[c]);
-            } else if (l - LEVEL == t) {
-#pragma unroll
-                for (int c = 0; c < NC; ++c) s[l][c] = v[c];
-            }
-        }
-    }
-};
 
 }  // namespace rbi
