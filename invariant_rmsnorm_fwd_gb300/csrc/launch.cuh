@@ -77,14 +77,13 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
     return RMSNORM_OK;
 }
 
-// The stats-warp count: a K-CTA team (K > 1) exchanges row partials through
-// distributed shared memory, and a stats warp waits for its peers on every
-// stage, so more stats warps keep more stages' exchanges in flight (measured
-// on hidden 8192: forward best with 3, backward with 6).  A single CTA keeps
-// 2 for the forward and takes 3 for the backward when they fit in 640
-// threads (hidden 4096: backward 0.73 -> 0.75 of the peak, step -3%).
-// Bounded by the 23 warps of the widest launch.  Thread counts up to 640 get
-// the 96-register budget, wider ones 80.
+// The stats-warp count: 3 when the CTA stays within 640 threads (96 registers
+// per thread), else 2; a single CTA's forward keeps 2.  Measured: hidden 4096
+// backward 0.73 -> 0.75 of the peak with 3; on the 2-CTA clusters of hidden
+// 8192, with the row-sum exchange by st.async, 3 beat 6 (736 threads, 80
+// registers) by 5% on the c2 headline and 4 by 7% (with the earlier exchange
+// by remote stores and release arrivals, 6 had been best).  Thread counts up
+// to 640 get the 96-register budget, wider ones 80.
 template <int MODE, int R, int K, int NS>
 int launch_split_ns(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
     if ((sh.nc + NS + 1) * 32 <= 640) return launch_split_t<MODE, R, 640, NS, K>(p, sh, d, stream);
@@ -93,10 +92,8 @@ int launch_split_ns(const KParams &p, const Shape &sh, const DeviceInfo &d, cuda
 
 template <int MODE, int R, int K>
 int launch_split_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
-    constexpr int kWant = K == 1 ? (ModeTraits<MODE>::kFwdLike ? kSplitStatsWarps : 3)
-                                 : (ModeTraits<MODE>::kFwdLike ? 3 : 6);
-    constexpr int kMaxWarps = K == 1 ? 640 / 32 : 736 / 32;
-    if (kWant > kSplitStatsWarps && sh.nc + kWant + 1 <= kMaxWarps)
+    constexpr int kWant = (K == 1 && ModeTraits<MODE>::kFwdLike) ? kSplitStatsWarps : 3;
+    if (kWant > kSplitStatsWarps && sh.nc + kWant + 1 <= 640 / 32)
         return launch_split_ns<MODE, R, K, kWant>(p, sh, d, stream);
     return launch_split_ns<MODE, R, K, kSplitStatsWarps>(p, sh, d, stream);
 }
