@@ -30,7 +30,7 @@ def _workload(lengths, hidden, seed=7, x_std=1.0, dy_std=1e-2):
 
 # ------------------------------------------------------------------ exact order
 
-@pytest.mark.parametrize("hidden", [8, 128, 4096, 5120])
+@pytest.mark.parametrize("hidden", [8, 24, 128, 200, 4096, 5120])
 @pytest.mark.parametrize("n_rows", [1, 63, 64, 65, 259, 4999, 10500])
 def test_dweight_follows_the_fixed_tree_bitwise(hidden, n_rows):
     """eps = 0 and rows of constant magnitude 2^k make xhat = +-1 exactly, so the
@@ -141,8 +141,8 @@ def test_constant_rows_map_to_w_times_sign_bitwise():
 
 # ------------------------------------------------------------------ hidden sizes
 
-@pytest.mark.parametrize("hidden", [8, 16, 24, 64, 128, 136, 256, 264, 512, 1024, 4096, 4104, 5120, 6144, 8192,
-                                    12288, 16384])
+@pytest.mark.parametrize("hidden", [8, 16, 24, 40, 64, 72, 128, 136, 200, 256, 264, 512, 1024, 4096, 4104, 5120,
+                                    6144, 8192, 12288, 16384])
 def test_hidden_sweep_invariance_and_accuracy(hidden):
     wl = _workload([70, 3, 130, 1, 64, 9], hidden, seed=hidden)
     x, dy, w, lays, runs = G.run_all_layouts(wl)
@@ -218,12 +218,15 @@ def test_in_place_forward_and_dx_over_dy():
     assert torch.equal(d2.view(torch.int16), dx_ref.view(torch.int16))
 
 
-def test_rstd_output_matches_oracle():
-    H = 256
+@pytest.mark.parametrize("with_plan", [False, True])
+@pytest.mark.parametrize("H", [8, 64, 128, 256, 1024, 8192])
+def test_rstd_output_matches_oracle(H, with_plan):
+    """rstd of every active slot (small-row teams of 1 to 32 lanes, one CTA and
+    2-CTA clusters); an inactive slot keeps what the caller put there."""
     wl = _workload([20, 12], H)
     x, dy, w = G.logical_inputs(wl)
     tok = np.array([3, -1, 0, 1, 2] + list(range(4, 32)), dtype=np.int32)
-    cl = rb.call_layout(tok, 1, 32, with_plan=False)
+    cl = rb.call_layout(tok, 1, 32, with_plan=with_plan)
     xp = torch.zeros(tok.size, H, dtype=torch.bfloat16, device=DEV)
     act = torch.as_tensor(tok >= 0, device=DEV)
     xp[act] = x.reshape(32, H)[torch.as_tensor(tok[tok >= 0], device=DEV).long()]
