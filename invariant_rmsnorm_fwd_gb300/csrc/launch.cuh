@@ -78,7 +78,8 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
 }
 
 // The stats-warp count: 3 when the CTA stays within 640 threads (96 registers
-// per thread), else 2; a single CTA's forward keeps 2.  Measured: hidden 4096
+// per thread), or for the backward within 768 (80 registers, the same as 736),
+// else 2; a single CTA's forward keeps 2.  Measured: hidden 4096
 // backward 0.73 -> 0.75 of the peak with 3; on the 2-CTA clusters of hidden
 // 8192, with the row-sum exchange by st.async, 3 beat 6 (736 threads, 80
 // registers) by 5% on the c2 headline and 4 by 7% (with the earlier exchange
@@ -87,14 +88,21 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
 template <int MODE, int R, int K, int NS>
 int launch_split_ns(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
     if ((sh.nc + NS + 1) * 32 <= 640) return launch_split_t<MODE, R, 640, NS, K>(p, sh, d, stream);
-    return launch_split_t<MODE, R, 736, NS, K>(p, sh, d, stream);
+    if ((sh.nc + NS + 1) * 32 <= 736) return launch_split_t<MODE, R, 736, NS, K>(p, sh, d, stream);
+    return launch_split_t<MODE, R, 768, NS, K>(p, sh, d, stream);
 }
 
 template <int MODE, int R, int K>
 int launch_split_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
     constexpr int kWant = (K == 1 && ModeTraits<MODE>::kFwdLike) ? kSplitStatsWarps : 3;
+    // 21 to 24 warps all leave 80 registers (six warps per sub-partition), so
+    // the widest backward takes the third stats warp for free (hidden 5120:
+    // 768 threads, c4 headline -0.9%)
+    constexpr int kMaxWarps = ModeTraits<MODE>::kFwdLike ? 640 / 32 : 768 / 32;
     if (kWant > kSplitStatsWarps && sh.nc + kWant + 1 <= 640 / 32)
         return launch_split_ns<MODE, R, K, kWant>(p, sh, d, stream);
+    if (kWant > kSplitStatsWarps && sh.nc + kWant + 1 <= kMaxWarps)
+        return launch_split_t<MODE, R, 768, kWant, K>(p, sh, d, stream);
     return launch_split_ns<MODE, R, K, kSplitStatsWarps>(p, sh, d, stream);
 }
 
