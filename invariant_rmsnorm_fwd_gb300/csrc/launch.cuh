@@ -77,33 +77,32 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
     return RMSNORM_OK;
 }
 
-// The stats-warp count: 3 when the CTA stays within 640 threads (96 registers
-// per thread), or for the backward within 768 (80 registers, the same as 736),
-// else 2; a single CTA's forward keeps 2.  Measured: hidden 4096
-// backward 0.73 -> 0.75 of the peak with 3; on the 2-CTA clusters of hidden
-// 8192, with the row-sum exchange by st.async, 3 beat 6 (736 threads, 80
-// registers) by 5% on the c2 headline and 4 by 7% (with the earlier exchange
-// by remote stores and release arrivals, 6 had been best).  Thread counts up
-// to 640 get the 96-register budget, wider ones 80.
-template <int MODE, int R, int K, int NS>
-int launch_split_ns(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
-    if ((sh.nc + NS + 1) * 32 <= 640) return launch_split_t<MODE, R, 640, NS, K>(p, sh, d, stream);
-    if ((sh.nc + NS + 1) * 32 <= 736) return launch_split_t<MODE, R, 736, NS, K>(p, sh, d, stream);
-    return launch_split_t<MODE, R, 768, NS, K>(p, sh, d, stream);
-}
-
+// The CTA shape: column warps (from the hidden size), stats warps and one
+// producer.  A CTA's warps are spread over the SM's four sub-partitions, so
+// up to 20 warps (640 threads) leave 96 registers per thread and 21 to 24
+// warps 80.  Three stats warps whenever the CTA stays within 640 threads;
+// beyond that the backward takes three in 768 threads (the same 80
+// registers as 736; hidden 5120: c4 headline -0.9%) and the forward two in
+// 736; a single CTA's forward keeps two.  Measured: hidden 4096 backward
+// 0.73 -> 0.75 of the peak with three; on the 2-CTA clusters of hidden 8192,
+// with the row-sum exchange by st.async, three beat six (736 threads) by 5%
+// on the c2 headline and four by 7%.  Only the shapes that hidden sizes up to
+// 16384 reach are instantiated: a slice has at most 20 column warps, and at
+// most 16 on 4-CTA clusters.
 template <int MODE, int R, int K>
 int launch_split_k(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaStream_t stream) {
-    constexpr int kWant = (K == 1 && ModeTraits<MODE>::kFwdLike) ? kSplitStatsWarps : 3;
-    // 21 to 24 warps all leave 80 registers (six warps per sub-partition), so
-    // the widest backward takes the third stats warp for free (hidden 5120:
-    // 768 threads, c4 headline -0.9%)
-    constexpr int kMaxWarps = ModeTraits<MODE>::kFwdLike ? 640 / 32 : 768 / 32;
-    if (kWant > kSplitStatsWarps && sh.nc + kWant + 1 <= 640 / 32)
-        return launch_split_ns<MODE, R, K, kWant>(p, sh, d, stream);
-    if (kWant > kSplitStatsWarps && sh.nc + kWant + 1 <= kMaxWarps)
-        return launch_split_t<MODE, R, 768, kWant, K>(p, sh, d, stream);
-    return launch_split_ns<MODE, R, K, kSplitStatsWarps>(p, sh, d, stream);
+    constexpr bool kFwd = ModeTraits<MODE>::kFwdLike;
+    constexpr int kStats = (kFwd && K == 1) ? kSplitStatsWarps : 3;
+    if ((sh.nc + kStats + 1) * 32 <= 640) return launch_split_t<MODE, R, 640, kStats, K>(p, sh, d, stream);
+    if constexpr (K == 4) {
+        return RMSNORM_ERR_HIDDEN;
+    } else if constexpr (!kFwd) {
+        return launch_split_t<MODE, R, 768, 3, K>(p, sh, d, stream);
+    } else {
+        if (kStats > kSplitStatsWarps && (sh.nc + kSplitStatsWarps + 1) * 32 <= 640)
+            return launch_split_t<MODE, R, 640, kSplitStatsWarps, K>(p, sh, d, stream);
+        return launch_split_t<MODE, R, 736, kSplitStatsWarps, K>(p, sh, d, stream);
+    }
 }
 
 template <int MODE, int R>

@@ -527,24 +527,34 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
         const int t = tid;                                   // vector owned: slice columns 8t..8t+7
         const bool has_vec = t < VS;
         const int64_t my_col = col0 + int64_t(t) * 8;
-        f2_t wv[4];
-        if (MODE != kDw && has_vec) f2_unpack8(*reinterpret_cast<const uint4 *>(p.w + my_col), wv);
-        const float gscale = p.grad_scale;
+        // Under the 80-register budget (more than 640 threads) the weights stay
+        // packed (4 registers instead of 8) and are unpacked for every row.
+        constexpr bool kPackW = MAXT > 640;
+        uint4 wpk = make_uint4(0, 0, 0, 0);
+        f2_t wv[4] = {0ull, 0ull, 0ull, 0ull};
+        if (MODE != kDw && has_vec) {
+            wpk = *reinterpret_cast<const uint4 *>(p.w + my_col);
+            if (!kPackW) f2_unpack8(wpk, wv);
+        }
         TreeStackF2<4, 4> tree;            // levels log2(R)..3 of the 16-leaf unit
-        int32_t kind = 0, block = -1, quarter = 0, qmask = 0;
-        bool keep = false, spill_unit = false;           // of the current unit
-        const uint32_t vec_mask = has_vec ? ~0u : 0u;
+        // Of the current unit: where its partial goes (a quarter of a block, or
+        // an eighth in the last round), whether it is stored, whether its rows
+        // are spilled.  Set at the unit's first batch, so nothing else about
+        // the item stays live across the unit.
+        float *part = p.ws.block_partial;
+        uint32_t part_mask = 0;
+        bool spill_unit = false;
         int s = 0;
         uint32_t parity = 0;
-        int64_t u = cluster_id;                               // current quarter unit
+        uint32_t u = uint32_t(cluster_id);                    // current quarter unit (low bits)
         // Leaf modes walk their 16-row units; the inner loop over the unit's
         // batches (stages of R rows) is unrolled, so `sub`, the batch's place in
         // the unit, is a compile-time constant and the tree positions are static.
         // A team's eighth (8 rows, kInner / 2 batches) comes after its quarters.
         constexpr int kInner = T::kLeaves ? kUnitBatches : 1;
-        const int64_t n_outer = T::kLeaves ? my_units + my_eighths : n_batches;
+        const int n_outer = T::kLeaves ? int(my_units + my_eighths) : n_batches;
         bool stop = false;
-        for (int64_t j = 0; j < n_outer && !stop; ++j, u += n_clusters) {
+        for (int j = 0; j < n_outer && !stop; ++j, u += uint32_t(n_clusters)) {
           const bool half_unit = T::kLeaves && j >= my_units;
 #pragma unroll
           for (int sub = 0; sub < kInner; ++sub) {
@@ -561,18 +571,28 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
             }
             if (T::kLeaves && sub == 0) {                    // item header, staged by the producer
                 const int2 hd = item_hdr[s];
-                quarter = half_unit ? int((q_full * n_clusters + (cluster_id >> 1)) & 3) : int(u & 3);
-                kind = hd.x & 0xff;
-                qmask = hd.x >> 8;
-                block = hd.y;
+                const int quarter = half_unit ? int((q_full * n_clusters + (cluster_id >> 1)) & 3) : int(u & 3u);
+                int kind = hd.x & 0xff;
+                const int qmask = hd.x >> 8;
+                const int32_t block = hd.y;
                 const bool blocked = kind == kItemWhole || kind == kItemQuarters;
                 if ((blocked && (block < 0 || block >= p.ws.n_blocks)) || (!blocked && kind != kItemSpill)) {
                     if (t == 0 && rank == 0) set_status(p.ws.hdr, kStPlan);
                     kind = kBadItem;
                 }
                 // a quarter of a kind-2 item that the call does not hold is skipped
-                keep = kind == kItemWhole || (kind == kItemQuarters && ((qmask >> quarter) & 1));
+                const bool keep = kind == kItemWhole || (kind == kItemQuarters && ((qmask >> quarter) & 1));
                 spill_unit = kind == kItemSpill;
+                const int half = int(cluster_id & 1);
+                part = ((half_unit && half) ? p.ws.eighth : p.ws.block_partial) +
+                       (int64_t(keep ? block : 0) * 4 + quarter) * H + my_col;
+                part_mask = (keep && has_vec) ? ~0u : 0u;
+                // the finalize reads the marks after this launch, so the unit is
+                // marked here rather than after its partial is stored
+                if (keep && t == 0 && rank == 0) {
+                    if (half_unit) mark_eighth(p.ws, block, quarter, half);
+                    else mark_quarter(p.ws, block, quarter);
+                }
             }
             const StageMeta *m = meta + s * R;
             TreeStackF2<4, (kLogR > 0 ? kLogR : 1)> mini;
@@ -585,6 +605,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     const SplitStats st = stats[s * R + r];
                     const f2_t r2 = f2_make(st.rstd, st.rstd);
                     f2_t xf[4], xh[4], o[4];
+                    if (kPackW) f2_unpack8_v(wpk, wv);
                     f2_unpack8(ld_shared_v4(stage_ptr(s, 0, r) + t * 16), xf);
                     if (MODE == kAddFwd) {                          // h = bf16(x + r), stored, then normed
                         f2_t rf[4];
@@ -606,7 +627,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                         f2_unpack8(ld_shared_v4(stage_ptr(s, 1, r) + t * 16), df);
                         if (T::kNeedGx && p.out != nullptr) {
                             const f2_t nm2 = f2_make(-st.mg, -st.mg);
-                            const float rs = __fmul_rn(st.rstd, gscale);    // == rstd when unscaled
+                            const float rs = __fmul_rn(st.rstd, p.grad_scale);    // == rstd when unscaled
                             const f2_t rs2 = f2_make(rs, rs);
 #pragma unroll
                             for (int i = 0; i < 4; ++i) o[i] = f2_mul(rs2, f2_fma(xh[i], nm2, f2_mul(df[i], wv[i])));
@@ -631,16 +652,9 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     if (R > 1) mini.template push_static<0>(leaf, r);
                     if (r == R - 1) {
                         tree.template push_static<kLogR>(leaf, sub);
-                        if (sub == kUnitBatches - 1) {               // leaf[] is the quarter partial
-                            st_global_f2_if(p.ws.block_partial + (int64_t(block) * 4 + quarter) * H + my_col, leaf,
-                                            keep ? vec_mask : 0u);
-                            if (keep && t == 0 && rank == 0) mark_quarter(p.ws, block, quarter);
-                        } else if (half_unit && sub == kUnitBatches / 2 - 1) {   // the eighth partial
-                            const int half = int(cluster_id & 1);
-                            float *dst = half ? p.ws.eighth : p.ws.block_partial;
-                            st_global_f2_if(dst + (int64_t(block) * 4 + quarter) * H + my_col, leaf, keep ? vec_mask : 0u);
-                            if (keep && t == 0 && rank == 0) mark_eighth(p.ws, block, quarter, half);
-                        }
+                        // leaf[] is now the quarter partial, or the eighth partial
+                        if (sub == kUnitBatches - 1 || (half_unit && sub == kUnitBatches / 2 - 1))
+                            st_global_f2_if(part, leaf, part_mask);
                     }
                 }
             }
