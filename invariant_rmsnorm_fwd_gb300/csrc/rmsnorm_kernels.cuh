@@ -22,6 +22,7 @@
 // output depends only on its row (y, dx, the leaf) or on the fixed trees.
 #pragma once
 #include "rbi_device.cuh"
+#include "umma.cuh"
 
 namespace rbi {
 
@@ -196,6 +197,7 @@ struct SplitStats {
 };
 
 constexpr int kSplitFlagOff = 480;                                   // after 5 x 12 barriers (480 B)
+constexpr int kSplitTmemOff = 484;                                   // tensor-memory base (column warps)
 constexpr int kSplitItemOff = 496;                                   // [kSplitMaxStages] int2 item headers
 constexpr int kSplitMetaOff = 608;
 constexpr int kSplitStatsOff = kSplitMetaOff + kSplitMaxStages * kMaxBatch * 16;
@@ -216,6 +218,7 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     uint64_t *empty = stats_bar + kSplitMaxStages;
     uint64_t *xchg = empty + kSplitMaxStages;              // [S][2]: one per parity of a stage's use
     volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(smem + kSplitFlagOff);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kSplitTmemOff);
     int2 *item_hdr = reinterpret_cast<int2 *>(smem + kSplitItemOff);          // [S] (kind, block)
     StageMeta *meta = reinterpret_cast<StageMeta *>(smem + kSplitMetaOff);   // [S][R]
     SplitStats *stats = reinterpret_cast<SplitStats *>(smem + kSplitStatsOff);
@@ -317,6 +320,22 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
     if (warp == NC + NS && lane == 0) {
 #pragma unroll
         for (int i = 0; i < kPrefetch; ++i) load(i, ring[i]);
+    }
+    // Under the 80-register budget (more than 640 threads) the leaf modes of
+    // 2-CTA clusters and of the residual chain park level 3 of a column
+    // thread's unit tree (the partial of a quarter's first 8 rows, pending while
+    // the second half runs) in tensor memory, which this kernel does not
+    // otherwise use; without it they spill.  Column warp w holds it in
+    // tensor-memory lanes 32 (w % 4) .. +31, columns 8 (w / 4) .. +7.  Warp 0
+    // allocates and, after the closing barrier, frees it.  (The single-CTA
+    // fused backward fits 80 registers without it, and is 0.9% faster so on
+    // the hidden-5120 headline: 2.342 against 2.363 ms.)
+    constexpr bool kStash = T::kLeaves && MAXT > 640 && kLogR < 3 && (K > 1 || T::kRes);
+    constexpr uint32_t kStashCols = 64;                  // 8 (ceil(NC / 4)) <= 64 for NC <= 32
+    if (kStash && warp == 0) {
+        umma::tmem_alloc(tmem_slot, kStashCols);
+        umma::tmem_relinquish();
+        umma::fence_before();
     }
     if (K > 1) cluster_barrier(); else __syncthreads();
     // The weights in shared memory are read by the stats warps only: they fill
@@ -527,16 +546,22 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
         const int t = tid;                                   // vector owned: slice columns 8t..8t+7
         const bool has_vec = t < VS;
         const int64_t my_col = col0 + int64_t(t) * 8;
-        // Under the 80-register budget (more than 640 threads) the weights stay
-        // packed (4 registers instead of 8) and are unpacked for every row.
-        constexpr bool kPackW = MAXT > 640;
+        // In the leaf modes under the 80-register budget (more than 640
+        // threads) the weights stay packed (4 registers instead of 8) and are
+        // unpacked for every row.
+        constexpr bool kPackW = T::kLeaves && MAXT > 640;
         uint4 wpk = make_uint4(0, 0, 0, 0);
         f2_t wv[4] = {0ull, 0ull, 0ull, 0ull};
         if (MODE != kDw && has_vec) {
             wpk = *reinterpret_cast<const uint4 *>(p.w + my_col);
             if (!kPackW) f2_unpack8(wpk, wv);
         }
-        TreeStackF2<4, 4> tree;            // levels log2(R)..3 of the 16-leaf unit
+        TreeStackF2<4, kStash ? 3 : 4> tree;   // levels log2(R)..3 (..2 with the stash) of the 16-leaf unit
+        uint32_t stash = 0;
+        if (kStash) {
+            umma::fence_after();
+            stash = *tmem_slot + (uint32_t((warp & 3) * 32) << 16) + uint32_t((warp >> 2) * 8);
+        }
         // Of the current unit: where its partial goes (a quarter of a block, or
         // an eighth in the last round), whether it is stored, whether its rows
         // are spilled.  Set at the unit's first batch, so nothing else about
@@ -559,11 +584,14 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
 #pragma unroll
           for (int sub = 0; sub < kInner; ++sub) {
             if (half_unit && sub >= kInner / 2) break;
-            if (*abort_flag) {
+            // with the stash the warp leaves as one (tensor-memory accesses are
+            // warp-wide)
+            if (kStash ? __any_sync(kFull, *abort_flag != 0) : *abort_flag != 0) {
                 stop = true;
                 break;
             }
-            if (!mbar_wait_bounded(&stats_bar[s], parity) || !mbar_wait_bounded(&full[s], parity)) {
+            const bool ready = mbar_wait_bounded(&stats_bar[s], parity) && mbar_wait_bounded(&full[s], parity);
+            if (kStash ? !__all_sync(kFull, ready) : !ready) {
                 *abort_flag = 1;
                 if (T::kLeaves) set_status(p.ws.hdr, kStTimeout);
                 stop = true;
@@ -652,6 +680,25 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
                     if (R > 1) mini.template push_static<0>(leaf, r);
                     if (r == R - 1) {
                         tree.template push_static<kLogR>(leaf, sub);
+                        if (kStash && !half_unit && sub == kUnitBatches / 2 - 1) {   // the first half's partial
+                            uint32_t h[8];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                h[2 * c] = uint32_t(leaf[c]);
+                                h[2 * c + 1] = uint32_t(leaf[c] >> 32);
+                            }
+                            __syncwarp();
+                            umma::st_32x32_x8(stash, h);
+                            umma::wait_st();
+                        }
+                        if (kStash && sub == kUnitBatches - 1) {     // first half + second half
+                            uint32_t h[8];
+                            __syncwarp();
+                            umma::ld_32x32_x8(stash, h);
+                            umma::wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) leaf[c] = f2_add((f2_t(h[2 * c + 1]) << 32) | h[2 * c], leaf[c]);
+                        }
                         // leaf[] is now the quarter partial, or the eighth partial
                         if (sub == kUnitBatches - 1 || (half_unit && sub == kUnitBatches / 2 - 1))
                             st_global_f2_if(part, leaf, part_mask);
@@ -677,7 +724,17 @@ __global__ void __launch_bounds__(MAXT, 1) split_kernel(const KParams p, const i
           }
         }
     }
-    if (K > 1) cluster_barrier();      // peers may still store into our exchange buffers
+    if (kStash) {
+        umma::fence_before();
+        if (K > 1) cluster_barrier(); else __syncthreads();
+        if (warp == 0) {
+            __syncwarp();
+            umma::fence_after();
+            umma::tmem_dealloc(*tmem_slot, kStashCols);
+        }
+    } else if (K > 1) {
+        cluster_barrier();             // peers may still store into our exchange buffers
+    }
 }
 
 __device__ __forceinline__ f2_t shfl_xor_f2(f2_t v, int k) {

@@ -59,7 +59,7 @@ def _check_chain(run, x, r, dy, dres, w, eps, s, rows=None):
     return rep
 
 
-@pytest.mark.parametrize("hidden", [8, 64, 128, 256, 264, 1024, 4096, 5120, 8192, 16384])
+@pytest.mark.parametrize("hidden", [8, 64, 128, 256, 264, 1024, 4096, 5120, 8192, 10240, 16384])
 def test_chain_matches_oracle_and_is_layout_invariant(hidden):
     wl = synth.Workload("t", hidden, np.asarray([70, 3, 130, 1, 64, 9]), seed=hidden, chunk_rows=37)
     x, r, dy, dres, w = _inputs(wl)

@@ -98,13 +98,15 @@ def _assert_tree_layouts(lengths, rpt, hidden, seed, kinds=_TREE_KINDS, chunk=37
         assert got.tobytes() == want.tobytes(), (kind, hidden, rpt, np.flatnonzero(got != want)[:5])
 
 
-@pytest.mark.parametrize("hidden", [8192, 16384])
+@pytest.mark.parametrize("hidden", [8192, 10240, 16384])
 @pytest.mark.parametrize("n_tok", [1, 65, 259, 4999])
 def test_dweight_tree_bitwise_on_cluster_kernels(hidden, n_tok):
     """Hidden sizes above 5120 run on 2- and 4-CTA clusters (row sums exchanged
-    through distributed shared memory, column slices split over the CTAs); the
-    tree must still be the fixed one, in every layout.  4999 rows: 316 quarter
-    units leave a partial last round, which the backward splits into eighths."""
+    through distributed shared memory, column slices split over the CTAs;
+    10240: 768-thread CTAs, whose column threads keep part of the unit tree
+    in tensor memory); the tree must still be the fixed one, in every layout.
+    4999 rows: 316 quarter units leave a partial last round, which the
+    backward splits into eighths."""
     _assert_tree_layouts(_split_lengths(n_tok, hidden + n_tok), 1, hidden, hidden * 7 + n_tok)
 
 
@@ -142,7 +144,7 @@ def test_constant_rows_map_to_w_times_sign_bitwise():
 # ------------------------------------------------------------------ hidden sizes
 
 @pytest.mark.parametrize("hidden", [8, 16, 24, 40, 64, 72, 128, 136, 200, 256, 264, 512, 1024, 4096, 4104, 5120,
-                                    6144, 8192, 12288, 16384])
+                                    6144, 8192, 10240, 12288, 16384])
 def test_hidden_sweep_invariance_and_accuracy(hidden):
     wl = _workload([70, 3, 130, 1, 64, 9], hidden, seed=hidden)
     x, dy, w, lays, runs = G.run_all_layouts(wl)
@@ -179,8 +181,8 @@ def test_empty_multiset_gives_zero_dweight():
 
 # ------------------------------------------------------------------ paths agree
 
-def test_contrib_only_and_dx_only_match_fused():
-    H = 4096
+@pytest.mark.parametrize("H", [4096, 5120, 10240])
+def test_contrib_only_and_dx_only_match_fused(H):
     wl = _workload([100, 50], H)
     x, dy, w = G.logical_inputs(wl)
     cl = rb.call_layout(np.arange(150, dtype=np.int32), 1, 150)
