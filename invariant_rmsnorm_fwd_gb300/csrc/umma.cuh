@@ -1,8 +1,8 @@
 // Fifth-generation tensor-core (tcgen05) and tensor-memory-access (TMA)
-// wrappers for sm_103a, as inline PTX: tensor-memory allocation, the
-// bf16 x bf16 -> FP32 MMA with operands in shared memory, its commit to an
-// mbarrier, tensor-memory loads, 2-D tiled TMA loads, and the two 32/64-bit
-// descriptors the MMA takes.
+// wrappers for sm_103a, as inline PTX: tensor-memory allocation, loads and
+// stores (registers <-> tensor memory), the CTA-pair bf16 x bf16 -> FP32 MMA
+// with operands in shared memory and its commit to the pair's mbarriers, 2-D
+// tiled TMA loads, and the two 32/64-bit descriptors the MMA takes.
 #pragma once
 #include <cuda.h>
 
@@ -33,25 +33,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 // `after` behind the sync in the thread that continues.
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D[tmem] (+)= A[smem] * B[smem], kind::f16 (here bf16 inputs, FP32
-// accumulator); accumulate = 0 overwrites D.  Issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// One arrival on `bar` once every tcgen05 operation this thread issued so far
-// has completed.
-__device__ __forceinline__ void commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_addr(bar))
-                 : "memory");
-}
 
 // 32 consecutive FP32 columns of the warp's 32 lanes: lane l gets tensor-memory
 // lane (taddr.lane + l), columns taddr.col .. +31.  Whole warp; the values are
