@@ -82,11 +82,12 @@ int launch_split_t(const KParams &p, const Shape &sh, const DeviceInfo &d, cudaS
 // up to 20 warps (640 threads) leave 96 registers per thread and 21 to 24
 // warps 80.  Three stats warps whenever the CTA stays within 640 threads;
 // beyond that the backward takes three in 768 threads (the same 80
-// registers as 736; hidden 5120: c4 headline -0.9%) and the forward two in
+// registers as 736; hidden 5120 in 256 calls of 4096 token slots: -0.9% per
+// step) and the forward two in
 // 736; a single CTA's forward keeps two.  Measured: hidden 4096 backward
 // 0.73 -> 0.75 of the peak with three; on the 2-CTA clusters of hidden 8192,
 // with the row-sum exchange by st.async, three beat six (736 threads) by 5%
-// on the c2 headline and four by 7%.  Only the shapes that hidden sizes up to
+// on hidden 8192 in 117 calls of 2048 token slots and four by 7%.  Only the shapes that hidden sizes up to
 // 16384 reach are instantiated: a slice has at most 20 column warps, and at
 // most 16 on 4-CTA clusters.
 template <int MODE, int R, int K>
