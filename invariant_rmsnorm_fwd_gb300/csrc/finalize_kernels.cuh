@@ -200,7 +200,26 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, c
     }
 #pragma unroll
     for (int c = 0; c < 8; ++c) part[w][c][lane] = pair[c];
-    // the pair results, level by level: element i of the next level is
+    if (m == 32) {
+        // a full group: the 16 pair results make a complete tree (levels 2-5),
+        // formed in registers after one barrier, warp c < 8 taking column c of
+        // the CTA's 32 vectors
+        __syncthreads();
+        if (w < 8 && has_vec) {
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = part[i][w][lane];
+#pragma unroll
+            for (int n = 8; n >= 1; n >>= 1)
+#pragma unroll
+                for (int i = 0; i < n; ++i) x[i] = __fadd_rn(x[2 * i], x[2 * i + 1]);
+            const float r = scale != 1.f ? __fmul_rn(x[0], scale) : x[0];   // scaled only at the root
+            out[g * int64_t(H) + int64_t(v) * 8 + w] = r;
+        }
+        return;
+    }
+    // a partial group (the last of a pass): the pair results, level by level:
+    // element i of the next level is
     // (2i) + (2i + 1), an odd last element carried up unchanged; warp i forms
     // element i (operands into registers, barrier, store, barrier)
     for (int n = (m + 1) / 2; n > 1; n = (n + 1) / 2) {    // uniform across the CTA
