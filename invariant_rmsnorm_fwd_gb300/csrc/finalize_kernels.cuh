@@ -31,11 +31,12 @@ __global__ void ws_begin_kernel(WsView ws) {
 // reduces inputs [32g, 32g+32) for the 32 vectors (256 columns) of chunk c:
 // lane l owns vector 32c+l, so every load of a warp is one contiguous 512-byte
 // row piece.  Warp w forms inputs 2w and 2w+1 and adds them (level 1); the 16
-// pair results go through shared memory and are added level by level (levels
-// 2-5), warp i forming element i of each level.  Pairs are added only when
-// their right half is non-empty, which is the pairwise tree with odd carry
-// restricted to an aligned group of 32; later passes reduce the group results
-// the same way.
+// pair results go through shared memory, and levels 2-5 are added in
+// registers by 8 warps (one column of the 32 vectors each) for a full group,
+// level by level by the CTA's warps for the last, partial group of a pass.
+// Pairs are added only when their right half is non-empty, which is the
+// pairwise tree with odd carry restricted to an aligned group of 32; later
+// passes reduce the group results the same way.
 // In the first pass (from_blocks) an input is a block partial: the four
 // quarter partials as (q0 + q1) + (q2 + q3) (levels 5 and 6 of the 64-leaf
 // tree), a whole-block partial as is, or, for a block cut by a call boundary,
@@ -112,92 +113,121 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_pass_kernel(WsView ws, c
     const bool has_vec = v < V;
     const int64_t g = blockIdx.x;
     const int m = int(min64(32, n_in - g * 32));          // inputs in this group
+    // Everything the warp reads first is requested before any of it is used:
+    // the states of the group's inputs (one per lane) and, for each of the
+    // warp's two inputs, its four partial slots (the quarters of a block, or
+    // its whole partial in slot 0; for a cut block they are read again below)
+    // or the group result of the previous pass.  The slots lie inside the
+    // workspace whatever the state says, so nothing waits on the state.
+    const int64_t base = (from_blocks ? block_base : 0) + g * 32;
+    uint32_t st_lane = kStateWhole;
+    if (from_blocks && lane < m) st_lane = reinterpret_cast<const uint32_t *>(ws.block_state)[base + lane];
+    float slot[2][4][8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = 2 * w + h;
+        if (i < m && has_vec) {
+            if (from_blocks) {
+                const float *src = ws.block_partial + (base + i) * 4 * int64_t(H) + int64_t(v) * 8;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) load8(src + k * int64_t(H), slot[h][k]);
+            } else {
+                load8(in + (base + i) * int64_t(H) + int64_t(v) * 8, slot[h][0]);
+            }
+        }
+    }
+    const uint32_t states[2] = {__shfl_sync(kFull, st_lane, 2 * w), __shfl_sync(kFull, st_lane, 2 * w + 1)};
     if (from_blocks && !header_ok(ws)) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) set_status(ws.hdr, kStHeader);
         return;                                          // uniform across the CTA
     }
-    float pair[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) pair[c] = 0.f;
+    // The inputs that the slots already give (the previous pass's results,
+    // whole blocks, blocks that arrived as quarters or eighths) first, so that
+    // the slots are dead before a cut block, which is rebuilt from scratch,
+    // needs its registers.
+    float val[2][8];
+    bool cut[2] = {false, false};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const int i = 2 * w + h;
-        if (i >= m) break;                               // uniform per warp
-        const int64_t b = (from_blocks ? block_base : 0) + g * 32 + i;
-        float val[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) val[c] = 0.f;
-        const uint32_t state = from_blocks ? reinterpret_cast<const uint32_t *>(ws.block_state)[b] : kStateWhole;
-        if (!from_blocks) {
-            if (has_vec) load8(in + b * int64_t(H) + int64_t(v) * 8, val);
+        for (int c = 0; c < 8; ++c) val[h][c] = 0.f;
+        const int i = 2 * w + h;
+        if (i >= m) continue;                            // uniform per warp
+        const int64_t b = base + i;
+        const uint32_t state = states[h];
+        if (!from_blocks || state == kStateWhole) {
+            if (has_vec) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) val[h][c] = slot[h][0][c];
+            }
         } else if (quarter_state(state)) {
             if (has_vec) {
-                float q0[8], q1[8], q2[8], q3[8];
-                const float *src = ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8;
                 const float *src2 = ws.eighth + b * 4 * int64_t(H) + int64_t(v) * 8;
-                load8(src, q0);
-                load8(src + H, q1);
-                load8(src + 2 * int64_t(H), q2);
-                load8(src + 3 * int64_t(H), q3);
                 // a quarter that arrived as two eighths: the halves make level 4
-                add_second_eighth(state, 0, src2, q0);
-                add_second_eighth(state, 1, src2 + H, q1);
-                add_second_eighth(state, 2, src2 + 2 * int64_t(H), q2);
-                add_second_eighth(state, 3, src2 + 3 * int64_t(H), q3);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) val[c] = __fadd_rn(__fadd_rn(q0[c], q1[c]), __fadd_rn(q2[c], q3[c]));
+                for (int k = 0; k < 4; ++k) add_second_eighth(state, k, src2 + k * int64_t(H), slot[h][k]);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    val[h][c] = __fadd_rn(__fadd_rn(slot[h][0][c], slot[h][1][c]), __fadd_rn(slot[h][2][c], slot[h][3][c]));
             }
-        } else if (state == kStateWhole) {
-            if (has_vec) load8(ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8, val);
         } else {
-            // a block cut by a call boundary: each quarter arrived as a partial
-            // (byte 1), as two eighth partials (byte 12), or as spilled rows
-            // (byte 0), which each lane rebuilds for its own 8-column vector;
-            // then the block is (q0 + q1) + (q2 + q3) as in the other paths
-            const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
-            bool bad = false;
+            cut[h] = true;
+        }
+    }
 #pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (!cut[h]) continue;                           // uniform per warp
+        const int64_t b = base + 2 * w + h;
+        const uint32_t state = states[h];
+        float (&out8)[8] = val[h];
+        // a block cut by a call boundary: each quarter arrived as a partial
+        // (byte 1), as two eighth partials (byte 12), or as spilled rows
+        // (byte 0), which each lane rebuilds for its own 8-column vector;
+        // then the block is (q0 + q1) + (q2 + q3) as in the other paths
+        const int64_t rows = min64(kBlockRows, ws.n_rows - b * kBlockRows);
+        bool bad = false;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t by = (state >> (8 * q)) & 0xffu;
+            bad |= by != 0 && by != kStateQuarter && by != (kStateEighth0 | kStateEighth1);
+        }
+        bool missing = bad;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int r = 2 * lane + k;
+            if (r < rows && ((state >> (8 * (r / 16))) & 0xffu) == 0 && ws.leaf_flag[b * kBlockRows + r] == 0)
+                missing = true;
+        }
+        if (__any_sync(kFull, missing) && lane == 0 && blockIdx.y == 0) set_status(ws.hdr, kStMissing);
+        if (has_vec) {
+            const float *part = ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8;
+            const float *part2 = ws.eighth + b * 4 * int64_t(H) + int64_t(v) * 8;
+            const float *src = ws.spill + b * kBlockRows * int64_t(H) + int64_t(v) * 8;
+            float h0[8], acc[8];
+#pragma unroll 1
             for (int q = 0; q < 4; ++q) {
                 const uint32_t by = (state >> (8 * q)) & 0xffu;
-                bad |= by != 0 && by != kStateQuarter && by != (kStateEighth0 | kStateEighth1);
-            }
-            bool missing = bad;
+                float qv[8];
+                if (by == kStateQuarter) {
+                    load8(part + q * int64_t(H), qv);
+                } else if (by == (kStateEighth0 | kStateEighth1)) {
+                    load8(part + q * int64_t(H), qv);
+                    add_second_eighth(state, q, part2 + q * int64_t(H), qv);
+                } else {
+                    quarter_from_spill(src, H, q, rows, qv);
+                }
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int r = 2 * lane + k;
-                if (r < rows && ((state >> (8 * (r / 16))) & 0xffu) == 0 && ws.leaf_flag[b * kBlockRows + r] == 0)
-                    missing = true;
-            }
-            if (__any_sync(kFull, missing) && lane == 0 && blockIdx.y == 0) set_status(ws.hdr, kStMissing);
-            if (has_vec) {
-                const float *part = ws.block_partial + b * 4 * int64_t(H) + int64_t(v) * 8;
-                const float *part2 = ws.eighth + b * 4 * int64_t(H) + int64_t(v) * 8;
-                const float *src = ws.spill + b * kBlockRows * int64_t(H) + int64_t(v) * 8;
-                float h0[8], acc[8];
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t by = (state >> (8 * q)) & 0xffu;
-                    float qv[8];
-                    if (by == kStateQuarter) {
-                        load8(part + q * int64_t(H), qv);
-                    } else if (by == (kStateEighth0 | kStateEighth1)) {
-                        load8(part + q * int64_t(H), qv);
-                        add_second_eighth(state, q, part2 + q * int64_t(H), qv);
-                    } else {
-                        quarter_from_spill(src, H, q, rows, qv);
-                    }
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        if (q == 0 || q == 2) acc[c] = qv[c];
-                        else if (q == 1) h0[c] = __fadd_rn(acc[c], qv[c]);
-                        else val[c] = __fadd_rn(h0[c], __fadd_rn(acc[c], qv[c]));
-                    }
+                for (int c = 0; c < 8; ++c) {
+                    if (q == 0 || q == 2) acc[c] = qv[c];
+                    else if (q == 1) h0[c] = __fadd_rn(acc[c], qv[c]);
+                    else out8[c] = __fadd_rn(h0[c], __fadd_rn(acc[c], qv[c]));
                 }
             }
         }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) pair[c] = h == 0 ? val[c] : __fadd_rn(pair[c], val[c]);
     }
+    float pair[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) pair[c] = 2 * w + 1 < m ? __fadd_rn(val[0][c], val[1][c]) : val[0][c];
 #pragma unroll
     for (int c = 0; c < 8; ++c) part[w][c][lane] = pair[c];
     if (m == 32) {
