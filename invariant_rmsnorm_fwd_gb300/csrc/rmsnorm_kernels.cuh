@@ -174,10 +174,12 @@ constexpr int kMaxBatch = 8;                     // rows per pipeline stage <= 8
 // memory: each sends its partials to every CTA of the cluster with st.async,
 // counted in bytes on that CTA's exchange barrier of the stage, then waits
 // for all K slices on its own.
-// No CTA-wide barrier is used after set-up.  Rows of the dweight modes are
-// processed in 16-row units (a quarter of a logical block): the column warps
-// reduce the unit's 16 leaves with the 64-leaf tree's lower four levels and
-// store the quarter partial; dweight_finalize adds the four quarters.
+// No CTA-wide barrier is used in the streaming loop (the shapes that hold
+// tensor memory meet once more at the end, before it is freed).  Rows of the
+// dweight modes are processed in 16-row units (a quarter of a logical block):
+// the column warps reduce the unit's 16 leaves with the 64-leaf tree's lower
+// four levels and store the quarter partial; dweight_finalize adds the four
+// quarters.
 //
 // Row sums (this family's canonical tree, which depends on H only): in each
 // slice, lane l folds vectors l, l+32, l+64, ... in order, columns
