@@ -330,6 +330,10 @@ class Step:
         """The forward launches of one step alone."""
         self._fan(self.fwd_call, stream)
 
+    def fin_phase(self, stream):
+        """The finalize of one step alone (over the workspace of the last backward)."""
+        self.finalize(stream)
+
     def _lanes(self, stream):
         import torch
         if len(self.calls) == 1:
@@ -412,12 +416,13 @@ def time_bwd_kernel(step_objs, stream, reps, flush):
 def time_phase(multi, stream, reps, flush, which="bwd"):
     """Duration of one phase of a step as it runs inside the step: every forward
     ("fwd") or fused-backward ("bwd") launch of every normed tensor (all calls
-    of a many-call layout, forked over the step's streams), captured as one
-    CUDA graph and replayed between two CUDA events on the launching stream.
-    For the backward each workspace is begun (eagerly, outside the events);
-    L2 is flushed before each replay."""
+    of a many-call layout, forked over the step's streams), or the finalize
+    ("fin") of each workspace over what the last backward left in it,
+    captured as one CUDA graph and replayed between two CUDA events on the
+    launching stream.  For the backward each workspace is begun (eagerly,
+    outside the events); L2 is flushed before each replay."""
     import torch
-    phase = multi.bwd_phase if which == "bwd" else multi.fwd_phase
+    phase = {"bwd": multi.bwd_phase, "fwd": multi.fwd_phase, "fin": multi.fin_phase}[which]
 
     def prep():
         if which == "bwd":
@@ -673,6 +678,9 @@ class Multi:
     def fwd_phase(self, stream):
         self._fork(stream, lambda s, st: s.fwd_phase(st))
 
+    def fin_phase(self, stream):
+        self._fork(stream, lambda s, st: s.fin_phase(st))
+
 
 def workload_data(wl, device, chain=False):
     """Logical inputs of every normed tensor of a workload: (rows per token, x, dy, w[, r, dres])."""
@@ -732,6 +740,7 @@ def measure(wl, lay, data, args, device, flush, stream, hbm_peak, dist=None, sam
     phase_ms = statistics.mean(time_phase(multi, stream, reps, flush, "bwd"))
     bwd_ms = time_bwd_kernel(steps, stream, 1 if len(lay.calls) > 16 else reps, flush)
     fwd_ms = time_phase(multi, stream, reps, flush, "fwd")
+    fin_ms = time_phase(multi, stream, reps, flush, "fin")
     heff = wl.hidden * sum(wl.heads)
     n_act = wl.n_tokens
     fwd_b, bwd_b = (8.0, 8.0) if args.chain else (4.0, 6.0)
@@ -746,7 +755,8 @@ def measure(wl, lay, data, args, device, flush, stream, hbm_peak, dist=None, sam
          "bwd_phase_ms": phase_ms, "bwd_alg_bytes": alg_bwd, "bwd_launches": bwd_launches,
          "bwd_gbs": alg_bwd / (phase_ms * 1e-3) / 1e9,
          "bwd_iso_launch_ms": iso_ms, "bwd_iso_gbs": alg_bwd / bwd_launches / (iso_ms * 1e-3) / 1e9,
-         "fwd_gbs": fwd_b * heff * n_act / (statistics.mean(fwd_ms) * 1e-3) / 1e9}
+         "fwd_gbs": fwd_b * heff * n_act / (statistics.mean(fwd_ms) * 1e-3) / 1e9,
+         "fin_phase_ms": statistics.mean(fin_ms)}
     return r, multi
 
 
@@ -817,6 +827,7 @@ def main():
         "hbm_gbs_step": round(m["hbm_gbs_step"], 1),
         "frac_step": round(m["frac_step"], 4),
         "fwd_gbs": round(m["fwd_gbs"], 1),
+        "fin_phase_ms": round(m["fin_phase_ms"], 5),
         "roofline": {"bound": "hbm", "kernel": kernel,
                      "achieved": round(m["bwd_gbs"], 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(m["bwd_gbs"] / hbm_peak, 4),
@@ -898,7 +909,8 @@ def main():
                           "hbm_gbs_step": round(mc["hbm_gbs_step"], 1), "frac_step": round(mc["frac_step"], 4),
                           "bwd_phase_ms": round(mc["bwd_phase_ms"], 5), "bwd_gbs": round(mc["bwd_gbs"], 1),
                           "bwd_frac": round(mc["bwd_gbs"] / hbm_peak, 4), "bwd_launches": mc["bwd_launches"],
-                          "fwd_gbs": round(mc["fwd_gbs"], 1), "gpu_launches_per_step": mc["launches"]}
+                          "fwd_gbs": round(mc["fwd_gbs"], 1), "fin_phase_ms": round(mc["fin_phase_ms"], 5),
+                          "gpu_launches_per_step": mc["launches"]}
             del mm, data
             torch.cuda.empty_cache()
         line["other_workloads"] = per_cfg
